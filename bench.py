@@ -1,0 +1,377 @@
+"""Benchmark of the GDN decode-step front: µs per launch and achieved HBM
+bandwidth at 1..16 rows on one GB300, through the C ABI.
+
+A step is one launch of the whole path (residual add + norm, in_proj_qkvz /
+in_proj_ba, conv update, gates, gated delta rule, gated norm) over one batch
+of rows. Launches are replayed from a CUDA graph; every launch reads another
+copy of the layer weights (the copies together exceed L2) and another set of
+state slots, so each launch streams its weights and state from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--rows R] [--workload shard]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode-block µs/launch and achieved HBM GB/s (% of peak) at rows 1–16"
+PAGES_NOTE = ("pages report 13.3-34.7 µs/launch at 1-16 rows on MI355X TP8 with MXFP4 weights "
+              "(other hardware and format: context only)")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="shard")
+    ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
+    ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width table")
+    ap.add_argument("--engine", default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_inputs(shape, rows, seed):
+    import torch
+    from gated_deltanet_layer_gb300 import workloads as WL
+    w = WL.make_weights(shape, seed)
+    st = WL.make_state(shape, seed + 1)
+    stp = WL.make_step(shape, rows, seed + 2)
+    f64 = lambda t: None if t is None else (t.numpy() if t.dtype == torch.uint8 else t.to(torch.float64).numpy())
+    return (f64(stp["x"]), f64(stp["residual"]), {k: f64(v) for k, v in w.items()},
+            stp["state_indices"].numpy(), f64(st["conv_state"]), f64(st["ssm_state"]))
+
+
+def cpu_child(args):
+    """Time the oracle (as it stands) for about --cpu-seconds; print a JSON line."""
+    from gated_deltanet_layer_gb300 import workloads as WL
+    from oracle import gdn_oracle as O
+    shape = WL.SHAPES[args.workload]
+    x, res, w, idx, conv, ssm = oracle_inputs(shape, args.rows, 777)
+    n, t0 = 0, time.perf_counter()
+    limit = args.steps if args.impl == "reference" else None
+    while True:
+        O.gdn_step(shape, x, res, w, idx, conv, ssm)
+        n += 1
+        el = time.perf_counter() - t0
+        if (limit is not None and n >= limit) or (limit is None and el >= args.cpu_seconds):
+            break
+    print(json.dumps({"n": n, "seconds": el, "us_per_step": el / n * 1e6}))
+
+
+def run_cpu_baseline(args, steps=None, seconds=None):
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", args.workload,
+           "--rows", str(args.rows), "--cpu-seconds", str(seconds or args.cpu_seconds)]
+    if steps is not None:
+        cmd += ["--impl", "reference", "--steps", str(steps)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d, cores
+
+
+# ----------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = sorted(sm)
+        med = busy[len(busy) // 2]
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def native(args):
+    import torch
+    from gated_deltanet_layer_gb300 import GdnDecode, workloads as WL
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    shape = WL.SHAPES[args.workload]
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    peak, peak_kind = peaks()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + rank)
+
+    # Weight copies: together at least 3x L2, so no launch finds its weights in L2.
+    wbytes = shape.weight_bytes()
+    ncopy = max(4, int((3 * l2 + wbytes - 1) // wbytes) + 1)
+
+    def bf16(*s, std):
+        return (torch.randn(*s, generator=g, device="cuda") * std).to(torch.bfloat16)
+
+    H, Hv = shape.hidden, shape.num_v_heads
+    copies = []
+    for _ in range(ncopy):
+        copies.append({
+            "input_norm_w": bf16(H, std=0.1),
+            "qkvz": bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None,
+            "ba": bf16(shape.n_ba, H, std=0.02),
+            "conv_w": bf16(shape.conv_channels, shape.conv_kernel, std=0.02),
+            "A_log": -2.0 * torch.rand(Hv, generator=g, device="cuda"),
+            "dt_bias": bf16(Hv, std=0.5),
+            "gated_norm_w": bf16(shape.head_v_dim, std=0.1),
+        })
+    sdt = torch.bfloat16 if shape.ssm_dtype == "bf16" else torch.float32
+    conv = bf16(shape.num_slots, shape.conv_channels, shape.conv_kernel - 1, std=1.0)
+    ssm = (torch.randn(shape.num_slots, Hv, shape.head_v_dim, shape.head_k_dim, generator=g,
+                       device="cuda") * 0.1).to(sdt)
+    layer = GdnDecode(shape, engine=args.engine)
+    wstructs = [layer.weights_struct(c) for c in copies]
+
+    def make_batch(rows, n):
+        """n distinct step inputs of `rows` rows with fresh random slots each."""
+        out = []
+        for _ in range(n):
+            perm = torch.randperm(shape.num_slots - 1, generator=g, device="cuda")[:rows] + 1
+            out.append((bf16(rows, H, std=1.0), bf16(rows, H, std=1.0), perm.to(torch.int32).contiguous(),
+                        torch.empty(rows, Hv * shape.head_v_dim, dtype=torch.bfloat16, device="cuda"),
+                        torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")))
+        return out
+
+    def capture(rows, n):
+        batch = make_batch(rows, min(n, 64))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            # one eager launch per input set first (lazy init outside capture)
+            x, r, i, c, ro = batch[0]
+            layer.step(x, r, copies[0], i, conv, ssm, c, ro, weights_struct=wstructs[0])
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(graph, stream=s):
+                for k in range(n):
+                    x, r, i, c, ro = batch[k % len(batch)]
+                    layer.step(x, r, copies[k % ncopy], i, conv, ssm, c, ro, weights_struct=wstructs[k % ncopy])
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return graph
+
+    def time_graph(graph):
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(st)
+        graph.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        return e0.elapsed_time(e1)  # ms
+
+    K, Wm = args.steps, args.warmup
+    clocks = Clocks(local)
+    # warm-up: W untimed steps
+    gw = capture(args.rows, max(3, Wm))
+    gw.replay()
+    torch.cuda.synchronize()
+    # headline: exactly K timed steps
+    gk = capture(args.rows, K)
+    ms = time_graph(gk)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us = ms * 1e3 / K
+    live = args.rows
+    bytes_launch = shape.launch_bytes(args.rows, live)
+    st, detail = layer.check()
+    if st != 0:
+        raise RuntimeError(f"device error word 0x{detail:08x}")
+
+    # per-width table (outside the headline timed region); each graph replayed
+    # for ~0.3 s so the clock sampler sees the GPU under load
+    table = {}
+    for wdt in [int(v) for v in args.widths.split(",") if v]:
+        gg = capture(wdt, 100)
+        times = []
+        t_end = time.time() + 0.3
+        while time.time() < t_end or len(times) < 5:
+            times.append(time_graph(gg) * 10.0)  # µs per launch
+        times.sort()
+        u = times[len(times) // 2]
+        b = shape.launch_bytes(wdt, wdt)
+        table[str(wdt)] = {"us": round(u, 3), "GBps": round(b / u / 1e3, 1),
+                           "frac_of_" + peak_kind: round(b / u / 1e3 / peak, 4), "bytes": b}
+    clk = clocks.stop()
+
+    # end to end through the public API with host buffers: per step, copy this
+    # step's inputs from pinned host memory, launch, read the outputs back
+    Bi = args.rows * H * 2 * 2 + args.rows * 4
+    Bo = args.rows * Hv * shape.head_v_dim * 2 + args.rows * H * 2
+    hx = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+    hr = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+    hi = torch.randperm(shape.num_slots - 1)[:args.rows].add(1).to(torch.int32).pin_memory()
+    hx.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
+    hr.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
+    hc = torch.empty(args.rows, Hv * shape.head_v_dim, dtype=torch.bfloat16).pin_memory()
+    ho = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+    dx, dr, di = torch.empty_like(hx, device="cuda"), torch.empty_like(hr, device="cuda"), torch.empty_like(hi, device="cuda")
+    dc, do = torch.empty_like(hc, device="cuda"), torch.empty_like(ho, device="cuda")
+
+    def e2e_step(k):
+        dx.copy_(hx, non_blocking=True)
+        dr.copy_(hr, non_blocking=True)
+        di.copy_(hi, non_blocking=True)
+        layer.step(dx, dr, copies[k % ncopy], di, conv, ssm, dc, do, weights_struct=wstructs[k % ncopy])
+        hc.copy_(dc, non_blocking=True)
+        ho.copy_(do, non_blocking=True)
+
+    for k in range(max(3, Wm)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    st0 = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st0)
+    for k in range(K):
+        e2e_step(k)
+    e1.record(st0)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1e3 / K
+
+    n_ctas, engine = layer.launch_info(args.rows)
+    result = {
+        "metric": METRIC, "value": round(us, 3), "unit": "µs/launch", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 math, " + shape.ssm_dtype + " state",
+        "data": "synthetic (seeded random weights and states of the layer's shapes)",
+        "config": {"workload": f"{shape.name}: H={H} Hk={shape.num_k_heads} Hv={Hv} dk=dv={shape.head_k_dim} "
+                               f"slots={shape.num_slots} {shape.ssm_dtype} state, bf16 in_proj",
+                   "rows": args.rows, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: weights rotated over {ncopy} copies "
+                         f"({ncopy * wbytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2), fresh slots per launch",
+                   "timing": "CUDA graph of K launches, CUDA events on the launching stream",
+                   "grid": n_ctas, "engine": engine},
+        "achieved_GBps": round(bytes_launch / us / 1e3, 1),
+        "widths": table,
+        "roofline": {"bound": "hbm", "achieved": round(bytes_launch / us / 1e3, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(bytes_launch / us / 1e3 / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": bytes_launch},
+        "e2e": {"value": round(e2e_us, 3), "unit": "µs/launch", "h2d_bytes_per_step": Bi,
+                "d2h_bytes_per_step": Bo, "how": "eager gdn_decode_step via the Python binding with "
+                                                 "pinned-host copies in and out each step"},
+        "gpu_launches": K,
+        "clocks": clk,
+        "context": PAGES_NOTE,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        d, cores = run_cpu_baseline(args)
+        result["cpu_baseline"] = {"value": round(d["us_per_step"], 1), "unit": "µs/launch", "cores": cores,
+                                  "kind": "oracle", "sample": f"{d['n']} oracle steps of the same workload "
+                                  f"({args.rows} rows) in {d['seconds']:.1f} s, float64 numpy"}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gated_deltanet_layer_gb300 import workloads as WL
+    shape = WL.SHAPES[args.workload]
+    # warm-up steps are not timed
+    run_cpu_baseline(args, steps=max(1, args.warmup))
+    d, cores = run_cpu_baseline(args, steps=args.steps)
+    v = round(d["us_per_step"], 1)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "µs/launch", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{shape.name}", "rows": args.rows},
+        "cpu_baseline": {"value": v, "unit": "µs/launch", "cores": cores, "kind": "oracle",
+                         "sample": f"{d['n']} oracle steps ({args.rows} rows) in {d['seconds']:.1f} s"},
+        "e2e": {"value": v, "unit": "µs/launch", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.cpu_child:
+        cpu_child(args)
+    elif args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+// Shared definitions of the GDN decode-step kernels: launch parameters,
+// workspace layout, bf16 helpers, release/acquire counters and bounded waits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kThreads = 512;              // one persistent CTA per SM
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRows = 16;               // rows of one decode step
+constexpr int kTileM = 128;                // projection rows per tile
+constexpr int kKStep = 64;                 // projection columns per work unit
+constexpr int kMaxCtas = 256;
+constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
+constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
+
+// Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
+constexpr uint32_t kStatusDeadline = 4;
+constexpr uint32_t kStatusIndex = 5;
+constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3;
+
+constexpr int kDebugSkipNormPublish = 0x1;
+
+// Workspace header: counters on separate 128-byte lines. Every counter only
+// grows; launch L waits for (L+1) * arrivals, so nothing is reset between
+// launches.
+struct WsCounters {
+  unsigned long long norm_arrive;   // +1 per CTA once its norm partials are out
+  unsigned long long pad0[15];
+  unsigned long long xn_arrive;     // +1 per CTA once its normed columns are out
+  unsigned long long pad1[15];
+  unsigned int error;               // sticky error word
+  unsigned int pad2[63];
+  unsigned long long tile_arrive[kMaxTiles];  // +1 per contributor of a tile
+  unsigned long long tile_done[kMaxTiles];    // +1 when the tile's epilogue is out
+};
+
+struct StepParams {
+  // shapes
+  int H, Hk, Hv, dk, dv, C, Nqkvz, Nba, num_slots, rows;
+  int group;           // Hv / Hk
+  int tiles_qkvz;      // Nqkvz / 128
+  int num_tiles;       // tiles_qkvz + ceil(Nba / 128)
+  int ksteps;          // H / 64
+  int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
+  int max_contrib;     // most CTAs contributing to one tile
+  int num_ctas;
+  float norm_eps, gnorm_eps, l2_eps, q_scale;
+  unsigned long long deadline_ns;
+  int debug_flags;
+  // step tensors
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* res;   // nullptr: first layer
+  __nv_bfloat16* res_out;
+  __nv_bfloat16* core_out;
+  const int* idx;
+  __nv_bfloat16* conv_state;
+  void* ssm_state;
+  // weights
+  const __nv_bfloat16* w_in;
+  const __nv_bfloat16* w_qkvz;
+  const uint8_t* w_qkvz_scales;
+  const __nv_bfloat16* w_ba;
+  const __nv_bfloat16* conv_w;
+  const float* A_log;
+  const __nv_bfloat16* dt_bias;
+  const __nv_bfloat16* gnorm_w;
+  // workspace
+  WsCounters* ctr;
+  float* norm_part;        // [kMaxRows][num_ctas]
+  __nv_bfloat16* xn;       // [kMaxRows][H]
+  float* proj_part;        // [num_tiles][max_contrib][kMaxRows][128]
+  float* act;              // [kMaxRows][Nqkvz]: q^, k^ (normalised), v (conv out), z
+  float* act_ba;           // [kMaxRows][Nba]: b, a (bf16-rounded projections)
+  // stream-K plan of the projection work units (unit = tile * ksteps + kstep)
+  // CTA c takes units [unit_begin[c], unit_begin[c+1]). Its partial of the
+  // first tile it touches goes to slot cta_slot0[c] of that tile; it is the
+  // first contributor (slot 0) of every later tile it touches. Tile t has
+  // tile_num_ctas[t] contributors.
+  int unit_begin[kMaxCtas + 1];
+  unsigned char cta_slot0[kMaxCtas];
+  unsigned char tile_num_ctas[kMaxTiles];
+};
+
+// ------------------------------------------------------------------ bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ uint16_t f_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)f_to_bf16_bits(lo) | ((uint32_t)f_to_bf16_bits(hi) << 16);
+}
+__device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+// ------------------------------------------------------------------ memory
+
+// Streamed once per launch: read-only, keep out of L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+// Written by other CTAs during this launch: read at L2.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float ld_cg_f(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Release add: every write of this thread (and, after a bar.sync, of its CTA)
+// before the add is visible to a thread that acquires the new value.
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p,
+                                                                   unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long long* p,
+                                                                   unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void record_error(WsCounters* c, uint32_t status, uint32_t wait_id,
+                                             uint32_t who) {
+  uint32_t word = (status << 24) | ((wait_id & 0xff) << 16) | (who & 0xffff);
+  atomicCAS(&c->error, 0u, word);  // the first error wins
+}
+
+// Spin (one thread) until *ctr >= target. Gives up after the deadline, or at
+// once when another CTA recorded a deadline error; returns false then. An
+// iteration cap backs up the timer.
+static __device__ __noinline__ bool wait_counter(const StepParams& p, const unsigned long long* ctr,
+                                          unsigned long long target, uint32_t wait_id) {
+  if (ld_acquire_u64(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long cap = p.deadline_ns / 32 + 4096;
+  unsigned ns = 32;
+  for (unsigned long long it = 0;; ++it) {
+    __nanosleep(ns);
+    if (ns < 64) ns <<= 1;
+    if (ld_acquire_u64(ctr) >= target) return true;
+    if ((ld_relaxed_u32(&p.ctr->error) >> 24) == kStatusDeadline) return false;
+    if (globaltimer_ns() - t0 > p.deadline_ns || it > cap) {
+      record_error(p.ctr, kStatusDeadline, wait_id, blockIdx.x);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float t) { return t / (1.0f + expf(-t)); }
+
+}  // namespace gdn

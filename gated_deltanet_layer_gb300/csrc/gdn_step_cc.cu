@@ -1,0 +1,167 @@
+// GDN decode-step launch with the projections on CUDA cores (f32 FMA dot
+// products of bf16 weights and the bf16 normed input).
+//
+// One persistent CTA per SM runs, in order: the residual add and its norm
+// partials, the normed input image, its share of the in_proj_qkvz/in_proj_ba
+// work units (a stream-K split of (128-row tile, 64-column step) units, so
+// every CTA streams the same number of weight bytes), the epilogues of the
+// tiles it finishes last, and its share of the (row, value head) recurrence
+// tasks. Cross-CTA hand-offs go through release/acquire counters with bounded
+// waits (vLLM #60833, Claims and Limitations: every wait is bounded and a
+// failed wait leaves a sticky failed word).
+#include "gdn_kernels.h"
+#include "gdn_phases.cuh"
+
+namespace gdn {
+
+__device__ __forceinline__ const __nv_bfloat16* weight_row(const StepParams& p, int t, int r, bool& valid) {
+  if (t < p.tiles_qkvz) {
+    valid = true;
+    return p.w_qkvz + (size_t)(t * kTileM + r) * p.H;
+  }
+  const int n = (t - p.tiles_qkvz) * kTileM + r;
+  valid = n < p.Nba;
+  return p.w_ba + (size_t)(valid ? n : 0) * p.H;
+}
+
+// Projection engine on CUDA cores. Thread (row = tid/4, sub = tid%4) owns one
+// weight row of the current tile and 16 of the 64 columns of each unit; its
+// f32 sums over the CTA's units of one tile are combined over the 4 lanes of
+// the row and written as this CTA's partial of the tile.
+static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
+                                     float (*xs)[kMaxRows][kKStep], int L) {
+  const int cta = blockIdx.x, tid = threadIdx.x, W = p.rows;
+  const int ub = p.unit_begin[cta], ue = p.unit_begin[cta + 1];
+  if (ub >= ue) return true;
+  if (tid == 0)
+    sm.flag = wait_counter(p, &p.ctr->xn_arrive, (unsigned long long)(L + 1) * p.num_ctas, kWaitXn);
+  __syncthreads();
+  if (!sm.flag) return false;
+
+  const int row = tid >> 2, sub = tid & 3;
+  auto stage = [&](int u, int buf) {
+    if (tid < W * 8) {
+      const int ks = u % p.ksteps;
+      const int w = tid >> 3, c = (tid & 7) * 8;
+      const uint4 v = ld_cg_v4(p.xn + (size_t)w * p.H + ks * kKStep + c);
+      float4* d = reinterpret_cast<float4*>(&xs[buf][w][c]);
+      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    }
+  };
+  auto wload = [&](int u, uint4& a, uint4& b) {
+    const int t = u / p.ksteps, ks = u - t * p.ksteps;
+    bool valid;
+    const __nv_bfloat16* rp = weight_row(p, t, row, valid);
+    if (valid) {
+      const __nv_bfloat16* q = rp + ks * kKStep + sub * 16;
+      a = ld_stream_v4(q);
+      b = ld_stream_v4(q + 8);
+    } else {
+      a = make_uint4(0, 0, 0, 0);
+      b = a;
+    }
+  };
+
+  float acc[kMaxRows];
+#pragma unroll
+  for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
+
+  auto flush = [&](int t) {
+#pragma unroll
+    for (int w = 0; w < kMaxRows; ++w) {
+      float v = acc[w];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      acc[w] = v;
+    }
+    const int j = (t == ub / p.ksteps) ? p.cta_slot0[cta] : 0;
+    float* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
+    if (sub == 0) {
+#pragma unroll
+      for (int w = 0; w < kMaxRows; ++w)
+        if (w < W) dst[w * kTileM + row] = acc[w];
+    }
+#pragma unroll
+    for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
+    deliver_tile_partial(p, sm, t, L);
+  };
+
+  constexpr int D = 4;  // units of weights in flight per thread
+  uint4 wa[D], wb[D];
+#pragma unroll
+  for (int j = 0; j < D; ++j)
+    if (ub + j < ue) wload(ub + j, wa[j], wb[j]);
+  stage(ub, 0);
+  __syncthreads();
+
+  int cur = ub / p.ksteps;
+  for (int u0 = ub; u0 < ue; u0 += D) {
+#pragma unroll
+    for (int j = 0; j < D; ++j) {
+      const int u = u0 + j;
+      if (u < ue) {
+        const int t = u / p.ksteps;
+        if (t != cur) {
+          flush(cur);
+          cur = t;
+        }
+        if (u + 1 < ue) stage(u + 1, (u + 1 - ub) & 1);
+        const float(*x)[kKStep] = xs[(u - ub) & 1];
+        float wv[16];
+        const uint32_t ws_[8] = {wa[j].x, wa[j].y, wa[j].z, wa[j].w, wb[j].x, wb[j].y, wb[j].z, wb[j].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wv[2 * e] = bf16_lo(ws_[e]);
+          wv[2 * e + 1] = bf16_hi(ws_[e]);
+        }
+#pragma unroll
+        for (int w = 0; w < kMaxRows; ++w) {
+          if (w < W) {
+            const float4* xr = reinterpret_cast<const float4*>(&x[w][sub * 16]);
+            const float4 x0 = xr[0], x1 = xr[1], x2 = xr[2], x3 = xr[3];
+            float s = acc[w];
+            s = fmaf(wv[0], x0.x, s);   s = fmaf(wv[1], x0.y, s);
+            s = fmaf(wv[2], x0.z, s);   s = fmaf(wv[3], x0.w, s);
+            s = fmaf(wv[4], x1.x, s);   s = fmaf(wv[5], x1.y, s);
+            s = fmaf(wv[6], x1.z, s);   s = fmaf(wv[7], x1.w, s);
+            s = fmaf(wv[8], x2.x, s);   s = fmaf(wv[9], x2.y, s);
+            s = fmaf(wv[10], x2.z, s);  s = fmaf(wv[11], x2.w, s);
+            s = fmaf(wv[12], x3.x, s);  s = fmaf(wv[13], x3.y, s);
+            s = fmaf(wv[14], x3.z, s);  s = fmaf(wv[15], x3.w, s);
+            acc[w] = s;
+          }
+        }
+        if (u + D < ue) wload(u + D, wa[j], wb[j]);
+        __syncthreads();
+      }
+    }
+  }
+  flush(cur);
+  return true;
+}
+
+template <bool HAS_RES, bool STATE_BF16, int DK>
+__global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_constant__ StepParams p) {
+  __shared__ SmemPhases sm;
+  __shared__ __align__(16) float xs[2][kMaxRows][kKStep];
+  if (threadIdx.x == 0) sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
+  __syncthreads();
+  if (!sm.flag) return;  // sticky error: every later launch returns at once
+  phase_norm_partials<HAS_RES>(p, sm);
+  const int L = sm.L;
+  if (!phase_normed_input(p, sm, L)) return;
+  if (!phase_proj_cuda_core(p, sm, xs, L)) return;
+  phase_recurrence<DK, STATE_BF16>(p, sm, L);
+}
+
+const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk) {
+#define GDN_PICK(R, B, D) \
+  if (has_res == R && state_bf16 == B && dk == D) return (const void*)&gdn_step_cc_kernel<R, B, D>;
+  GDN_PICK(true, false, 128) GDN_PICK(true, true, 128) GDN_PICK(false, false, 128) GDN_PICK(false, true, 128)
+  GDN_PICK(true, false, 64) GDN_PICK(true, true, 64) GDN_PICK(false, false, 64) GDN_PICK(false, true, 64)
+#undef GDN_PICK
+  return nullptr;
+}
+
+}  // namespace gdn

@@ -1,0 +1,126 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every
+symbol the header declares; argument errors come back before any launch.
+No kernel runs here (no GPU is needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gated_deltanet_layer_gb300 import _native, build as B, make_config
+from gated_deltanet_layer_gb300 import workloads as WL
+
+HEADER = os.path.join(B.ROOT, "include", "gdn_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_\w+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_binds():
+    assert declared_functions() == sorted(_native.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _native.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.gdn_status_string(code)
+    assert lib.gdn_status_string(99) == b"unknown status"
+
+
+def _cfg(**kw):
+    c = make_config(WL.SHARD)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value", [
+    ("max_rows", 0), ("max_rows", 17), ("hidden", 0), ("num_slots", 0), ("ssm_dtype", 7),
+    ("engine", 9), ("num_ctas", -1), ("norm_eps", float("nan")),
+])
+def test_invalid_config_has_no_workspace(lib, field, value):
+    c = _cfg(**{field: value})
+    assert lib.gdn_decode_workspace_bytes(ctypes.byref(c)) == 0
+
+
+@pytest.mark.parametrize("field,value", [
+    ("conv_kernel", 3), ("head_k_dim", 96), ("hidden", 8192 + 32), ("num_k_heads", 3),
+])
+def test_unsupported_shapes_refused_at_create(lib, field, value):
+    c = _cfg(**{field: value})
+    h = ctypes.c_void_p()
+    st = lib.gdn_decode_create(ctypes.byref(c), ctypes.c_void_p(256), 1 << 30, None, ctypes.byref(h))
+    assert st in (_native.GDN_ERR_UNSUPPORTED, _native.GDN_ERR_ARG)
+    assert not h.value
+
+
+def test_create_and_step_argument_errors(lib):
+    c = _cfg()
+    assert lib.gdn_decode_create(ctypes.byref(c), None, 0, None, None) == _native.GDN_ERR_ARG
+    h = ctypes.c_void_p()
+    assert lib.gdn_decode_create(ctypes.byref(c), None, 1 << 20, None, ctypes.byref(h)) == _native.GDN_ERR_ARG
+    w = _native.Weights()
+    assert lib.gdn_decode_step(None, 1, None, None, ctypes.byref(w), None, None, None, None, None,
+                               None) == _native.GDN_ERR_ARG
+    assert lib.gdn_decode_check(None, None, None) == _native.GDN_ERR_ARG
+    assert lib.gdn_decode_reset(None, None) == _native.GDN_ERR_ARG
+    lib.gdn_decode_destroy(None)  # no-op
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(B.ROOT, "gated_deltanet_layer_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
+            if f.endswith((".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text, f
+
+
+@pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16])
+@pytest.mark.parametrize("G", [1, 7, 33, 148, 152, 160])
+def test_stream_k_plan_invariants(lib, shape, G):
+    """The units partition [0, U) in CTA order; each CTA's weight cost is within
+    one unit of the mean; every tile's contributor count equals the number of
+    CTAs with a unit in it, and their slots are 0..count-1 without repeats."""
+    cfg = make_config(shape)
+    if (shape.hidden + G - 1) // G > 256:
+        with pytest.raises(_native.GdnError):
+            _native.plan(cfg, G)
+        return
+    ub, slot0, tc, nt, ks = _native.plan(cfg, G)
+    U = nt * ks
+    assert ub[0] == 0 and ub[G] == U and all(a <= b for a, b in zip(ub, ub[1:]))
+    tq = shape.n_qkvz // 128
+    cost = lambda u: 128 if u // ks < tq else min(128, shape.n_ba - (u // ks - tq) * 128)
+    costs = [sum(cost(u) for u in range(ub[c], ub[c + 1])) for c in range(G)]
+    assert max(costs) - sum(costs) / G <= 128
+    slots = {t: [] for t in range(nt)}
+    for c in range(G):
+        if ub[c] == ub[c + 1]:
+            continue
+        t0, t1 = ub[c] // ks, (ub[c + 1] - 1) // ks
+        for t in range(t0, t1 + 1):
+            slots[t].append(slot0[c] if t == t0 else 0)
+    for t in range(nt):
+        assert tc[t] == len(slots[t]) >= 1
+        assert sorted(slots[t]) == list(range(tc[t]))

@@ -1,0 +1,80 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element,
+on seeded synthetic layers of every workload shape: widths 1..16, pad rows,
+the first-layer variant and the bf16 state."""
+import pytest
+import torch
+
+from gated_deltanet_layer_gb300 import GdnDecode, workloads as WL
+from gdn_harness import Case, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _run(shape, rows, seed, engine="auto", **kw):
+    case = Case(shape, rows, seed, **kw).to_device()
+    layer = GdnDecode(shape, engine=engine)
+    core, res_out = case.run_gpu(layer)
+    st, detail = layer.check()
+    assert st == 0, f"device error 0x{detail:08x}"
+    compare(case, case.run_oracle(), core, res_out)
+
+
+TINY32 = WL.TINY.with_(num_slots=32)
+
+
+@pytest.mark.parametrize("rows", [1, 2, 3, 5, 8, 13, 16])
+def test_tiny_layer(rows):
+    _run(TINY32, rows, 1000 + rows)
+
+
+@pytest.mark.parametrize("rows", [1, 4, 11, 16])
+def test_tiny_layer_pad_rows_and_first_layer(rows):
+    _run(TINY32, rows, 1100 + rows, first_layer=True, pad_rows=WL.default_pad_rows(rows))
+
+
+def test_tiny_layer_config_slots():
+    # the tiny workload as specified: 16 slots, one row
+    _run(WL.TINY, 1, 1200)
+
+
+@pytest.mark.parametrize("rows", [1, 2, 4, 8, 16])
+def test_shard_layer(rows):
+    _run(WL.SHARD, rows, 2000 + rows)
+
+
+@pytest.mark.parametrize("rows", [1, 3, 8, 9, 16])
+def test_shard_bf16_state_first_layer_with_pad_rows(rows):
+    _run(WL.SHARD_BF16, rows, 3000 + rows, first_layer=True, pad_rows=WL.default_pad_rows(rows))
+
+
+@pytest.mark.parametrize("rows", [3, 16])
+def test_shard_bf16_state_with_residual(rows):
+    _run(WL.SHARD_BF16, rows, 3100 + rows)
+
+
+@pytest.mark.parametrize("rows", [1, 16])
+def test_full_layer(rows):
+    _run(WL.FULL, rows, 4000 + rows)
+
+
+@pytest.mark.parametrize("shape", [TINY32, WL.SHARD])
+def test_strong_conv_weights_and_unit_q_scale(shape):
+    # conv weights ~N(0, 0.5) make the v path and the state update matter; q_scale = 1
+    _run(shape.with_(q_scale=1.0), 6, 5000, conv_std=0.5)
+
+
+def test_all_rows_pad():
+    shape = TINY32
+    case = Case(shape, 4, 5100)
+    case.step["state_indices"] = torch.tensor([0, -1, 0, -7], dtype=torch.int32)
+    case.to_device()
+    layer = GdnDecode(shape)
+    core, res_out = case.run_gpu(layer)
+    assert layer.check()[0] == 0
+    compare(case, case.run_oracle(), core, res_out)
