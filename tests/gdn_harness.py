@@ -1,7 +1,13 @@
 """Helpers shared by the parity tests: seeded inputs on host and device, the
 CUDA path through the C ABI, the CPU oracle on the same inputs, and the
 comparisons with the tolerances of the method's own checks (core cosine >=
-0.9999 as in sgl-amd-mono #89 "check mode": NUMERICS k1.core.cosine)."""
+0.9999 as in sgl-amd-mono #89 "check mode": NUMERICS k1.core.cosine).
+
+Why not bit-exact: the kernel sums the 8192-term projections in f32 in its own
+order, the oracle in float64. The absolute f32 accumulation error (~1e-5 at
+these magnitudes) can exceed one bf16 ulp of a near-zero projection output, so
+bf16 outputs are compared with absolute bars, and only order-free results
+(residual_out, pad rows, copied conv taps, untouched slots) bit for bit."""
 from __future__ import annotations
 
 import numpy as np
@@ -10,11 +16,16 @@ import torch
 from gated_deltanet_layer_gb300 import workloads as WL
 
 # Tolerances (core: cosine and max-abs; states: max-abs; residual_out and pad
-# handling: bit-exact). bf16 conv state: at most one bf16 ulp.
+# handling: bit-exact).
 CORE_COS = 0.9999
 CORE_MAX_ABS = 2e-2
 STATE_F32_MAX_ABS = 1e-3
 STATE_BF16_MAX_ABS = 1e-2
+# The conv state's new tap is the bf16 projection output: within one bf16 ulp
+# of the oracle's value (one rounding step either way), plus an absolute floor
+# that covers the f32 accumulation error of an 8192-term dot product near zero
+# (typical size 1e-5, floor 2e-3); and at most 2% of the taps may differ.
+CONV_NEW_TAP_FLOOR = 2e-3
 
 
 def f64(t):
@@ -95,8 +106,14 @@ def compare(case, ref, core, res_out, *, state_tol=None):
     np.testing.assert_array_equal(gconv[untouched], conv0[untouched], err_msg="untouched conv slots")
     np.testing.assert_array_equal(gssm[untouched], ssm0[untouched], err_msg="untouched ssm slots")
     if touched:
-        dconv = np.abs(gconv[touched] - ref["conv_state"][touched])
-        assert np.all(dconv <= bf16_ulp(ref["conv_state"][touched])), "conv state beyond 1 bf16 ulp"
+        # the two older taps are copies of the previous state: bit-exact; the
+        # new tap is the bf16 projection output: within the bf16-state bar
+        np.testing.assert_array_equal(gconv[touched][..., :-1], ref["conv_state"][touched][..., :-1],
+                                      err_msg="shifted conv taps")
+        g_new, r_new = gconv[touched][..., -1], ref["conv_state"][touched][..., -1]
+        excess = np.abs(g_new - r_new) - (bf16_ulp(r_new) + CONV_NEW_TAP_FLOOR)
+        assert np.all(excess <= 0), f"conv state new tap beyond 1 ulp + floor by {float(excess.max())}"
+        assert np.mean(g_new != r_new) <= 0.02, f"conv new tap mismatch rate {np.mean(g_new != r_new)}"
         tol = state_tol if state_tol is not None else (
             STATE_BF16_MAX_ABS if shape.ssm_dtype == "bf16" else STATE_F32_MAX_ABS)
         m = float(np.max(np.abs(gssm[touched] - ref["ssm_state"][touched])))
