@@ -16,12 +16,13 @@ GDN_STATE_F32, GDN_STATE_BF16 = 0, 1
 GDN_W_BF16, GDN_W_MXFP4 = 0, 1
 GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05 = 0, 1, 2
 GDN_DEBUG_SKIP_NORM_PUBLISH = 0x1
+GDN_DEBUG_TIMELINE = 0x2
 
 # Every symbol the header declares.
 EXPORTS = (
     "gdn_decode_workspace_bytes", "gdn_decode_create", "gdn_decode_step", "gdn_decode_check",
     "gdn_decode_reset", "gdn_decode_destroy", "gdn_status_string", "gdn_decode_launch_info",
-    "gdn_decode_plan",
+    "gdn_decode_plan", "gdn_decode_debug_timeline",
 )
 
 
@@ -77,24 +78,35 @@ def lib() -> ctypes.CDLL:
     L.gdn_decode_launch_info.restype = ctypes.c_int
     u8p = ctypes.POINTER(ctypes.c_uint8)
     i32p = ctypes.POINTER(ctypes.c_int32)
-    L.gdn_decode_plan.argtypes = [cfgp, i32, i32p, u8p, u8p, i32, i32p, i32p]
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    L.gdn_decode_plan.argtypes = [cfgp, i32, i32p, i32p, u8p, u16p, u8p, u8p, i32, i32p, i32p, i32p]
     L.gdn_decode_plan.restype = ctypes.c_int
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    L.gdn_decode_debug_timeline.argtypes = [vp, vp, u64p, i32, u64p, i32, i32p, i32p]
+    L.gdn_decode_debug_timeline.restype = ctypes.c_int
     _lib = L
     return L
 
 
-def plan(cfg: Config, num_ctas: int):
+def plan(cfg: Config, num_ctas: int) -> dict:
     """Stream-K plan of the projection units (host-only diagnostics)."""
     L = lib()
+    eng = ctypes.c_int32()
     ub = (ctypes.c_int32 * (num_ctas + 1))()
-    slot0 = (ctypes.c_uint8 * num_ctas)()
+    seg = (ctypes.c_uint8 * (num_ctas * 16))()
+    ksf = (ctypes.c_uint16 * num_ctas)()
+    nbs = (ctypes.c_uint8 * num_ctas)()
     cap = 4096
     tc = (ctypes.c_uint8 * cap)()
-    nt, ks = ctypes.c_int32(), ctypes.c_int32()
-    st = L.gdn_decode_plan(ctypes.byref(cfg), num_ctas, ub, slot0, tc, cap, ctypes.byref(nt), ctypes.byref(ks))
+    nt, ks, kb = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = L.gdn_decode_plan(ctypes.byref(cfg), num_ctas, ctypes.byref(eng), ub, seg, ksf, nbs, tc, cap,
+                           ctypes.byref(nt), ctypes.byref(ks), ctypes.byref(kb))
     if st != GDN_OK:
         raise GdnError("gdn_decode_plan", st)
-    return list(ub), list(slot0), list(tc[:nt.value]), nt.value, ks.value
+    return {"engine": eng.value, "unit_begin": list(ub),
+            "seg_slot": [list(seg[c * 16:(c + 1) * 16]) for c in range(num_ctas)],
+            "ks_first": list(ksf), "nb_slots": list(nbs), "tile_count": list(tc[:nt.value]),
+            "num_tiles": nt.value, "ksteps": ks.value, "kblock": kb.value}
 
 
 def status_string(code: int) -> str:

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <new>
+#include <vector>
 
 #include "../../include/gdn_decode.h"
 #include "gdn_kernels.h"
@@ -21,9 +22,12 @@ struct Layout {
 };
 
 struct Plan {
-  int G, tiles_qkvz, num_tiles, ksteps, norm_chunk, max_contrib;
+  int engine;  // GDN_ENGINE_CUDA_CORE or GDN_ENGINE_TCGEN05
+  int G, tiles_qkvz, num_tiles, ksteps, kblock, norm_chunk, max_contrib;
   int unit_begin[kMaxCtas + 1];
-  unsigned char cta_slot0[kMaxCtas];
+  unsigned char seg_slot[kMaxCtas][kMaxSegs];
+  unsigned short ks_first[kMaxCtas];
+  unsigned char nb_slots[kMaxCtas];
   unsigned char tile_count[kMaxTiles];
 };
 
@@ -37,6 +41,11 @@ struct gdn_decode {
   size_t ws_bytes;
   Layout lay;
   Plan plan;
+  // TMA maps of the last weights a step used
+  const void* map_qkvz_ptr;
+  const void* map_ba_ptr;
+  CUtensorMap map_qkvz;
+  CUtensorMap map_ba;
 };
 
 namespace {
@@ -64,70 +73,94 @@ gdn_status validate(const gdn_decode_config* c) {
   if (c->head_k_dim != c->head_v_dim) return GDN_ERR_UNSUPPORTED;
   if (c->head_k_dim != 64 && c->head_k_dim != 128) return GDN_ERR_UNSUPPORTED;
   if (c->num_v_heads % c->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+  if (c->num_v_heads % 2 != 0) return GDN_ERR_UNSUPPORTED;  // in_proj_ba rows come in fours
   if ((c->num_k_heads * c->head_k_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if ((c->num_v_heads * c->head_v_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if (c->hidden % kKStep != 0 || c->hidden > (1 << 20)) return GDN_ERR_UNSUPPORTED;
   if (c->qkvz_format == GDN_W_MXFP4) return GDN_ERR_UNSUPPORTED;
-  if (c->engine == GDN_ENGINE_TCGEN05) return GDN_ERR_UNSUPPORTED;
   const int tiles = n_qkvz(*c) / kTileM + (n_ba(*c) + kTileM - 1) / kTileM;
   if (tiles > kMaxTiles) return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
 }
 
 // Stream-K split of the projection units over G CTAs. A unit is one 64-column
-// step of one 128-row tile; a unit of a partial in_proj_ba tile costs its row
-// count, so every CTA streams about the same number of weight bytes. CTA c
-// takes units [unit_begin[c], unit_begin[c+1]).
-gdn_status make_plan(const gdn_decode_config& c, int G, Plan* pl) {
+// step (k-step) of one 128-row tile. Units are ordered by group: group g =
+// (k-block kb = g / T, tile t = g % T) holds the `kblock` k-steps kb*kblock ..
+// of tile t. With kblock = ksteps the order is tile-major (a CTA sweeps K of
+// one tile, then the next); the tensor-core engine of a large layer uses
+// kblock = 16, so a CTA's units touch at most two k-blocks and the normed
+// input it needs (<= 32 k-steps) fits in shared memory. Every unit counts the
+// same, also one of the partial in_proj_ba tile: a unit's time is set by its
+// fixed per-unit cost, not by its row count. CTA c takes units
+// [unit_begin[c], unit_begin[c+1]) with unit_begin[c] = floor(c * U / G).
+gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
+  pl->engine = engine;
   pl->G = G;
   pl->tiles_qkvz = n_qkvz(c) / kTileM;
   const int nba = n_ba(c);
-  pl->num_tiles = pl->tiles_qkvz + (nba + kTileM - 1) / kTileM;
-  pl->ksteps = c.hidden / kKStep;
+  const int T = pl->tiles_qkvz + (nba + kTileM - 1) / kTileM;
+  pl->num_tiles = T;
+  const int KS = c.hidden / kKStep;
+  pl->ksteps = KS;
   int chunk = (c.hidden + G - 1) / G;
   chunk = (chunk + 7) / 8 * 8;
   pl->norm_chunk = chunk;
   if (chunk > kMaxNormChunk) return GDN_ERR_UNSUPPORTED;
-  const long long KS = pl->ksteps;
-  const long long U = (long long)pl->num_tiles * KS;
-  auto cost = [&](long long t) -> long long {
-    return t < pl->tiles_qkvz ? kTileM : std::min<long long>(kTileM, nba - (t - pl->tiles_qkvz) * kTileM);
-  };
-  long long total = 0;
-  for (long long t = 0; t < pl->num_tiles; ++t) total += cost(t) * KS;
-  // unit_begin[c] = first unit whose cost prefix reaches c * total / G
-  long long u = 0, prefix = 0;
-  for (int cta = 0; cta <= G; ++cta) {
-    while (u < U && prefix * G < (long long)cta * total) {
-      prefix += cost(u / KS);
-      ++u;
-    }
-    pl->unit_begin[cta] = (int)(cta == G ? U : u);
+  const long long U = (long long)T * KS;
+  const long long per_cta = (U + G - 1) / G;
+  int KB = KS;
+  if (engine == GDN_ENGINE_TCGEN05 && per_cta + 1 > kMaxBSlots) {
+    if (KS % kKBlock != 0) return GDN_ERR_UNSUPPORTED;
+    KB = kKBlock;
   }
-  // Contributors of a tile are the CTAs with at least one unit in it, slotted
-  // in CTA order. A CTA whose range starts inside tile t0 takes the next slot
-  // of t0; every later tile it touches starts inside its range, so it is that
-  // tile's first contributor.
+  pl->kblock = KB;
+  for (int cta = 0; cta <= G; ++cta) pl->unit_begin[cta] = (int)((long long)cta * U / G);
+  // Partial slots: the pieces of tile t in unit order (k-block, then CTA)
+  // take slots 0, 1, ... of the tile; the epilogue adds them in slot order.
   int count[kMaxTiles];
-  for (int t = 0; t < pl->num_tiles; ++t) count[t] = 0;
+  for (int t = 0; t < T; ++t) count[t] = 0;
+  std::vector<char> need(KS);
   for (int cta = 0; cta < G; ++cta) {
-    pl->cta_slot0[cta] = 0;
-    const int b = pl->unit_begin[cta], e = pl->unit_begin[cta + 1];
+    const long long b = pl->unit_begin[cta], e = pl->unit_begin[cta + 1];
+    for (int i = 0; i < kMaxSegs; ++i) pl->seg_slot[cta][i] = 0;
+    pl->ks_first[cta] = 0;
+    pl->nb_slots[cta] = 0;
     if (b >= e) continue;
-    const int t0 = (int)(b / KS);
-    for (int t = t0; t <= (int)((e - 1) / KS); ++t) {
-      if (t == t0) {
-        if (count[t] > 255) return GDN_ERR_UNSUPPORTED;
-        pl->cta_slot0[cta] = (unsigned char)count[t];
-      } else if (count[t] != 0) {
-        return GDN_ERR_UNSUPPORTED;  // cannot happen with contiguous ranges
-      }
-      ++count[t];
+    int seg = 0;
+    for (long long g = b / KB; g <= (e - 1) / KB; ++g, ++seg) {
+      if (seg >= kMaxSegs) return GDN_ERR_UNSUPPORTED;
+      const int t = (int)(g % T);
+      if (count[t] > 254) return GDN_ERR_UNSUPPORTED;
+      pl->seg_slot[cta][seg] = (unsigned char)count[t]++;
     }
+    // the k-steps this CTA multiplies, as one cyclic window ks_first + j
+    std::fill(need.begin(), need.end(), 0);
+    int nneed = 0;
+    for (long long u = b; u < e; ++u) {
+      const long long g = u / KB;
+      const int ks = (int)((g / T) * KB + u % KB);
+      if (!need[ks]) { need[ks] = 1; ++nneed; }
+    }
+    int first = 0, len = KS;
+    if (nneed < KS) {
+      // the window starts after the longest cyclic run of unneeded k-steps
+      int best_gap = -1, best_end = 0;
+      for (int i = 0; i < KS; ++i) {
+        if (need[i] || !need[(i + KS - 1) % KS]) continue;  // i starts a gap run
+        int j = i;
+        while (!need[j % KS]) ++j;
+        if (j - i > best_gap) { best_gap = j - i; best_end = j % KS; }
+      }
+      first = best_end;
+      len = KS - best_gap;
+    }
+    pl->ks_first[cta] = (unsigned short)first;
+    pl->nb_slots[cta] = (unsigned char)std::min(len, 255);
+    if (engine == GDN_ENGINE_TCGEN05 && len > kMaxBSlots) return GDN_ERR_UNSUPPORTED;
   }
   int maxc = 1;
-  for (int t = 0; t < pl->num_tiles; ++t) {
-    if (count[t] < 1 || count[t] > 255) return GDN_ERR_UNSUPPORTED;
+  for (int t = 0; t < T; ++t) {
+    if (count[t] < 1) return GDN_ERR_UNSUPPORTED;
     pl->tile_count[t] = (unsigned char)count[t];
     maxc = std::max(maxc, count[t]);
   }
@@ -166,8 +199,55 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-const void* pick_kernel(const gdn_decode_config& c, bool has_res) {
-  return cuda_core_kernel(has_res, c.ssm_dtype == GDN_STATE_BF16, c.head_k_dim);
+const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
+  const bool b16 = c.ssm_dtype == GDN_STATE_BF16;
+  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim)
+                                      : cuda_core_kernel(has_res, b16, c.head_k_dim);
+}
+
+size_t kernel_smem(int engine) { return engine == GDN_ENGINE_TCGEN05 ? tensor_core_smem_bytes() : 0; }
+
+// The engine a config runs with and its plan: the requested engine, or for
+// GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA cores.
+gdn_status resolve_plan(const gdn_decode_config& c, int G, Plan* pl) {
+  if (c.engine == GDN_ENGINE_CUDA_CORE) return make_plan(c, G, GDN_ENGINE_CUDA_CORE, pl);
+  const gdn_status st = make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
+  if (st == GDN_OK || c.engine == GDN_ENGINE_TCGEN05) return st;
+  return make_plan(c, G, GDN_ENGINE_CUDA_CORE, pl);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  }
+  return fn;
+}
+
+// Tile map of a row-major [rows][H] bf16 weight: box 64 columns x 128 rows,
+// 128-byte swizzle (the K-major layout tcgen05.mma reads), zero fill past the
+// last row.
+bool encode_weight_map(CUtensorMap* m, const void* base, int rows, int H) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kKStep, (cuuint32_t)kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -194,7 +274,7 @@ size_t gdn_decode_workspace_bytes(const gdn_decode_config* cfg) {
   Plan* pl = new (std::nothrow) Plan;
   if (!pl) return 0;
   size_t bytes = 0;
-  if (make_plan(*cfg, G, pl) == GDN_OK) bytes = make_layout(*cfg, *pl).total;
+  if (resolve_plan(*cfg, G, pl) == GDN_OK) bytes = make_layout(*cfg, *pl).total;
   delete pl;
   return bytes;
 }
@@ -209,10 +289,11 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
   gdn_decode* h = new (std::nothrow) gdn_decode;
   if (!h) return GDN_ERR_ARG;
   h->cfg = *cfg;
+  h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
   if (h->cfg.deadline_us == 0) h->cfg.deadline_us = 200000;
   int G;
   st = device_grid(h->cfg, &h->device, &h->num_sms, &G);
-  if (st == GDN_OK) st = make_plan(h->cfg, G, &h->plan);
+  if (st == GDN_OK) st = resolve_plan(h->cfg, G, &h->plan);
   if (st != GDN_OK) {
     delete h;
     return st;
@@ -228,11 +309,13 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
     return GDN_ERR_UNSUPPORTED;
   }
   // Every CTA of the persistent grid must be co-resident.
+  const size_t smem = kernel_smem(h->plan.engine);
   for (int r = 0; r < 2; ++r) {
-    const void* k = pick_kernel(h->cfg, r == 1);
+    const void* k = pick_kernel(h->cfg, h->plan.engine, r == 1);
     int per_sm = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0) != cudaSuccess ||
-        per_sm < 1) {
+    if (!k || (smem && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                           cudaSuccess) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess || per_sm < 1) {
       delete h;
       return GDN_ERR_UNSUPPORTED;
     }
@@ -315,16 +398,32 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->proj_part = (float*)(base + h->lay.proj_part);
   p->act = (float*)(base + h->lay.act);
   p->act_ba = (float*)(base + h->lay.act_ba);
+  p->kblock = pl.kblock;
   memcpy(p->unit_begin, pl.unit_begin, sizeof(int) * (pl.G + 1));
-  memcpy(p->cta_slot0, pl.cta_slot0, pl.G);
+  memcpy(p->seg_slot, pl.seg_slot, sizeof(pl.seg_slot[0]) * pl.G);
+  memcpy(p->ks_first, pl.ks_first, sizeof(unsigned short) * pl.G);
+  memcpy(p->nb_slots, pl.nb_slots, pl.G);
   memcpy(p->tile_num_ctas, pl.tile_count, pl.num_tiles);
+  // weight tile maps (cached for the last weights seen)
+  if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
+    if (!encode_weight_map(&h->map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
+        !encode_weight_map(&h->map_ba, w->ba, n_ba(c), c.hidden)) {
+      h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
+      delete p;
+      return GDN_ERR_CUDA;
+    }
+    h->map_qkvz_ptr = w->qkvz;
+    h->map_ba_ptr = w->ba;
+  }
+  p->tm_qkvz = h->map_qkvz;
+  p->tm_ba = h->map_ba;
 
-  const void* kern = pick_kernel(c, residual != nullptr);
+  const void* kern = pick_kernel(c, pl.engine, residual != nullptr);
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(pl.G);
   lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = 0;
+  lc.dynamicSmemBytes = kernel_smem(pl.engine);
   lc.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -365,28 +464,52 @@ gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows, int32_t* 
                                   int32_t* engine) {
   if (!h || rows < 1 || rows > h->cfg.max_rows) return GDN_ERR_ARG;
   if (num_ctas) *num_ctas = h->plan.G;
-  if (engine) *engine = GDN_ENGINE_CUDA_CORE;
+  if (engine) *engine = h->plan.engine;
   return GDN_OK;
 }
 
-gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* unit_begin,
-                           uint8_t* cta_slot0, uint8_t* tile_count, int32_t tile_cap,
-                           int32_t* num_tiles, int32_t* ksteps) {
+gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
+                                     int32_t cta_cap, uint64_t* tile_stamps, int32_t tile_cap,
+                                     int32_t* num_ctas, int32_t* num_tiles) {
+  if (!h || !cta_stamps || !tile_stamps || !num_ctas || !num_tiles) return GDN_ERR_ARG;
+  const int G = h->plan.G, T = h->plan.num_tiles;
+  if (cta_cap < G * kTlSlots || tile_cap < T * 2) return GDN_ERR_ARG;
+  const char* base = (const char*)h->ws + h->lay.ctr;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(cta_stamps, base + offsetof(WsCounters, tl_cta), sizeof(uint64_t) * G * kTlSlots,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(tile_stamps, base + offsetof(WsCounters, tl_tile), sizeof(uint64_t) * T * 2,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  *num_ctas = G;
+  *num_tiles = T;
+  return GDN_OK;
+}
+
+gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* engine,
+                           int32_t* unit_begin, uint8_t* seg_slot, uint16_t* ks_first, uint8_t* nb_slots,
+                           uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
+                           int32_t* kblock) {
   gdn_status st = validate(cfg);
   if (st != GDN_OK) return st;
-  if (num_ctas < 1 || num_ctas > kMaxCtas || !unit_begin || !cta_slot0 || !tile_count || !num_tiles ||
-      !ksteps)
+  if (num_ctas < 1 || num_ctas > kMaxCtas || !engine || !unit_begin || !seg_slot || !ks_first ||
+      !nb_slots || !tile_count || !num_tiles || !ksteps || !kblock)
     return GDN_ERR_ARG;
   Plan* pl = new (std::nothrow) Plan;
   if (!pl) return GDN_ERR_ARG;
-  st = make_plan(*cfg, num_ctas, pl);
+  st = resolve_plan(*cfg, num_ctas, pl);
   if (st == GDN_OK && pl->num_tiles > tile_cap) st = GDN_ERR_ARG;
   if (st == GDN_OK) {
+    *engine = pl->engine;
     memcpy(unit_begin, pl->unit_begin, sizeof(int32_t) * (num_ctas + 1));
-    memcpy(cta_slot0, pl->cta_slot0, num_ctas);
+    memcpy(seg_slot, pl->seg_slot, (size_t)kMaxSegs * num_ctas);
+    memcpy(ks_first, pl->ks_first, sizeof(uint16_t) * num_ctas);
+    memcpy(nb_slots, pl->nb_slots, num_ctas);
     memcpy(tile_count, pl->tile_count, pl->num_tiles);
     *num_tiles = pl->num_tiles;
     *ksteps = pl->ksteps;
+    *kblock = pl->kblock;
   }
   delete pl;
   return st;

@@ -2,6 +2,7 @@
 // workspace layout, bf16 helpers, release/acquire counters and bounded waits.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -16,6 +17,9 @@ constexpr int kKStep = 64;                 // projection columns per work unit
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
 constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
+constexpr int kMaxSegs = 16;               // tile segments in one CTA's unit range
+constexpr int kKBlock = 16;                // k-steps per k-block in the k-block-major order
+constexpr int kMaxBSlots = 32;             // normed-input k-steps a CTA keeps in shared memory
 
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
 constexpr uint32_t kStatusDeadline = 4;
@@ -23,6 +27,8 @@ constexpr uint32_t kStatusIndex = 5;
 constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3;
 
 constexpr int kDebugSkipNormPublish = 0x1;
+constexpr int kDebugTimeline = 0x2;
+constexpr int kTlSlots = 16;  // timeline stamps per CTA
 
 // Workspace header: counters on separate 128-byte lines. Every counter only
 // grows; launch L waits for (L+1) * arrivals, so nothing is reset between
@@ -36,7 +42,16 @@ struct WsCounters {
   unsigned int pad2[63];
   unsigned long long tile_arrive[kMaxTiles];  // +1 per contributor of a tile
   unsigned long long tile_done[kMaxTiles];    // +1 when the tile's epilogue is out
+  // Debug timeline (kDebugTimeline): %globaltimer stamps per CTA at phase
+  // boundaries, and per tile the start and end of its epilogue.
+  unsigned long long tl_cta[kMaxCtas][kTlSlots];
+  unsigned long long tl_tile[kMaxTiles][2];
 };
+
+// Timeline stamp points of a CTA.
+enum TlPoint { TL_START = 0, TL_NORM_OUT, TL_NORM_IN, TL_XN_OUT, TL_PROJ_START, TL_PROJ_END,
+               TL_REC_WAITED, TL_END, TL_EPI_COUNT, TL_MMA_FIRST, TL_MMA_LAST, TL_ISSUED,
+               TL_R_STAGED, TL_EPI_DONE };
 
 struct StepParams {
   // shapes
@@ -45,6 +60,7 @@ struct StepParams {
   int tiles_qkvz;      // Nqkvz / 128
   int num_tiles;       // tiles_qkvz + ceil(Nba / 128)
   int ksteps;          // H / 64
+  int kblock;          // k-steps per k-block of the unit order (== ksteps: tile-major)
   int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
   int max_contrib;     // most CTAs contributing to one tile
   int num_ctas;
@@ -75,13 +91,21 @@ struct StepParams {
   float* proj_part;        // [num_tiles][max_contrib][kMaxRows][128]
   float* act;              // [kMaxRows][Nqkvz]: q^, k^ (normalised), v (conv out), z
   float* act_ba;           // [kMaxRows][Nba]: b, a (bf16-rounded projections)
-  // stream-K plan of the projection work units (unit = tile * ksteps + kstep)
-  // CTA c takes units [unit_begin[c], unit_begin[c+1]). Its partial of the
-  // first tile it touches goes to slot cta_slot0[c] of that tile; it is the
-  // first contributor (slot 0) of every later tile it touches. Tile t has
-  // tile_num_ctas[t] contributors.
+  // TMA descriptors of the bf16 weights (box 64 columns x 128 rows, 128-byte
+  // swizzle); used by the tensor-core engine and for L2 prefetches.
+  CUtensorMap tm_qkvz;
+  CUtensorMap tm_ba;
+  // Stream-K plan of the projection work units. Unit u belongs to group
+  // g = u / kblock (k-block kb = g / num_tiles, tile t = g % num_tiles) and is
+  // k-step kb * kblock + u % kblock of tile t. CTA c takes units
+  // [unit_begin[c], unit_begin[c+1]); the i-th group it touches is its
+  // segment i, whose partial goes to slot seg_slot[c][i] of the tile. Tile t
+  // receives tile_num_ctas[t] partials. The CTA's normed-input k-steps are
+  // ks_first[c] + j (mod ksteps) for j < nb_slots[c].
   int unit_begin[kMaxCtas + 1];
-  unsigned char cta_slot0[kMaxCtas];
+  unsigned char seg_slot[kMaxCtas][kMaxSegs];
+  unsigned short ks_first[kMaxCtas];
+  unsigned char nb_slots[kMaxCtas];
   unsigned char tile_num_ctas[kMaxTiles];
 };
 
@@ -148,6 +172,16 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Thread 0 of the CTA stamps a phase boundary when the timeline is on.
+__device__ __forceinline__ void tl_stamp(const StepParams& p, int point) {
+  if ((p.debug_flags & kDebugTimeline) && threadIdx.x == 0)
+    p.ctr->tl_cta[blockIdx.x][point] = globaltimer_ns();
+}
+// The same from whichever single thread calls it.
+__device__ __forceinline__ void tl_stamp_here(const StepParams& p, int point) {
+  if (p.debug_flags & kDebugTimeline) p.ctr->tl_cta[blockIdx.x][point] = globaltimer_ns();
+}
+
 __device__ __forceinline__ void record_error(WsCounters* c, uint32_t status, uint32_t wait_id,
                                              uint32_t who) {
   uint32_t word = (status << 24) | ((wait_id & 0xff) << 16) | (who & 0xffff);
@@ -172,6 +206,37 @@ static __device__ __noinline__ bool wait_counter(const StepParams& p, const unsi
       record_error(p.ctr, kStatusDeadline, wait_id, blockIdx.x);
       return false;
     }
+  }
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Spin (one thread) until every one of n counters is >= target, polling them
+// together (relaxed loads in flight at once, then one acquire fence). Same
+// deadline and error behaviour as wait_counter.
+static __device__ __noinline__ bool wait_counters(const StepParams& p, const unsigned long long* const* ctrs,
+                                                  int n, unsigned long long target, uint32_t wait_id) {
+  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long cap = p.deadline_ns / 32 + 4096;
+  for (unsigned long long it = 0;; ++it) {
+    unsigned long long v[8];
+    for (int i = 0; i < n; ++i) v[i] = ld_relaxed_u64(ctrs[i]);
+    bool all = true;
+    for (int i = 0; i < n; ++i) all = all && (v[i] >= target);
+    if (all) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      return true;
+    }
+    if ((ld_relaxed_u32(&p.ctr->error) >> 24) == kStatusDeadline) return false;
+    if (globaltimer_ns() - t0 > p.deadline_ns || it > cap) {
+      record_error(p.ctr, kStatusDeadline, wait_id, blockIdx.x);
+      return false;
+    }
+    __nanosleep(32);
   }
 }
 

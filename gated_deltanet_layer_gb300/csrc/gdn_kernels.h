@@ -10,4 +10,9 @@ namespace gdn {
 // there is none.
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk);
 
+// The same for the tensor-core (tcgen05) projection engine, and the dynamic
+// shared memory its launch needs.
+const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk);
+size_t tensor_core_smem_bytes();
+
 }  // namespace gdn

@@ -35,6 +35,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
   if (ub >= ue) return true;
   if (tid == 0)
     sm.flag = wait_counter(p, &p.ctr->xn_arrive, (unsigned long long)(L + 1) * p.num_ctas, kWaitXn);
+  tl_stamp(p, TL_PROJ_START);
   __syncthreads();
   if (!sm.flag) return false;
 
@@ -67,6 +68,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
 #pragma unroll
   for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
 
+  int seg = 0;  // segment index within this CTA's range (tile-major order)
   auto flush = [&](int t) {
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) {
@@ -75,7 +77,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       acc[w] = v;
     }
-    const int j = (t == ub / p.ksteps) ? p.cta_slot0[cta] : 0;
+    const int j = p.seg_slot[cta][seg];
     float* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
     if (sub == 0) {
 #pragma unroll
@@ -84,7 +86,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
     }
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
-    deliver_tile_partial(p, sm, t, L);
+    deliver_tile_partial<kThreads>(p, sm, t, L, tid);
   };
 
   constexpr int D = 4;  // units of weights in flight per thread
@@ -105,6 +107,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
         if (t != cur) {
           flush(cur);
           cur = t;
+          ++seg;
         }
         if (u + 1 < ue) stage(u + 1, (u + 1 - ub) & 1);
         const float(*x)[kKStep] = xs[(u - ub) & 1];
@@ -138,6 +141,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
     }
   }
   flush(cur);
+  tl_stamp(p, TL_PROJ_END);
   return true;
 }
 
@@ -148,11 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   if (threadIdx.x == 0) sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
   __syncthreads();
   if (!sm.flag) return;  // sticky error: every later launch returns at once
+  tl_stamp(p, TL_START);
   phase_norm_partials<HAS_RES>(p, sm);
   const int L = sm.L;
   if (!phase_normed_input(p, sm, L)) return;
   if (!phase_proj_cuda_core(p, sm, xs, L)) return;
   phase_recurrence<DK, STATE_BF16>(p, sm, L);
+  tl_stamp(p, TL_END);
 }
 
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk) {

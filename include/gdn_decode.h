@@ -83,6 +83,8 @@ typedef enum {
 /* Test hooks (debug_flags). Never set in production. */
 #define GDN_DEBUG_SKIP_NORM_PUBLISH 0x1 /* CTA 0 never publishes its norm partials,
                                            so every CTA's first wait runs out */
+#define GDN_DEBUG_TIMELINE 0x2          /* record %globaltimer stamps of each CTA's
+                                           phases (read with gdn_decode_debug_timeline) */
 
 typedef struct {
   int32_t hidden;
@@ -164,17 +166,32 @@ const char* gdn_status_string(gdn_status s);
 gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows,
                                   int32_t* num_ctas, int32_t* engine);
 
+/* Diagnostics: synchronise `stream` and copy the phase timeline the last
+ * step recorded (handle created with GDN_DEBUG_TIMELINE). cta_stamps receives
+ * num_ctas x 16 uint64 nanosecond stamps: 0 start, 1 norm partials out,
+ * 2 norm wait done, 3 normed input out, 4 projection start, 5 projection end,
+ * 6 first recurrence task's inputs ready, 7 end, 8 epilogues run (a count);
+ * tile_stamps receives num_tiles x 2 (epilogue start, end). Capacities are in
+ * elements; *num_ctas and *num_tiles receive the sizes. */
+gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
+                                     int32_t cta_cap, uint64_t* tile_stamps, int32_t tile_cap,
+                                     int32_t* num_ctas, int32_t* num_tiles);
+
 /* Host-only diagnostics of the stream-K split of the projection work units
- * (no device call). A unit is one 64-column step of one 128-row projection
- * tile (tiles: in_proj_qkvz rows first, then in_proj_ba rows). For a grid of
- * num_ctas CTAs it fills unit_begin[num_ctas+1] (CTA c takes units
- * [unit_begin[c], unit_begin[c+1])), cta_slot0[num_ctas] (the partial slot CTA
- * c writes in the first tile it touches), tile_count[*num_tiles] (CTAs that
- * deliver a partial of each tile; capacity `tile_cap`), *num_tiles and
- * *ksteps. GDN_ERR_ARG / GDN_ERR_UNSUPPORTED as for gdn_decode_create. */
-gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* unit_begin,
-                           uint8_t* cta_slot0, uint8_t* tile_count, int32_t tile_cap,
-                           int32_t* num_tiles, int32_t* ksteps);
+ * (no device call) for a grid of num_ctas CTAs. A unit is one 64-column step
+ * (k-step) of one 128-row projection tile (tiles: in_proj_qkvz rows first,
+ * then in_proj_ba rows); units are ordered by group g = (k-block g / T,
+ * tile g % T) of `kblock` k-steps. Fills *engine (the engine the config runs
+ * with), unit_begin[num_ctas+1] (CTA c takes units [unit_begin[c],
+ * unit_begin[c+1])), seg_slot[num_ctas][16] (partial slot of the i-th group
+ * CTA c touches), ks_first[num_ctas] and nb_slots[num_ctas] (CTA c keeps the
+ * normed input of k-steps ks_first[c] + j mod ksteps, j < nb_slots[c]),
+ * tile_count[*num_tiles] (partials per tile; capacity tile_cap), *ksteps and
+ * *kblock. Errors as for gdn_decode_create. */
+gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* engine,
+                           int32_t* unit_begin, uint8_t* seg_slot, uint16_t* ks_first, uint8_t* nb_slots,
+                           uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
+                           int32_t* kblock);
 
 #ifdef __cplusplus
 }

@@ -96,31 +96,41 @@ def test_product_path_never_imports_the_oracle():
                 assert "oracle" not in text, f
 
 
+@pytest.mark.parametrize("engine", ["cuda_core", "auto"])
 @pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16])
 @pytest.mark.parametrize("G", [1, 7, 33, 148, 152, 160])
-def test_stream_k_plan_invariants(lib, shape, G):
-    """The units partition [0, U) in CTA order; each CTA's weight cost is within
-    one unit of the mean; every tile's contributor count equals the number of
-    CTAs with a unit in it, and their slots are 0..count-1 without repeats."""
-    cfg = make_config(shape)
+def test_stream_k_plan_invariants(lib, shape, G, engine):
+    """The units partition [0, U) in CTA order with equal counts (within one);
+    walking each CTA's units the way the kernels do (group g = u // kblock,
+    tile g % T, k-step (g // T) * kblock + u % kblock) gives per tile the
+    slots 0..count-1 exactly once; with the tensor-core engine every unit's
+    normed-input slot lies inside the CTA's window of at most 32 k-steps."""
+    cfg = make_config(shape, engine=engine)
     if (shape.hidden + G - 1) // G > 256:
         with pytest.raises(_native.GdnError):
             _native.plan(cfg, G)
         return
-    ub, slot0, tc, nt, ks = _native.plan(cfg, G)
-    U = nt * ks
+    P = _native.plan(cfg, G)
+    ub, nt, KS, KB = P["unit_begin"], P["num_tiles"], P["ksteps"], P["kblock"]
+    U = nt * KS
     assert ub[0] == 0 and ub[G] == U and all(a <= b for a, b in zip(ub, ub[1:]))
-    tq = shape.n_qkvz // 128
-    cost = lambda u: 128 if u // ks < tq else min(128, shape.n_ba - (u // ks - tq) * 128)
-    costs = [sum(cost(u) for u in range(ub[c], ub[c + 1])) for c in range(G)]
-    assert max(costs) - sum(costs) / G <= 128
+    counts = [ub[c + 1] - ub[c] for c in range(G)]
+    assert max(counts) - min(counts) <= 1
+    assert engine == "cuda_core" and P["engine"] == 1 or engine == "auto"
     slots = {t: [] for t in range(nt)}
     for c in range(G):
-        if ub[c] == ub[c + 1]:
-            continue
-        t0, t1 = ub[c] // ks, (ub[c + 1] - 1) // ks
-        for t in range(t0, t1 + 1):
-            slots[t].append(slot0[c] if t == t0 else 0)
+        seg, g_prev = -1, None
+        for u in range(ub[c], ub[c + 1]):
+            g = u // KB
+            t, ks = g % nt, (g // nt) * KB + u % KB
+            if g != g_prev:
+                seg += 1
+                assert seg < 16
+                slots[t].append(P["seg_slot"][c][seg])
+                g_prev = g
+            if P["engine"] == 2:
+                j = (ks - P["ks_first"][c]) % KS
+                assert j < P["nb_slots"][c] <= 32
     for t in range(nt):
-        assert tc[t] == len(slots[t]) >= 1
-        assert sorted(slots[t]) == list(range(tc[t]))
+        assert P["tile_count"][t] == len(slots[t]) >= 1
+        assert sorted(slots[t]) == list(range(P["tile_count"][t]))
