@@ -8,7 +8,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/gdn_decode.h"
+#include "gdn_decode.h"
 #include "gdn_kernels.h"
 
 using namespace gdn;
@@ -18,7 +18,7 @@ namespace {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t ctr, norm_part, xn, proj_part, act, act_ba, total;
+  size_t ctr, norm_part, xn, proj_part, total;
 };
 
 struct Plan {
@@ -73,6 +73,7 @@ gdn_status validate(const gdn_decode_config* c) {
   if (c->head_k_dim != c->head_v_dim) return GDN_ERR_UNSUPPORTED;
   if (c->head_k_dim != 64 && c->head_k_dim != 128) return GDN_ERR_UNSUPPORTED;
   if (c->num_v_heads % c->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+  if (c->num_k_heads > kMaxKHeads) return GDN_ERR_UNSUPPORTED;
   if (c->num_v_heads % 2 != 0) return GDN_ERR_UNSUPPORTED;  // in_proj_ba rows come in fours
   if ((c->num_k_heads * c->head_k_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if ((c->num_v_heads * c->head_v_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
@@ -175,8 +176,6 @@ Layout make_layout(const gdn_decode_config& c, const Plan& pl) {
   l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(float), 256);
   l.xn = off;         off += align_up((size_t)kMaxRows * c.hidden * 2, 256);
   l.proj_part = off;  off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(float), 256);
-  l.act = off;        off += align_up((size_t)kMaxRows * n_qkvz(c) * sizeof(float), 256);
-  l.act_ba = off;     off += align_up((size_t)kMaxRows * n_ba(c) * sizeof(float), 256);
   l.total = off;
   return l;
 }
@@ -205,7 +204,9 @@ const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
                                       : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
-size_t kernel_smem(int engine) { return engine == GDN_ENGINE_TCGEN05 ? tensor_core_smem_bytes() : 0; }
+size_t kernel_smem(int engine) {
+  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_smem_bytes() : cuda_core_smem_bytes();
+}
 
 // The engine a config runs with and its plan: the requested engine, or for
 // GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA cores.
@@ -396,8 +397,6 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->norm_part = (float*)(base + h->lay.norm_part);
   p->xn = (__nv_bfloat16*)(base + h->lay.xn);
   p->proj_part = (float*)(base + h->lay.proj_part);
-  p->act = (float*)(base + h->lay.act);
-  p->act_ba = (float*)(base + h->lay.act_ba);
   p->kblock = pl.kblock;
   memcpy(p->unit_begin, pl.unit_begin, sizeof(int) * (pl.G + 1));
   memcpy(p->seg_slot, pl.seg_slot, sizeof(pl.seg_slot[0]) * pl.G);

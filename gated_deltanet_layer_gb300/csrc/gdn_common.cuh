@@ -12,14 +12,16 @@ namespace gdn {
 constexpr int kThreads = 512;              // one persistent CTA per SM
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRows = 16;               // rows of one decode step
-constexpr int kTileM = 128;                // projection rows per tile
+constexpr int kTileM = 256;                // projection rows per tile (one MMA's N)
+constexpr int kTileShift = 8;              // log2(kTileM)
 constexpr int kKStep = 64;                 // projection columns per work unit
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
 constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
 constexpr int kMaxSegs = 16;               // tile segments in one CTA's unit range
-constexpr int kKBlock = 16;                // k-steps per k-block in the k-block-major order
-constexpr int kMaxBSlots = 32;             // normed-input k-steps a CTA keeps in shared memory
+constexpr int kKBlock = 8;                 // k-steps per k-block in the k-block-major order
+constexpr int kMaxBSlots = 24;             // normed-input k-steps a CTA keeps in shared memory
+constexpr int kMaxKHeads = 64;             // key heads of a layer (conv-group counters)
 
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
 constexpr uint32_t kStatusDeadline = 4;
@@ -28,7 +30,7 @@ constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3;
 
 constexpr int kDebugSkipNormPublish = 0x1;
 constexpr int kDebugTimeline = 0x2;
-constexpr int kTlSlots = 16;  // timeline stamps per CTA
+constexpr int kTlSlots = 48;  // timeline stamps per CTA: 16 phase points, then 16 + 16 per-unit stamps
 
 // Workspace header: counters on separate 128-byte lines. Every counter only
 // grows; launch L waits for (L+1) * arrivals, so nothing is reset between
@@ -40,25 +42,28 @@ struct WsCounters {
   unsigned long long pad1[15];
   unsigned int error;               // sticky error word
   unsigned int pad2[63];
-  unsigned long long tile_arrive[kMaxTiles];  // +1 per contributor of a tile
-  unsigned long long tile_done[kMaxTiles];    // +1 when the tile's epilogue is out
+  unsigned long long tile_arrive[kMaxTiles];  // +1 per partial delivered to a tile
+  // +1 per recurrence task of (row, key head) once it has read the old q/k
+  // conv state; every launch adds the group size G or nothing, so the task
+  // that makes the count a multiple of G is the group's last reader
+  unsigned int conv_group[kMaxRows][kMaxKHeads];
   // Debug timeline (kDebugTimeline): %globaltimer stamps per CTA at phase
-  // boundaries, and per tile the start and end of its epilogue.
+  // boundaries, and per tile when its last partial arrived.
   unsigned long long tl_cta[kMaxCtas][kTlSlots];
   unsigned long long tl_tile[kMaxTiles][2];
 };
 
 // Timeline stamp points of a CTA.
 enum TlPoint { TL_START = 0, TL_NORM_OUT, TL_NORM_IN, TL_XN_OUT, TL_PROJ_START, TL_PROJ_END,
-               TL_REC_WAITED, TL_END, TL_EPI_COUNT, TL_MMA_FIRST, TL_MMA_LAST, TL_ISSUED,
-               TL_R_STAGED, TL_EPI_DONE };
+               TL_REC_WAITED, TL_END, TL_REC_INPUTS, TL_MMA_FIRST, TL_MMA_LAST, TL_ISSUED,
+               TL_R_STAGED, TL_REC_STATE, TL_UNIT_READY = 16, TL_UNIT_ISSUED = 32 };
 
 struct StepParams {
   // shapes
   int H, Hk, Hv, dk, dv, C, Nqkvz, Nba, num_slots, rows;
   int group;           // Hv / Hk
-  int tiles_qkvz;      // Nqkvz / 128
-  int num_tiles;       // tiles_qkvz + ceil(Nba / 128)
+  int tiles_qkvz;      // Nqkvz / kTileM
+  int num_tiles;       // tiles_qkvz + ceil(Nba / kTileM)
   int ksteps;          // H / 64
   int kblock;          // k-steps per k-block of the unit order (== ksteps: tile-major)
   int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
@@ -88,10 +93,8 @@ struct StepParams {
   WsCounters* ctr;
   float* norm_part;        // [kMaxRows][num_ctas]
   __nv_bfloat16* xn;       // [kMaxRows][H]
-  float* proj_part;        // [num_tiles][max_contrib][kMaxRows][128]
-  float* act;              // [kMaxRows][Nqkvz]: q^, k^ (normalised), v (conv out), z
-  float* act_ba;           // [kMaxRows][Nba]: b, a (bf16-rounded projections)
-  // TMA descriptors of the bf16 weights (box 64 columns x 128 rows, 128-byte
+  float* proj_part;        // [num_tiles][max_contrib][kMaxRows][kTileM]
+  // TMA descriptors of the bf16 weights (box 64 columns x 256 rows, 128-byte
   // swizzle); used by the tensor-core engine and for L2 prefetches.
   CUtensorMap tm_qkvz;
   CUtensorMap tm_ba;
@@ -215,18 +218,18 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
-// Spin (one thread) until every one of n counters is >= target, polling them
-// together (relaxed loads in flight at once, then one acquire fence). Same
-// deadline and error behaviour as wait_counter.
+// Spin (one thread) until every counter ctrs[i] >= targets[i] (i < n <= 8),
+// polling them together (relaxed loads in flight at once, then one acquire
+// fence). Same deadline and error behaviour as wait_counter.
 static __device__ __noinline__ bool wait_counters(const StepParams& p, const unsigned long long* const* ctrs,
-                                                  int n, unsigned long long target, uint32_t wait_id) {
+                                                  const unsigned long long* targets, int n, uint32_t wait_id) {
   const unsigned long long t0 = globaltimer_ns();
   const unsigned long long cap = p.deadline_ns / 32 + 4096;
   for (unsigned long long it = 0;; ++it) {
     unsigned long long v[8];
     for (int i = 0; i < n; ++i) v[i] = ld_relaxed_u64(ctrs[i]);
     bool all = true;
-    for (int i = 0; i < n; ++i) all = all && (v[i] >= target);
+    for (int i = 0; i < n; ++i) all = all && (v[i] >= targets[i]);
     if (all) {
       asm volatile("fence.acq_rel.gpu;" ::: "memory");
       return true;

@@ -9,6 +9,7 @@ namespace gdn {
 // combination of first-layer variant, state dtype and head dim; nullptr if
 // there is none.
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk);
+size_t cuda_core_smem_bytes();
 
 // The same for the tensor-core (tcgen05) projection engine, and the dynamic
 // shared memory its launch needs.

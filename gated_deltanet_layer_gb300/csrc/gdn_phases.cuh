@@ -12,16 +12,8 @@ namespace gdn {
 struct SmemPhases {
   alignas(16) __nv_bfloat16 rbuf[kMaxRows][kMaxNormChunk];  // r = x + residual of this CTA's columns
   alignas(16) float part8[kMaxRows * (kMaxNormChunk / 8)];  // sums of 8 squares
-  alignas(16) float ep[kMaxRows][kTileM];                   // tile epilogue values
-  alignas(16) float v[128];                                 // recurrence task vectors (dv <= 128)
-  alignas(16) float z[128];
-  alignas(16) float o[128];
   alignas(16) float rstd[kMaxRows];
-  alignas(16) float inv[kMaxRows * 2];                      // q/k inverse norms of one tile
   alignas(16) float red[kWarps];
-  alignas(16) __nv_bfloat16 cst[kMaxRows][kTileM * 3];      // conv state of one tile's channels
-  alignas(16) __nv_bfloat16 cw[kTileM * 4];                 // conv weights of one tile's channels
-  int slot[kMaxRows];                                       // state index of each row
   int L;                 // launch number on this workspace
   int flag;              // CTA-wide decision broadcast by thread 0
 };
@@ -57,7 +49,7 @@ __device__ __forceinline__ uint4 residual8(uint4 xv, uint4 qv) {
 // consumer builds the x it reads). Returns the launch number.
 // ---------------------------------------------------------------------------
 template <bool HAS_RES>
-__device__ void phase_norm_partials(const StepParams& p, SmemPhases& sm) {
+__device__ __forceinline__ void phase_norm_partials(const StepParams& p, SmemPhases& sm) {
   const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int c0 = cta * p.norm_chunk;
@@ -107,7 +99,7 @@ __device__ void phase_norm_partials(const StepParams& p, SmemPhases& sm) {
 // rstd = 1/sqrt(mean(r^2) + eps), xn = r * rstd * (1 + w)) and write this
 // CTA's columns of the normed input xn (bf16) to the workspace image.
 // ---------------------------------------------------------------------------
-static __device__ bool phase_wait_rstd(const StepParams& p, SmemPhases& sm, int L) {
+static __device__ __forceinline__ bool phase_wait_rstd(const StepParams& p, SmemPhases& sm, int L) {
   const int W = p.rows, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0)
@@ -126,7 +118,7 @@ static __device__ bool phase_wait_rstd(const StepParams& p, SmemPhases& sm, int 
   return true;
 }
 
-static __device__ bool phase_normed_input(const StepParams& p, SmemPhases& sm, int L) {
+static __device__ __forceinline__ bool phase_normed_input(const StepParams& p, SmemPhases& sm, int L) {
   const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
   if (!phase_wait_rstd(p, sm, L)) return false;
   const int c0 = cta * p.norm_chunk;
@@ -149,209 +141,69 @@ __device__ __forceinline__ bool row_is_live(const StepParams& p, int slot) {
   return slot > 0 && slot < p.num_slots;
 }
 
-// Synchronise the threads that run an epilogue: the whole CTA (barrier 0) or
-// the 128-thread drain group of the tensor-core engine (named barrier 1).
+// Synchronise the threads of a group: the whole CTA (barrier 0), one warp, or
+// another group of whole warps (named barrier 1).
 template <int NT>
 __device__ __forceinline__ void group_sync() {
   if (NT == kThreads)
     __syncthreads();
+  else if (NT == 32)
+    __syncwarp();
   else
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Tile epilogue, run by the last CTA to deliver a partial of projection tile t
-// (NT threads, group thread index gtid): sum the partials in slot order, round
-// to bf16 (the projection output), then by row kind: q/k/v channels -> conv
-// update + SiLU (and the L2 norm for q, k); z -> stored; b/a -> stored for the
-// gates. Pad rows write no state. (sgl-amd-mono #89, "Kernels before and
-// after": the split, the conv update and the gated delta rule's q/k
-// normalisation all move into one launch.)
-// ---------------------------------------------------------------------------
+// Publish a finished partial of tile t: called by all NT threads of a group
+// after they wrote it; group thread 0 counts it with a release add.
 template <int NT>
-static __device__ void tile_epilogue(const StepParams& p, SmemPhases& sm, int t, int gtid) {
-  constexpr int NW = NT / 32;
-  constexpr int IT = (kMaxRows * (kTileM / 4) + NT - 1) / NT;  // float4 items per thread
-  const int W = p.rows;
-  const int warp = gtid >> 5, lane = gtid & 31;
-  const bool is_ba = t >= p.tiles_qkvz;
-  const int n0 = is_ba ? (t - p.tiles_qkvz) * kTileM : t * kTileM;
-  const int rows_t = is_ba ? min(kTileM, p.Nba - n0) : kTileM;
-  const int nc = p.tile_num_ctas[t];
-  const float* part = p.proj_part + (size_t)t * p.max_contrib * kMaxRows * kTileM;
-  const bool conv_tile = !is_ba && n0 < p.C;
-  if (gtid < W) sm.slot[gtid] = p.idx[gtid];
-  // conv state and weights of this tile's channels, staged while the partials load
-  if (conv_tile) {
-    for (int i = gtid; i < W * (kTileM * 3 / 8); i += NT) {
-      const int w = i / (kTileM * 3 / 8), q = i - w * (kTileM * 3 / 8);
-      const int slot = p.idx[w];
-      if (row_is_live(p, slot))
-        reinterpret_cast<uint4*>(sm.cst[w])[q] =
-            *reinterpret_cast<const uint4*>(p.conv_state + ((size_t)slot * p.C + n0) * 3 + q * 8);
-    }
-    for (int i = gtid; i < kTileM * 4 / 8; i += NT)
-      reinterpret_cast<uint4*>(sm.cw)[i] = *reinterpret_cast<const uint4*>(p.conv_w + (size_t)n0 * 4 + i * 8);
-  }
-  // partial sums: float4 items (row w, rows 4*r4 .. 4*r4+3), slots added in order
-  float4 acc[IT];
-#pragma unroll
-  for (int it = 0; it < IT; ++it) acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < nc; j0 += 4) {
-    float4 v[4][IT];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-      for (int it = 0; it < IT; ++it) {
-        const int q = gtid + it * NT, w = q >> 5, r4 = q & 31;
-        if (j0 + jj < nc && w < W && r4 * 4 < rows_t)
-          v[jj][it] = ld_cg_f4(part + ((size_t)(j0 + jj) * kMaxRows + w) * kTileM + r4 * 4);
-      }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-      for (int it = 0; it < IT; ++it) {
-        const int q = gtid + it * NT, w = q >> 5, r4 = q & 31;
-        if (j0 + jj < nc && w < W && r4 * 4 < rows_t) {
-          acc[it].x += v[jj][it].x; acc[it].y += v[jj][it].y;
-          acc[it].z += v[jj][it].z; acc[it].w += v[jj][it].w;
-        }
-      }
-  }
-#pragma unroll
-  for (int it = 0; it < IT; ++it) {
-    const int q = gtid + it * NT, w = q >> 5, r4 = q & 31;
-    if (w < W && r4 * 4 < rows_t)
-      *reinterpret_cast<float4*>(&sm.ep[w][r4 * 4]) =
-          make_float4(round_bf16(acc[it].x), round_bf16(acc[it].y), round_bf16(acc[it].z), round_bf16(acc[it].w));
-  }
-  group_sync<NT>();
-  if (is_ba) {
-    for (int i = gtid; i < W * kTileM; i += NT) {
-      const int w = i >> 7, r = i & (kTileM - 1);
-      if (r < rows_t) p.act_ba[(size_t)w * p.Nba + n0 + r] = sm.ep[w][r];
-    }
-    return;
-  }
-  if (!conv_tile) {  // z rows
-    for (int i = gtid; i < W * kTileM; i += NT) {
-      const int w = i >> 7, r = i & (kTileM - 1);
-      p.act[(size_t)w * p.Nqkvz + n0 + r] = sm.ep[w][r];
-    }
-    return;
-  }
-  // conv channels c = n0 + r over [q | k | v]: y = silu(w0 s0 + w1 s1 + w2 s2 + w3 p),
-  // state <- [s1, s2, p]
-  for (int i = gtid; i < W * kTileM; i += NT) {
-    const int w = i >> 7, r = i & (kTileM - 1);
-    if (!row_is_live(p, sm.slot[w])) continue;
-    __nv_bfloat16* cs = &sm.cst[w][r * 3];
-    const __nv_bfloat16* cw = &sm.cw[r * 4];
-    const float pv = sm.ep[w][r];
-    const float s1 = bf16_to_f(cs[1]), s2 = bf16_to_f(cs[2]);
-    float acc1 = bf16_to_f(cw[0]) * bf16_to_f(cs[0]);
-    acc1 = fmaf(bf16_to_f(cw[1]), s1, acc1);
-    acc1 = fmaf(bf16_to_f(cw[2]), s2, acc1);
-    acc1 = fmaf(bf16_to_f(cw[3]), pv, acc1);
-    cs[0] = __float2bfloat16_rn(s1);
-    cs[1] = __float2bfloat16_rn(s2);
-    cs[2] = __float2bfloat16_rn(pv);
-    sm.ep[w][r] = silu_f(acc1);
-  }
-  group_sync<NT>();
-  for (int i = gtid; i < W * (kTileM * 3 / 8); i += NT) {
-    const int w = i / (kTileM * 3 / 8), q = i - w * (kTileM * 3 / 8);
-    const int slot = sm.slot[w];
-    if (row_is_live(p, slot))
-      *reinterpret_cast<uint4*>(p.conv_state + ((size_t)slot * p.C + n0) * 3 + q * 8) =
-          reinterpret_cast<const uint4*>(sm.cst[w])[q];
-  }
-  const bool is_qk = n0 < 2 * p.Hk * p.dk;
-  if (is_qk) {
-    const bool is_q = n0 < p.Hk * p.dk;
-    const int hpt = kTileM / p.dk;  // heads in this tile
-    for (int pr = warp; pr < W * hpt; pr += NW) {
-      const int w = pr / hpt, hd = pr - w * hpt;
-      float s = 0.f;
-      for (int j = lane; j < p.dk; j += 32) {
-        const float y = sm.ep[w][hd * p.dk + j];
-        s = fmaf(y, y, s);
-      }
-      s = warp_sum(s);
-      if (lane == 0) sm.inv[pr] = (1.0f / sqrtf(s + p.l2_eps)) * (is_q ? p.q_scale : 1.0f);
-    }
-    group_sync<NT>();
-    for (int i = gtid; i < W * kTileM; i += NT) {
-      const int w = i >> 7, r = i & (kTileM - 1);
-      p.act[(size_t)w * p.Nqkvz + n0 + r] = sm.ep[w][r] * sm.inv[w * hpt + r / p.dk];
-    }
-  } else {
-    for (int i = gtid; i < W * kTileM; i += NT) {
-      const int w = i >> 7, r = i & (kTileM - 1);
-      p.act[(size_t)w * p.Nqkvz + n0 + r] = sm.ep[w][r];
-    }
-  }
-}
-
-// Publish a finished partial of tile t and count it. Called by all NT
-// threads of a group after the partial is written; returns (to every thread
-// of the group) whether this was the tile's last partial.
-template <int NT>
-static __device__ bool arrive_tile_partial(const StepParams& p, SmemPhases& sm, int t, int L, int gtid) {
+static __device__ __forceinline__ void publish_tile_partial(const StepParams& p, int t, int gtid) {
   __threadfence();
   group_sync<NT>();
   if (gtid == 0) {
-    const unsigned long long old = atom_add_acq_rel_u64(&p.ctr->tile_arrive[t], 1ull);
-    const unsigned long long full = (unsigned long long)(L + 1) * p.tile_num_ctas[t];
-    sm.flag = (old + 1 == full);
+    atom_add_release_u64(&p.ctr->tile_arrive[t], 1ull);
+    if (p.debug_flags & kDebugTimeline) p.ctr->tl_tile[t][0] = globaltimer_ns();
   }
-  group_sync<NT>();
-  const bool last = sm.flag;
-  group_sync<NT>();
-  return last;
 }
 
-// Run tile t's epilogue (all partials are in) and publish the tile as done.
-template <int NT>
-static __device__ void finish_tile(const StepParams& p, SmemPhases& sm, int t, int gtid) {
-  __threadfence();
-  if ((p.debug_flags & kDebugTimeline) && gtid == 0) {
-    p.ctr->tl_tile[t][0] = globaltimer_ns();
-    p.ctr->tl_cta[blockIdx.x][TL_EPI_COUNT] += 1;
-  }
-  tile_epilogue<NT>(p, sm, t, gtid);
-  __threadfence();
-  group_sync<NT>();
-  if (gtid == 0) {
-    if (p.debug_flags & kDebugTimeline) p.ctr->tl_tile[t][1] = globaltimer_ns();
-    atom_add_release_u64(&p.ctr->tile_done[t], 1ull);
-  }
-  group_sync<NT>();
-}
-
-// Deliver a partial and, as the tile's last contributor, finish the tile.
-template <int NT>
-static __device__ void deliver_tile_partial(const StepParams& p, SmemPhases& sm, int t, int L, int gtid) {
-  if (arrive_tile_partial<NT>(p, sm, t, L, gtid)) finish_tile<NT>(p, sm, t, gtid);
-}
+// Shared memory of one recurrence task.
+struct SmemTask {
+  alignas(16) float q[128];     // q^ (after conv + SiLU, L2 norm, q_scale)
+  alignas(16) float k[128];     // k^
+  alignas(16) float v[128];     // v after conv + SiLU
+  alignas(16) float z[128];     // z (bf16 projection)
+  alignas(16) float o[128];     // o = S q
+  alignas(16) float cnew[2 * 128][3];  // new q/k conv taps, written by the group's last reader
+  float ba[2];                  // b, a (bf16 projections)
+  float red[kWarps];
+  int last;
+};
 
 // ---------------------------------------------------------------------------
-// Phase 3: per (row w, value head h) task: gates, the gated delta rule on
-// the row's state slot, and the gated RMSNorm x SiLU(z).
-//   g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
-//   S <- e^g S;  u = beta (v - S k);  S <- S + u k^T;  o = S q   (S[v][k])
-//   core = bf16(o * rsqrt(mean(o^2) + eps) * w_g * silu(z))
-// Each warp owns whole state rows S[v][:], so S k and S q are reductions over
-// one row's lanes (sgl-amd-mono #89, Modifications, gdn.py row: f32
+// Phase 3: per (row w, value head h) task, all of the layer front after the
+// projections for that head:
+//   * the task's 4*dk + 2 projection outputs (q, k of key head kh = h / G; v,
+//     z of head h; b, a) as the sum of the tiles' partials in slot order,
+//     rounded to bf16
+//   * causal conv update + SiLU over its q, k, v channels (old taps read,
+//     new taps [s1, s2, p]); the v channels are this task's alone; the q/k
+//     channels are shared by the G value heads of kh, and the last of those
+//     G tasks to read the old taps writes the new ones
+//   * q^ = q / sqrt(sum q^2 + eps) * q_scale, k^ likewise without the scale
+//   * g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+//   * S <- e^g S;  u = beta (v - S k^);  S <- S + u k^T;  o = S q^   (S[v][k])
+//   * core = bf16(o * rsqrt(mean(o^2) + eps) * w_g * silu(z))
+// Each warp owns whole state rows S[v][:], so S k and S q are reductions
+// over one row's lanes (sgl-amd-mono #89, Modifications, gdn.py row: f32
 // recurrence, state stored in f32 or bf16 in place; pad rows write a zero
 // core row and no state).
 // ---------------------------------------------------------------------------
 template <int DK, bool STATE_BF16>
-__device__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, int L) {
-  constexpr int LPR = DK / 4;            // lanes per state row, 4 elements each
-  constexpr int RPW = 32 / LPR;          // rows per warp per step
+__device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, SmemTask& st, int L) {
+  constexpr int LPR = DK / 4;              // lanes per state row, 4 elements each
+  constexpr int RPW = 32 / LPR;            // rows per warp per step
   constexpr int NR = DK / (kWarps * RPW);  // rows per lane (dv == dk)
-  static_assert(NR >= 1, "state rows per lane");
+  constexpr int NOUT = 4 * DK + 2;         // q, k, v, z, then b, a
+  static_assert(NR >= 1 && NOUT <= 2 * kThreads, "task layout");
   const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int sub = lane % LPR, rw = lane / LPR;
@@ -369,7 +221,7 @@ __device__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, int L) {
     }
     const int kh = h / p.group;
     // The state rows go into registers first, so their latency overlaps the
-    // wait for this task's projection tiles.
+    // wait for the projections.
     const size_t sbase = ((size_t)slot * p.Hv + h) * (size_t)DK * DK;
     uint2 rawb[NR];
     float4 rawf[NR];
@@ -382,34 +234,127 @@ __device__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, int L) {
       else
         rawf[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
     }
+    // Projection row of each task output, its tile and row in the tile.
+    auto proj_row = [&](int i) -> int {
+      if (i < DK) return kh * DK + i;
+      if (i < 2 * DK) return p.Hk * DK + kh * DK + (i - DK);
+      if (i < 3 * DK) return 2 * p.Hk * DK + h * DK + (i - 2 * DK);
+      if (i < 4 * DK) return p.C + h * DK + (i - 3 * DK);
+      return p.Nqkvz + (i == 4 * DK ? h : p.Hv + h);
+    };
+    auto tile_of = [&](int n) -> int {
+      return n < p.Nqkvz ? (n >> kTileShift) : p.tiles_qkvz + ((n - p.Nqkvz) >> kTileShift);
+    };
     if (tid == 0) {
-      const unsigned long long* ctrs[6] = {
-          &p.ctr->tile_done[(kh * DK) / kTileM],
-          &p.ctr->tile_done[(p.Hk * DK + kh * DK) / kTileM],
-          &p.ctr->tile_done[(2 * p.Hk * DK + h * DK) / kTileM],
-          &p.ctr->tile_done[(p.C + h * DK) / kTileM],
-          &p.ctr->tile_done[p.tiles_qkvz + h / kTileM],
-          &p.ctr->tile_done[p.tiles_qkvz + (p.Hv + h) / kTileM]};
-      sm.flag = wait_counters(p, ctrs, 6, (unsigned long long)(L + 1), kWaitTile);
+      const int tiles[6] = {tile_of(proj_row(0)), tile_of(proj_row(DK)), tile_of(proj_row(2 * DK)),
+                            tile_of(proj_row(3 * DK)), tile_of(proj_row(4 * DK)), tile_of(proj_row(4 * DK + 1))};
+      const unsigned long long* ctrs[6];
+      unsigned long long tgt[6];
+      for (int i = 0; i < 6; ++i) {
+        ctrs[i] = &p.ctr->tile_arrive[tiles[i]];
+        tgt[i] = (unsigned long long)(L + 1) * p.tile_num_ctas[tiles[i]];
+      }
+      sm.flag = wait_counters(p, ctrs, tgt, 6, kWaitTile);
       if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
     }
     __syncthreads();
     if (!sm.flag) return false;
-    const float* actw = p.act + (size_t)w * p.Nqkvz;
-    for (int i = tid; i < DK; i += kThreads) {
-      sm.v[i] = ld_cg_f(actw + 2 * p.Hk * DK + h * DK + i);
-      sm.z[i] = ld_cg_f(actw + p.C + h * DK + i);
+
+    // Projection outputs: partials in slot order; conv for q/k/v channels.
+    for (int i = tid; i < NOUT; i += kThreads) {
+      const int n = proj_row(i);
+      const int t = tile_of(n);
+      const int r = (n < p.Nqkvz ? n : n - p.Nqkvz) & (kTileM - 1);
+      const int nc = p.tile_num_ctas[t];
+      const float* src = p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
+      constexpr size_t kSlot = (size_t)kMaxRows * kTileM;
+      const bool conv = i < 3 * DK;
+      float c0 = 0.f, c1 = 0.f, c2 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+      if (conv) {  // old taps and weights of channel n, loaded with the partials
+        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+        const __nv_bfloat16* cw = p.conv_w + (size_t)n * 4;
+        c0 = bf16_to_f(cs[0]); c1 = bf16_to_f(cs[1]); c2 = bf16_to_f(cs[2]);
+        w0 = bf16_to_f(cw[0]); w1 = bf16_to_f(cw[1]); w2 = bf16_to_f(cw[2]); w3 = bf16_to_f(cw[3]);
+      }
+      float acc = 0.f;
+      for (int j0 = 0; j0 < nc; j0 += 8) {
+        float pv8[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) pv8[jj] = (j0 + jj < nc) ? ld_cg_f(src + (size_t)(j0 + jj) * kSlot) : 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          if (j0 + jj < nc) acc += pv8[jj];
+      }
+      const float pv = round_bf16(acc);
+      if (conv) {
+        float y = w0 * c0;
+        y = fmaf(w1, c1, y);
+        y = fmaf(w2, c2, y);
+        y = fmaf(w3, pv, y);
+        y = silu_f(y);
+        if (i < DK) {
+          st.q[i] = y;
+        } else if (i < 2 * DK) {
+          st.k[i - DK] = y;
+        } else {
+          st.v[i - 2 * DK] = y;
+          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;  // this head's own channel
+          cs[0] = __float2bfloat16_rn(c1);
+          cs[1] = __float2bfloat16_rn(c2);
+          cs[2] = __float2bfloat16_rn(pv);
+        }
+        if (i < 2 * DK) {
+          st.cnew[i][0] = c1;
+          st.cnew[i][1] = c2;
+          st.cnew[i][2] = pv;
+        }
+      } else if (i < 4 * DK) {
+        st.z[i - 3 * DK] = pv;
+      } else {
+        st.ba[i - 4 * DK] = pv;
+      }
     }
-    const float4 k4 = ld_cg_f4(actw + p.Hk * DK + kh * DK + sub * 4);
-    const float4 q4 = ld_cg_f4(actw + kh * DK + sub * 4);
-    const float bv = ld_cg_f(p.act_ba + (size_t)w * p.Nba + h);
-    const float av = ld_cg_f(p.act_ba + (size_t)w * p.Nba + p.Hv + h);
-    const float sp_in = av + bf16_to_f(p.dt_bias[h]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      // every thread's reads of the old q/k taps are done: count this reader
+      const unsigned int old = atomicAdd(&p.ctr->conv_group[w][kh], 1u);
+      st.last = ((old + 1) % (unsigned)p.group) == 0;
+      if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
+    }
+    // L2 norms of q and k: warps 0..DK/32-1 sum q^2, the next as many k^2
+    if (warp < 2 * (DK / 32)) {
+      const bool isq = warp < DK / 32;
+      const float y = isq ? st.q[warp * 32 + lane] : st.k[(warp - DK / 32) * 32 + lane];
+      const float s = warp_sum(y * y);
+      if (lane == 0) sm.red[warp] = s;
+    }
+    __syncthreads();
+    float sq = 0.f, sk = 0.f;
+    for (int i = 0; i < DK / 32; ++i) {
+      sq += sm.red[i];
+      sk += sm.red[DK / 32 + i];
+    }
+    const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
+    const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
+    if (st.last) {  // the last reader of the group writes the new q/k taps
+      for (int i = tid; i < 2 * DK; i += kThreads) {
+        const int n = proj_row(i);
+        __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+        cs[0] = __float2bfloat16_rn(st.cnew[i][0]);
+        cs[1] = __float2bfloat16_rn(st.cnew[i][1]);
+        cs[2] = __float2bfloat16_rn(st.cnew[i][2]);
+      }
+    }
+    const float4 kq = *reinterpret_cast<const float4*>(&st.k[sub * 4]);
+    const float4 qq = *reinterpret_cast<const float4*>(&st.q[sub * 4]);
+    const float4 k4 = make_float4(kq.x * inv_k, kq.y * inv_k, kq.z * inv_k, kq.w * inv_k);
+    const float4 q4 = make_float4(qq.x * inv_q, qq.y * inv_q, qq.z * inv_q, qq.w * inv_q);
+    const float sp_in = st.ba[1] + bf16_to_f(p.dt_bias[h]);
     const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
     const float g = -expf(p.A_log[h]) * sp;
     const float eg = expf(g);
-    const float beta = 1.0f / (1.0f + expf(-bv));
-    __syncthreads();
+    const float beta = 1.0f / (1.0f + expf(-st.ba[0]));
 
     float s[NR][4];
 #pragma unroll
@@ -421,44 +366,61 @@ __device__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, int L) {
         s[j][0] = rawf[j].x; s[j][1] = rawf[j].y; s[j][2] = rawf[j].z; s[j][3] = rawf[j].w;
       }
     }
+    // S k over all rows of this lane at once (independent butterflies)
+    float a[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[j][c] *= eg;
+      a[j] = s[j][0] * k4.x;
+      a[j] = fmaf(s[j][1], k4.y, a[j]);
+      a[j] = fmaf(s[j][2], k4.z, a[j]);
+      a[j] = fmaf(s[j][3], k4.w, a[j]);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < NR; ++j) a[j] += __shfl_xor_sync(0xffffffffu, a[j], o);
+    float ov[NR];
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
       const int v = (j * kWarps + warp) * RPW + rw;
-      float e[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) e[c] = eg * s[j][c];
-      float a = e[0] * k4.x;
-      a = fmaf(e[1], k4.y, a); a = fmaf(e[2], k4.z, a); a = fmaf(e[3], k4.w, a);
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      const float u = beta * (sm.v[v] - a);
-      e[0] = fmaf(k4.x, u, e[0]); e[1] = fmaf(k4.y, u, e[1]);
-      e[2] = fmaf(k4.z, u, e[2]); e[3] = fmaf(k4.w, u, e[3]);
-      float ov = e[0] * q4.x;
-      ov = fmaf(e[1], q4.y, ov); ov = fmaf(e[2], q4.z, ov); ov = fmaf(e[3], q4.w, ov);
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) ov += __shfl_xor_sync(0xffffffffu, ov, o);
+      const float u = beta * (st.v[v] - a[j]);
+      s[j][0] = fmaf(k4.x, u, s[j][0]); s[j][1] = fmaf(k4.y, u, s[j][1]);
+      s[j][2] = fmaf(k4.z, u, s[j][2]); s[j][3] = fmaf(k4.w, u, s[j][3]);
+      ov[j] = s[j][0] * q4.x;
+      ov[j] = fmaf(s[j][1], q4.y, ov[j]);
+      ov[j] = fmaf(s[j][2], q4.z, ov[j]);
+      ov[j] = fmaf(s[j][3], q4.w, ov[j]);
       const size_t off = sbase + (size_t)v * DK + sub * 4;
       if (STATE_BF16) {
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ssm_state) + off) =
-            make_uint2(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]));
+            make_uint2(pack_bf16x2(s[j][0], s[j][1]), pack_bf16x2(s[j][2], s[j][3]));
       } else {
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ssm_state) + off) =
-            make_float4(e[0], e[1], e[2], e[3]);
+            make_float4(s[j][0], s[j][1], s[j][2], s[j][3]);
       }
-      if (sub == 0) sm.o[v] = ov;
     }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < NR; ++j) ov[j] += __shfl_xor_sync(0xffffffffu, ov[j], o);
+#pragma unroll
+    for (int j = 0; j < NR; ++j)
+      if (sub == 0) st.o[(j * kWarps + warp) * RPW + rw] = ov[j];
     __syncthreads();
     if (warp == 0) {
       float q = 0.f;
-      for (int i = lane; i < DK; i += 32) q = fmaf(sm.o[i], sm.o[i], q);
+      for (int i = lane; i < DK; i += 32) q = fmaf(st.o[i], st.o[i], q);
       q = warp_sum(q);
       if (lane == 0) sm.red[0] = 1.0f / sqrtf(q / (float)DK + p.gnorm_eps);
     }
     __syncthreads();
     const float rn = sm.red[0];
     for (int i = tid; i < DK; i += kThreads)
-      core[i] = __float2bfloat16_rn(sm.o[i] * rn * bf16_to_f(p.gnorm_w[i]) * silu_f(sm.z[i]));
+      core[i] = __float2bfloat16_rn(st.o[i] * rn * bf16_to_f(p.gnorm_w[i]) * silu_f(st.z[i]));
+    if ((p.debug_flags & kDebugTimeline) && task == t0 && tid == 0)
+      p.ctr->tl_cta[cta][TL_REC_STATE] = globaltimer_ns();
     __syncthreads();
   }
   return true;

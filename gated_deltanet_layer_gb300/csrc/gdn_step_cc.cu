@@ -3,10 +3,10 @@
 //
 // One persistent CTA per SM runs, in order: the residual add and its norm
 // partials, the normed input image, its share of the in_proj_qkvz/in_proj_ba
-// work units (a stream-K split of (128-row tile, 64-column step) units, so
-// every CTA streams the same number of weight bytes), the epilogues of the
-// tiles it finishes last, and its share of the (row, value head) recurrence
-// tasks. Cross-CTA hand-offs go through release/acquire counters with bounded
+// work units (a stream-K split of (256-row tile, 64-column step) units, so
+// every CTA streams the same number of weight bytes), publishing a partial
+// per tile it touched, and its share of the (row, value head) recurrence
+// tasks, which reduce the partials they need. Cross-CTA hand-offs go through release/acquire counters with bounded
 // waits (vLLM #60833, Claims and Limitations: every wait is bounded and a
 // failed wait leaves a sticky failed word).
 #include "gdn_kernels.h"
@@ -24,12 +24,12 @@ __device__ __forceinline__ const __nv_bfloat16* weight_row(const StepParams& p, 
   return p.w_ba + (size_t)(valid ? n : 0) * p.H;
 }
 
-// Projection engine on CUDA cores. Thread (row = tid/4, sub = tid%4) owns one
-// weight row of the current tile and 16 of the 64 columns of each unit; its
-// f32 sums over the CTA's units of one tile are combined over the 4 lanes of
-// the row and written as this CTA's partial of the tile.
-static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
-                                     float (*xs)[kMaxRows][kKStep], int L) {
+// Projection engine on CUDA cores. Thread (row = tid/2, sub = tid%2) owns one
+// weight row of the current 256-row tile and 32 of the 64 columns of each
+// unit; its f32 sums over the CTA's units of one tile are combined over the 2
+// lanes of the row and written as this CTA's partial of the tile.
+static __device__ __forceinline__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
+                                                            float (*xs)[kMaxRows][kKStep], int L) {
   const int cta = blockIdx.x, tid = threadIdx.x, W = p.rows;
   const int ub = p.unit_begin[cta], ue = p.unit_begin[cta + 1];
   if (ub >= ue) return true;
@@ -39,7 +39,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
   __syncthreads();
   if (!sm.flag) return false;
 
-  const int row = tid >> 2, sub = tid & 3;
+  const int row = tid >> 1, sub = tid & 1;
   auto stage = [&](int u, int buf) {
     if (tid < W * 8) {
       const int ks = u % p.ksteps;
@@ -50,17 +50,17 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
       d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     }
   };
-  auto wload = [&](int u, uint4& a, uint4& b) {
+  auto wload = [&](int u, uint4 (&a)[4]) {
     const int t = u / p.ksteps, ks = u - t * p.ksteps;
     bool valid;
     const __nv_bfloat16* rp = weight_row(p, t, row, valid);
     if (valid) {
-      const __nv_bfloat16* q = rp + ks * kKStep + sub * 16;
-      a = ld_stream_v4(q);
-      b = ld_stream_v4(q + 8);
+      const __nv_bfloat16* q = rp + ks * kKStep + sub * 32;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] = ld_stream_v4(q + e * 8);
     } else {
-      a = make_uint4(0, 0, 0, 0);
-      b = a;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] = make_uint4(0, 0, 0, 0);
     }
   };
 
@@ -71,12 +71,7 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
   int seg = 0;  // segment index within this CTA's range (tile-major order)
   auto flush = [&](int t) {
 #pragma unroll
-    for (int w = 0; w < kMaxRows; ++w) {
-      float v = acc[w];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      acc[w] = v;
-    }
+    for (int w = 0; w < kMaxRows; ++w) acc[w] += __shfl_xor_sync(0xffffffffu, acc[w], 1);
     const int j = p.seg_slot[cta][seg];
     float* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
     if (sub == 0) {
@@ -86,14 +81,14 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
     }
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
-    deliver_tile_partial<kThreads>(p, sm, t, L, tid);
+    publish_tile_partial<kThreads>(p, t, tid);
   };
 
-  constexpr int D = 4;  // units of weights in flight per thread
-  uint4 wa[D], wb[D];
+  constexpr int D = 2;  // units of weights in flight per thread
+  uint4 wr[D][4];
 #pragma unroll
   for (int j = 0; j < D; ++j)
-    if (ub + j < ue) wload(ub + j, wa[j], wb[j]);
+    if (ub + j < ue) wload(ub + j, wr[j]);
   stage(ub, 0);
   __syncthreads();
 
@@ -111,31 +106,30 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
         }
         if (u + 1 < ue) stage(u + 1, (u + 1 - ub) & 1);
         const float(*x)[kKStep] = xs[(u - ub) & 1];
-        float wv[16];
-        const uint32_t ws_[8] = {wa[j].x, wa[j].y, wa[j].z, wa[j].w, wb[j].x, wb[j].y, wb[j].z, wb[j].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          wv[2 * e] = bf16_lo(ws_[e]);
-          wv[2 * e + 1] = bf16_hi(ws_[e]);
-        }
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t ws_[4] = {wr[j][e].x, wr[j][e].y, wr[j][e].z, wr[j][e].w};
+          float wv[8];
 #pragma unroll
-        for (int w = 0; w < kMaxRows; ++w) {
-          if (w < W) {
-            const float4* xr = reinterpret_cast<const float4*>(&x[w][sub * 16]);
-            const float4 x0 = xr[0], x1 = xr[1], x2 = xr[2], x3 = xr[3];
-            float s = acc[w];
-            s = fmaf(wv[0], x0.x, s);   s = fmaf(wv[1], x0.y, s);
-            s = fmaf(wv[2], x0.z, s);   s = fmaf(wv[3], x0.w, s);
-            s = fmaf(wv[4], x1.x, s);   s = fmaf(wv[5], x1.y, s);
-            s = fmaf(wv[6], x1.z, s);   s = fmaf(wv[7], x1.w, s);
-            s = fmaf(wv[8], x2.x, s);   s = fmaf(wv[9], x2.y, s);
-            s = fmaf(wv[10], x2.z, s);  s = fmaf(wv[11], x2.w, s);
-            s = fmaf(wv[12], x3.x, s);  s = fmaf(wv[13], x3.y, s);
-            s = fmaf(wv[14], x3.z, s);  s = fmaf(wv[15], x3.w, s);
-            acc[w] = s;
+          for (int h = 0; h < 4; ++h) {
+            wv[2 * h] = bf16_lo(ws_[h]);
+            wv[2 * h + 1] = bf16_hi(ws_[h]);
+          }
+#pragma unroll
+          for (int w = 0; w < kMaxRows; ++w) {
+            if (w < W) {
+              const float4* xr = reinterpret_cast<const float4*>(&x[w][sub * 32 + e * 8]);
+              const float4 x0 = xr[0], x1 = xr[1];
+              float sacc = acc[w];
+              sacc = fmaf(wv[0], x0.x, sacc); sacc = fmaf(wv[1], x0.y, sacc);
+              sacc = fmaf(wv[2], x0.z, sacc); sacc = fmaf(wv[3], x0.w, sacc);
+              sacc = fmaf(wv[4], x1.x, sacc); sacc = fmaf(wv[5], x1.y, sacc);
+              sacc = fmaf(wv[6], x1.z, sacc); sacc = fmaf(wv[7], x1.w, sacc);
+              acc[w] = sacc;
+            }
           }
         }
-        if (u + D < ue) wload(u + D, wa[j], wb[j]);
+        if (u + D < ue) wload(u + D, wr[j]);
         __syncthreads();
       }
     }
@@ -145,10 +139,18 @@ static __device__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
   return true;
 }
 
+// Dynamic shared memory of the CUDA-core kernel: the double-buffered
+// normed-input slice of the current unit.
+struct CcDynSmem {
+  alignas(16) float xs[2][kMaxRows][kKStep];
+};
+
 template <bool HAS_RES, bool STATE_BF16, int DK>
 __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_constant__ StepParams p) {
   __shared__ SmemPhases sm;
-  __shared__ __align__(16) float xs[2][kMaxRows][kKStep];
+  __shared__ SmemTask st;
+  extern __shared__ __align__(16) uint8_t cc_dyn[];
+  CcDynSmem& ds = *reinterpret_cast<CcDynSmem*>(cc_dyn);
   if (threadIdx.x == 0) sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
   __syncthreads();
   if (!sm.flag) return;  // sticky error: every later launch returns at once
@@ -156,10 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   phase_norm_partials<HAS_RES>(p, sm);
   const int L = sm.L;
   if (!phase_normed_input(p, sm, L)) return;
-  if (!phase_proj_cuda_core(p, sm, xs, L)) return;
-  phase_recurrence<DK, STATE_BF16>(p, sm, L);
+  if (!phase_proj_cuda_core(p, sm, ds.xs, L)) return;
+  phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
   tl_stamp(p, TL_END);
 }
+
+size_t cuda_core_smem_bytes() { return sizeof(CcDynSmem); }
 
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk) {
 #define GDN_PICK(R, B, D) \

@@ -168,9 +168,12 @@ gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows,
 
 /* Diagnostics: synchronise `stream` and copy the phase timeline the last
  * step recorded (handle created with GDN_DEBUG_TIMELINE). cta_stamps receives
- * num_ctas x 16 uint64 nanosecond stamps: 0 start, 1 norm partials out,
+ * num_ctas x 48 uint64 nanosecond stamps: 0 start, 1 norm partials out,
  * 2 norm wait done, 3 normed input out, 4 projection start, 5 projection end,
- * 6 first recurrence task's inputs ready, 7 end, 8 epilogues run (a count);
+ * 6 first recurrence task's inputs ready, 7 end, 8 epilogues run (a count),
+ * 9 first MMA, 10 last MMA done, 11 first weight tiles issued, 12 residual
+ * staged, 13 epilogues done; 16+n the n-th weight tile ready for the MMA and
+ * 32+n the n-th weight tile issued (n < 16, tensor-core engine);
  * tile_stamps receives num_tiles x 2 (epilogue start, end). Capacities are in
  * elements; *num_ctas and *num_tiles receive the sizes. */
 gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
