@@ -18,7 +18,7 @@ namespace {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t ctr, norm_part, xn, proj_part, total;
+  size_t ctr, plan, norm_part, xn, proj_part, total;
 };
 
 struct Plan {
@@ -29,6 +29,7 @@ struct Plan {
   unsigned short ks_first[kMaxCtas];
   unsigned char nb_slots[kMaxCtas];
   unsigned char tile_count[kMaxTiles];
+  unsigned int own_mask[kMaxCtas];
 };
 
 }  // namespace
@@ -159,9 +160,25 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
     pl->nb_slots[cta] = (unsigned char)std::min(len, 255);
     if (engine == GDN_ENGINE_TCGEN05 && len > kMaxBSlots) return GDN_ERR_UNSUPPORTED;
   }
+  // k-step owners (tensor-core engine): the first CTA whose window holds it
+  for (int cta = 0; cta < G; ++cta) pl->own_mask[cta] = 0;
+  if (engine == GDN_ENGINE_TCGEN05) {
+    for (int ks = 0; ks < KS; ++ks) {
+      int owner = -1;
+      for (int cta = 0; cta < G && owner < 0; ++cta) {
+        const int j = (ks - pl->ks_first[cta] + KS) % KS;
+        if (j < pl->nb_slots[cta]) {
+          owner = cta;
+          pl->own_mask[cta] |= 1u << j;
+        }
+      }
+      if (owner < 0) return GDN_ERR_UNSUPPORTED;
+    }
+  }
   int maxc = 1;
   for (int t = 0; t < T; ++t) {
-    if (count[t] < 1) return GDN_ERR_UNSUPPORTED;
+    // a recurrence task reduces one output's partials in one batch of <= 24
+    if (count[t] < 1 || count[t] > 24) return GDN_ERR_UNSUPPORTED;
     pl->tile_count[t] = (unsigned char)count[t];
     maxc = std::max(maxc, count[t]);
   }
@@ -173,6 +190,7 @@ Layout make_layout(const gdn_decode_config& c, const Plan& pl) {
   Layout l;
   size_t off = 0;
   l.ctr = off;        off += align_up(sizeof(WsCounters), 256);
+  l.plan = off;       off += align_up(sizeof(PlanDev), 256);
   l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(float), 256);
   l.xn = off;         off += align_up((size_t)kMaxRows * c.hidden * 2, 256);
   l.proj_part = off;  off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(float), 256);
@@ -323,7 +341,24 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
   }
   h->ws = workspace;
   h->ws_bytes = workspace_bytes;
-  if (cudaMemsetAsync(workspace, 0, h->lay.total, (cudaStream_t)stream) != cudaSuccess) {
+  PlanDev* pd = new (std::nothrow) PlanDev;
+  if (!pd) {
+    delete h;
+    return GDN_ERR_ARG;
+  }
+  memset(pd, 0, sizeof(*pd));
+  memcpy(pd->unit_begin, h->plan.unit_begin, sizeof(int) * (h->plan.G + 1));
+  memcpy(pd->seg_slot, h->plan.seg_slot, sizeof(h->plan.seg_slot[0]) * h->plan.G);
+  memcpy(pd->ks_first, h->plan.ks_first, sizeof(unsigned short) * h->plan.G);
+  memcpy(pd->nb_slots, h->plan.nb_slots, h->plan.G);
+  memcpy(pd->tile_num_ctas, h->plan.tile_count, h->plan.num_tiles);
+  memcpy(pd->own_mask, h->plan.own_mask, sizeof(unsigned int) * h->plan.G);
+  // pageable source: the copy has staged it when the call returns
+  const bool ok = cudaMemsetAsync(workspace, 0, h->lay.total, (cudaStream_t)stream) == cudaSuccess &&
+                  cudaMemcpyAsync((char*)workspace + h->lay.plan, pd, sizeof(PlanDev), cudaMemcpyHostToDevice,
+                                  (cudaStream_t)stream) == cudaSuccess;
+  delete pd;
+  if (!ok) {
     delete h;
     return GDN_ERR_CUDA;
   }
@@ -398,11 +433,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->xn = (__nv_bfloat16*)(base + h->lay.xn);
   p->proj_part = (float*)(base + h->lay.proj_part);
   p->kblock = pl.kblock;
-  memcpy(p->unit_begin, pl.unit_begin, sizeof(int) * (pl.G + 1));
-  memcpy(p->seg_slot, pl.seg_slot, sizeof(pl.seg_slot[0]) * pl.G);
-  memcpy(p->ks_first, pl.ks_first, sizeof(unsigned short) * pl.G);
-  memcpy(p->nb_slots, pl.nb_slots, pl.G);
-  memcpy(p->tile_num_ctas, pl.tile_count, pl.num_tiles);
+  p->plan = (const PlanDev*)(base + h->lay.plan);
   // weight tile maps (cached for the last weights seen)
   if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
     if (!encode_weight_map(&h->map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
@@ -453,8 +484,10 @@ gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail) {
 
 gdn_status gdn_decode_reset(gdn_decode_t* h, void* stream) {
   if (!h) return GDN_ERR_ARG;
-  return cudaMemsetAsync(h->ws, 0, h->lay.total, (cudaStream_t)stream) == cudaSuccess ? GDN_OK
-                                                                                      : GDN_ERR_CUDA;
+  // counters and the error word only; the plan stays
+  return cudaMemsetAsync((char*)h->ws + h->lay.ctr, 0, sizeof(WsCounters), (cudaStream_t)stream) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
 }
 
 void gdn_decode_destroy(gdn_decode_t* h) { delete h; }

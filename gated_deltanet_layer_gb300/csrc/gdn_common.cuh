@@ -98,18 +98,26 @@ struct StepParams {
   // swizzle); used by the tensor-core engine and for L2 prefetches.
   CUtensorMap tm_qkvz;
   CUtensorMap tm_ba;
-  // Stream-K plan of the projection work units. Unit u belongs to group
-  // g = u / kblock (k-block kb = g / num_tiles, tile t = g % num_tiles) and is
-  // k-step kb * kblock + u % kblock of tile t. CTA c takes units
-  // [unit_begin[c], unit_begin[c+1]); the i-th group it touches is its
-  // segment i, whose partial goes to slot seg_slot[c][i] of the tile. Tile t
-  // receives tile_num_ctas[t] partials. The CTA's normed-input k-steps are
-  // ks_first[c] + j (mod ksteps) for j < nb_slots[c].
+  const struct PlanDev* plan;  // stream-K plan, in the workspace (written once at create)
+};
+
+// Stream-K plan of the projection work units. Unit u belongs to group
+// g = u / kblock (k-block kb = g / num_tiles, tile t = g % num_tiles) and is
+// k-step kb * kblock + u % kblock of tile t. CTA c takes units
+// [unit_begin[c], unit_begin[c+1]); the i-th group it touches is its segment
+// i, whose partial goes to slot seg_slot[c][i] of the tile. Tile t receives
+// tile_num_ctas[t] partials. The CTA's normed-input k-steps are
+// ks_first[c] + j (mod ksteps) for j < nb_slots[c].
+// With the tensor-core engine each k-step's columns have one owner CTA (the
+// first whose window holds it): bit j of own_mask[c] marks window slot j as
+// owned; the owner writes residual_out and the norm partial of those columns.
+struct PlanDev {
   int unit_begin[kMaxCtas + 1];
   unsigned char seg_slot[kMaxCtas][kMaxSegs];
   unsigned short ks_first[kMaxCtas];
   unsigned char nb_slots[kMaxCtas];
   unsigned char tile_num_ctas[kMaxTiles];
+  unsigned int own_mask[kMaxCtas];
 };
 
 // ------------------------------------------------------------------ bf16
@@ -160,6 +168,15 @@ __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long
                                                                    unsigned long long v) {
   unsigned long long old;
   asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+// Release add without a result: the issuing thread does not wait for it.
+__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_add_release_u32(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
 __device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long long* p,

@@ -109,8 +109,18 @@ static __device__ __forceinline__ bool phase_wait_rstd(const StepParams& p, Smem
   __syncthreads();
   if (!sm.flag) return false;
   for (int w = warp; w < W; w += kWarps) {
+    // all of this lane's partials in flight at once, added in CTA order
+    constexpr int M = (kMaxCtas + 31) / 32;
+    float v[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const int c = lane + 32 * m;
+      v[m] = c < p.num_ctas ? ld_cg_f(p.norm_part + w * p.num_ctas + c) : 0.f;
+    }
     float s = 0.f;
-    for (int c = lane; c < p.num_ctas; c += 32) s += ld_cg_f(p.norm_part + w * p.num_ctas + c);
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      if (lane + 32 * m < p.num_ctas) s += v[m];
     s = warp_sum(s);
     if (lane == 0) sm.rstd[w] = 1.0f / sqrtf(s / (float)p.H + p.norm_eps);
   }
@@ -234,6 +244,10 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       else
         rawf[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
     }
+    // Per-head constants, also loaded now.
+    const float A_log_h = p.A_log[h];
+    const float dt_bias_h = bf16_to_f(p.dt_bias[h]);
+    const float gw = tid < DK ? bf16_to_f(p.gnorm_w[tid]) : 0.f;
     // Projection row of each task output, its tile and row in the tile.
     auto proj_row = [&](int i) -> int {
       if (i < DK) return kh * DK + i;
@@ -252,7 +266,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       unsigned long long tgt[6];
       for (int i = 0; i < 6; ++i) {
         ctrs[i] = &p.ctr->tile_arrive[tiles[i]];
-        tgt[i] = (unsigned long long)(L + 1) * p.tile_num_ctas[tiles[i]];
+        tgt[i] = (unsigned long long)(L + 1) * p.plan->tile_num_ctas[tiles[i]];
       }
       sm.flag = wait_counters(p, ctrs, tgt, 6, kWaitTile);
       if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
@@ -261,36 +275,42 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     if (!sm.flag) return false;
 
     // Projection outputs: partials in slot order; conv for q/k/v channels.
-    for (int i = tid; i < NOUT; i += kThreads) {
-      const int n = proj_row(i);
-      const int t = tile_of(n);
-      const int r = (n < p.Nqkvz ? n : n - p.Nqkvz) & (kTileM - 1);
-      const int nc = p.tile_num_ctas[t];
+    // A thread with two outputs (there are 4*dk + 2 of them) issues the loads
+    // of both before using any, so it costs one round trip like the others.
+    constexpr size_t kSlot = (size_t)kMaxRows * kTileM;
+    constexpr int kMaxSlots = 24;  // partials per tile handled in one batch
+    struct OutLoads {
+      float pv[kMaxSlots];
+      __nv_bfloat16 cb0, cb1, cb2;
+      uint2 cwv;
+      int n, nc;
+    };
+    auto issue = [&](int i, OutLoads& L) {
+      L.n = proj_row(i);
+      const int t = tile_of(L.n);
+      const int r = (L.n < p.Nqkvz ? L.n : L.n - p.Nqkvz) & (kTileM - 1);
+      L.nc = p.plan->tile_num_ctas[t];
       const float* src = p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
-      constexpr size_t kSlot = (size_t)kMaxRows * kTileM;
-      const bool conv = i < 3 * DK;
-      float c0 = 0.f, c1 = 0.f, c2 = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
-      if (conv) {  // old taps and weights of channel n, loaded with the partials
-        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
-        const __nv_bfloat16* cw = p.conv_w + (size_t)n * 4;
-        c0 = bf16_to_f(cs[0]); c1 = bf16_to_f(cs[1]); c2 = bf16_to_f(cs[2]);
-        w0 = bf16_to_f(cw[0]); w1 = bf16_to_f(cw[1]); w2 = bf16_to_f(cw[2]); w3 = bf16_to_f(cw[3]);
+      if (i < 3 * DK) {  // old taps and weights of channel n
+        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + L.n) * 3;
+        L.cb0 = cs[0]; L.cb1 = cs[1]; L.cb2 = cs[2];
+        L.cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)L.n * 4);
       }
+#pragma unroll
+      for (int jj = 0; jj < kMaxSlots; ++jj) L.pv[jj] = jj < L.nc ? ld_cg_f(src + (size_t)jj * kSlot) : 0.f;
+    };
+    auto finish = [&](int i, const OutLoads& L) {
       float acc = 0.f;
-      for (int j0 = 0; j0 < nc; j0 += 8) {
-        float pv8[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) pv8[jj] = (j0 + jj < nc) ? ld_cg_f(src + (size_t)(j0 + jj) * kSlot) : 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-          if (j0 + jj < nc) acc += pv8[jj];
-      }
+      for (int jj = 0; jj < kMaxSlots; ++jj)
+        if (jj < L.nc) acc += L.pv[jj];
       const float pv = round_bf16(acc);
-      if (conv) {
-        float y = w0 * c0;
-        y = fmaf(w1, c1, y);
-        y = fmaf(w2, c2, y);
-        y = fmaf(w3, pv, y);
+      if (i < 3 * DK) {
+        const float c0 = bf16_to_f(L.cb0), c1 = bf16_to_f(L.cb1), c2 = bf16_to_f(L.cb2);
+        float y = bf16_lo(L.cwv.x) * c0;
+        y = fmaf(bf16_hi(L.cwv.x), c1, y);
+        y = fmaf(bf16_lo(L.cwv.y), c2, y);
+        y = fmaf(bf16_hi(L.cwv.y), pv, y);
         y = silu_f(y);
         if (i < DK) {
           st.q[i] = y;
@@ -298,7 +318,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
           st.k[i - DK] = y;
         } else {
           st.v[i - 2 * DK] = y;
-          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;  // this head's own channel
+          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + L.n) * 3;  // this head's own channel
           cs[0] = __float2bfloat16_rn(c1);
           cs[1] = __float2bfloat16_rn(c2);
           cs[2] = __float2bfloat16_rn(pv);
@@ -313,13 +333,21 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       } else {
         st.ba[i - 4 * DK] = pv;
       }
+    };
+    if (tid < NOUT) {
+      OutLoads L0, L1;
+      const bool two = tid + kThreads < NOUT;
+      issue(tid, L0);
+      if (two) issue(tid + kThreads, L1);
+      finish(tid, L0);
+      if (two) finish(tid + kThreads, L1);
     }
-    __threadfence();
     __syncthreads();
+    unsigned int group_old = 0;
     if (tid == 0) {
-      // every thread's reads of the old q/k taps are done: count this reader
-      const unsigned int old = atomicAdd(&p.ctr->conv_group[w][kh], 1u);
-      st.last = ((old + 1) % (unsigned)p.group) == 0;
+      // every thread's reads of the old q/k taps are done (their values are
+      // used): count this reader; the result is needed only at the end
+      group_old = atom_add_release_u32(&p.ctr->conv_group[w][kh], 1u);
       if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
     }
     // L2 norms of q and k: warps 0..DK/32-1 sum q^2, the next as many k^2
@@ -337,22 +365,13 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     }
     const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
     const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
-    if (st.last) {  // the last reader of the group writes the new q/k taps
-      for (int i = tid; i < 2 * DK; i += kThreads) {
-        const int n = proj_row(i);
-        __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
-        cs[0] = __float2bfloat16_rn(st.cnew[i][0]);
-        cs[1] = __float2bfloat16_rn(st.cnew[i][1]);
-        cs[2] = __float2bfloat16_rn(st.cnew[i][2]);
-      }
-    }
     const float4 kq = *reinterpret_cast<const float4*>(&st.k[sub * 4]);
     const float4 qq = *reinterpret_cast<const float4*>(&st.q[sub * 4]);
     const float4 k4 = make_float4(kq.x * inv_k, kq.y * inv_k, kq.z * inv_k, kq.w * inv_k);
     const float4 q4 = make_float4(qq.x * inv_q, qq.y * inv_q, qq.z * inv_q, qq.w * inv_q);
-    const float sp_in = st.ba[1] + bf16_to_f(p.dt_bias[h]);
+    const float sp_in = st.ba[1] + dt_bias_h;
     const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
-    const float g = -expf(p.A_log[h]) * sp;
+    const float g = -expf(A_log_h) * sp;
     const float eg = expf(g);
     const float beta = 1.0f / (1.0f + expf(-st.ba[0]));
 
@@ -408,6 +427,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
 #pragma unroll
     for (int j = 0; j < NR; ++j)
       if (sub == 0) st.o[(j * kWarps + warp) * RPW + rw] = ov[j];
+    if (tid == 0) st.last = ((group_old + 1) % (unsigned)p.group) == 0;
     __syncthreads();
     if (warp == 0) {
       float q = 0.f;
@@ -416,9 +436,17 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       if (lane == 0) sm.red[0] = 1.0f / sqrtf(q / (float)DK + p.gnorm_eps);
     }
     __syncthreads();
+    if (st.last) {  // the last reader of the group writes the new q/k taps
+      for (int i = tid; i < 2 * DK; i += kThreads) {
+        const int n = proj_row(i);
+        __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+        cs[0] = __float2bfloat16_rn(st.cnew[i][0]);
+        cs[1] = __float2bfloat16_rn(st.cnew[i][1]);
+        cs[2] = __float2bfloat16_rn(st.cnew[i][2]);
+      }
+    }
     const float rn = sm.red[0];
-    for (int i = tid; i < DK; i += kThreads)
-      core[i] = __float2bfloat16_rn(st.o[i] * rn * bf16_to_f(p.gnorm_w[i]) * silu_f(st.z[i]));
+    if (tid < DK) core[tid] = __float2bfloat16_rn(st.o[tid] * rn * gw * silu_f(st.z[tid]));
     if ((p.debug_flags & kDebugTimeline) && task == t0 && tid == 0)
       p.ctr->tl_cta[cta][TL_REC_STATE] = globaltimer_ns();
     __syncthreads();

@@ -31,7 +31,7 @@ __device__ __forceinline__ const __nv_bfloat16* weight_row(const StepParams& p, 
 static __device__ __forceinline__ bool phase_proj_cuda_core(const StepParams& p, SmemPhases& sm,
                                                             float (*xs)[kMaxRows][kKStep], int L) {
   const int cta = blockIdx.x, tid = threadIdx.x, W = p.rows;
-  const int ub = p.unit_begin[cta], ue = p.unit_begin[cta + 1];
+  const int ub = p.plan->unit_begin[cta], ue = p.plan->unit_begin[cta + 1];
   if (ub >= ue) return true;
   if (tid == 0)
     sm.flag = wait_counter(p, &p.ctr->xn_arrive, (unsigned long long)(L + 1) * p.num_ctas, kWaitXn);
@@ -72,7 +72,7 @@ static __device__ __forceinline__ bool phase_proj_cuda_core(const StepParams& p,
   auto flush = [&](int t) {
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) acc[w] += __shfl_xor_sync(0xffffffffu, acc[w], 1);
-    const int j = p.seg_slot[cta][seg];
+    const int j = p.plan->seg_slot[cta][seg];
     float* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
     if (sub == 0) {
 #pragma unroll

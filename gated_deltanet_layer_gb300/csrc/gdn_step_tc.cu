@@ -12,14 +12,14 @@
 //   thread 0 (warp 0)   TMA producer: 256-row x 64-column bf16 weight tiles
 //                       into a ring of shared-memory stages; the first stages
 //                       and an L2 prefetch of the following units are issued
-//                       at kernel entry, so HBM streams weights while the norm
-//                       hand-off runs
+//                       as soon as the CTA has published its norm partials,
+//                       so HBM streams weights while the norm hand-off runs
 //   warp 1              allocates TMEM; its thread 0 issues tcgen05.mma into
 //                       one of two 128 x 256 f32 accumulators
-//   warp 4              drains an accumulator with tcgen05.ld (lane w holds
-//                       row w of the step), writes the CTA's partial of the
-//                       tile and publishes it; the recurrence tasks reduce the
-//                       partials they need
+//   warps 4 and 8       drain an accumulator with tcgen05.ld (lane w holds
+//                       row w of the step; each warp half of the columns),
+//                       write the CTA's partial of the tile and publish it;
+//                       the recurrence tasks reduce the partials they need
 // The A operand (xn of the CTA's k-steps, 16 rows, rows past the step's row
 // count zero) is built per launch in shared memory: r = x + residual is
 // staged while the norm hand-off is in flight and normalised in place once
@@ -44,6 +44,8 @@ constexpr int kPrefetchUnits = 4;                       // units prefetched to L
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileM);
 constexpr size_t kDynSmem = (size_t)kStages * kWBytes + (size_t)kMaxBSlots * kXBytes + kXPad +
                             (size_t)kMaxBSlots * kWinBytes + 1024;
+static_assert(kMaxRows * kMaxBSlots * 8 * sizeof(float) <= kXPad, "norm sums fit the A operand pad");
+static_assert(kMaxBSlots <= 32, "one owner bit per window slot");
 constexpr uint32_t kWaitPipe = 4;                       // error-word id of a pipeline wait
 constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on the abort path
 }  // namespace
@@ -160,13 +162,21 @@ static __device__ __forceinline__ void prefetch_states(const StepParams& p) {
 // shared memory. Slot j holds k-step (ks_first + j) mod ksteps, 16 rows x 64
 // columns bf16 in the 128-byte swizzled K-major layout (row r at r * 128
 // bytes, its 16-byte chunk c at position c ^ (r % 8)); rows past the step's
-// rows are 0. Built in two passes: r = bf16(x + residual) and the norm
-// weights are staged before the norm hand-off completes (they do not need
-// rstd), then xn = bf16(r * rstd * (1 + w)) is formed in place.
+// rows are 0. Built in two passes around the norm hand-off:
+//   stage_residual_slices: r = bf16(x + residual) of the window and the norm
+//     weights; for the k-steps this CTA owns it also writes residual_out and
+//     the sums of r^2 of 8 columns into `sq` ([row][slot * 8 + chunk])
+//   finish_normed_slices: xn = bf16(r * rstd * (1 + w)) in place.
+// One pass over x and the residual serves the residual add, the norm
+// partials and the MMA operand (vLLM #60833, Details, "x without an LDS
+// tile": each consumer builds the part of x it reads; the sums of squares
+// are handed between CTAs).
 template <bool HAS_RES>
-static __device__ __forceinline__ void stage_residual_slices(const StepParams& p, uint8_t* sX, uint8_t* sWin) {
+static __device__ __forceinline__ void stage_residual_slices(const StepParams& p, uint8_t* sX, uint8_t* sWin,
+                                                            float* sq) {
   const int cta = blockIdx.x, W = p.rows;
-  const int nb = p.nb_slots[cta], ks0 = p.ks_first[cta];
+  const int nb = p.plan->nb_slots[cta], ks0 = p.plan->ks_first[cta];
+  const unsigned own = p.plan->own_mask[cta];
   const int ntask = nb * kMaxRows * 8;  // (slot, row, 16-byte chunk)
   constexpr int B = 4;                  // tasks per thread in flight
   for (int i0 = threadIdx.x; i0 < ntask; i0 += kThreads * B) {
@@ -185,9 +195,24 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
     for (int k = 0; k < B; ++k) {
       const int i = i0 + k * kThreads;
       const int j = i >> 7, w = (i >> 3) & (kMaxRows - 1), c = i & 7;
-      if (i < ntask)
-        *reinterpret_cast<uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4)) =
-            w < W ? residual8<HAS_RES>(xv[k], qv[k]) : make_uint4(0, 0, 0, 0);
+      if (i < ntask) {
+        uint4 r = make_uint4(0, 0, 0, 0);
+        if (w < W) {
+          r = residual8<HAS_RES>(xv[k], qv[k]);
+          if ((own >> j) & 1u) {
+            const uint32_t rs[4] = {r.x, r.y, r.z, r.w};
+            float s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = bf16_lo(rs[e]), hi = bf16_hi(rs[e]);
+              s2 = fmaf(lo, lo, s2);
+              s2 = fmaf(hi, hi, s2);
+            }
+            sq[w * (kMaxBSlots * 8) + j * 8 + c] = s2;
+          }
+        }
+        *reinterpret_cast<uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4)) = r;
+      }
     }
   }
   for (int i = threadIdx.x; i < nb * 8; i += kThreads) {
@@ -197,10 +222,53 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
   }
 }
 
+// residual_out of the owned k-steps, from the staged r (after the norm
+// partials are out: these stores need not be visible to other CTAs, so they
+// stay out of the release fence).
+static __device__ __forceinline__ void write_residual_out(const StepParams& p, const uint8_t* sX) {
+  const int cta = blockIdx.x, W = p.rows;
+  const int nb = p.plan->nb_slots[cta], ks0 = p.plan->ks_first[cta];
+  const unsigned own = p.plan->own_mask[cta];
+  for (int i = threadIdx.x; i < nb * W * 8; i += kThreads) {
+    const int j = i / (W * 8), rem = i - j * (W * 8), w = rem >> 3, c = rem & 7;
+    if ((own >> j) & 1u) {
+      const size_t col = (size_t)((ks0 + j) % p.ksteps) * kKStep + c * 8;
+      *reinterpret_cast<uint4*>(p.res_out + (size_t)w * p.H + col) =
+          *reinterpret_cast<const uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4));
+    }
+  }
+}
+
+// Each row's sum of r^2 over the owned k-steps (slot-major, a fixed order),
+// published to every CTA through the norm counter. Only the threads that
+// store a partial fence; thread 0 publishes with a release add it does not
+// wait for (the launch number was read at kernel entry).
+static __device__ __forceinline__ void publish_norm_partials(const StepParams& p, const float* sq) {
+  const int cta = blockIdx.x, W = p.rows, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nb = p.plan->nb_slots[cta];
+  const unsigned own = p.plan->own_mask[cta];
+  __syncthreads();
+  for (int w = warp; w < W; w += kWarps) {
+    float s = 0.f;
+    for (int e = lane; e < nb * 8; e += 32)
+      if ((own >> (e >> 3)) & 1u) s += sq[w * (kMaxBSlots * 8) + e];
+    s = warp_sum(s);
+    if (lane == 31) {  // not lane 0: thread 32 has bulk copies in flight that a fence would wait for
+      p.norm_part[w * p.num_ctas + cta] = s;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && !((p.debug_flags & kDebugSkipNormPublish) && cta == 0))  // test hook: never publish
+    red_add_release_u64(&p.ctr->norm_arrive, 1ull);
+  tl_stamp(p, TL_NORM_OUT);
+}
+
 static __device__ __forceinline__ void finish_normed_slices(const StepParams& p, const SmemPhases& sm,
                                                             uint8_t* sX, const uint8_t* sWin) {
   const int cta = blockIdx.x, W = p.rows;
-  const int ntask = p.nb_slots[cta] * W * 8;  // (slot, row < W, chunk)
+  const int ntask = p.plan->nb_slots[cta] * W * 8;  // (slot, row < W, chunk)
   for (int i = threadIdx.x; i < ntask; i += kThreads) {
     const int j = i / (W * 8), rem = i - j * (W * 8), w = rem >> 3, c = rem & 7;
     uint4* d = reinterpret_cast<uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4));
@@ -234,7 +302,7 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
 // accumulator to the drain.
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                 uint8_t* sX, int ub, int nunits, uint32_t tmem) {
-  const int ks0 = p.ks_first[blockIdx.x], KS = p.ksteps;
+  const int ks0 = p.plan->ks_first[blockIdx.x], KS = p.ksteps;
   UnitIter it(p, ub);
   int seg = -1;
   bool seg_open = false;
@@ -270,12 +338,14 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   tl_stamp_here(p, TL_MMA_LAST);
 }
 
-// Drain (warp 4): per segment, read the 128 x 256 accumulator (lane w = row
-// w of the step, 256 weight rows), release it, write the CTA's partial of the
-// tile and publish it.
+// Drain (warps 4 and 8, both in TMEM sub-partition 0, so lane w reads row w
+// of the step): per segment, each warp reads half of the 128 x 256
+// accumulator's columns (weight rows), the accumulator is released, the CTA's
+// partial of the tile is written and published.
+constexpr int kDrainThreads = 64;
 static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared& ts, int ub, int nunits,
-                                                  uint32_t tmem, int lane) {
-  const int W = p.rows;
+                                                  uint32_t tmem, int gtid) {
+  const int W = p.rows, lane = gtid & 31, half = gtid >> 5;
   UnitIter it(p, ub);
   int seg = 0;
   for (int n = 0; n < nunits; ++seg) {
@@ -291,10 +361,10 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
     if (lane == 0) ok = pipe_wait(p, ts, &ts.acc_full[b], (seg >> 1) & 1);
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     tc::tc_fence_after();
-    float* dst = p.proj_part + ((size_t)t * p.max_contrib + p.seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
+    float* dst = p.proj_part + ((size_t)t * p.max_contrib + p.plan->seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
                  (size_t)lane * kTileM;
 #pragma unroll 1
-    for (int c = 0; c < kTileM / 32; ++c) {
+    for (int c = half * (kTileM / 64); c < (half + 1) * (kTileM / 64); ++c) {
       float v[32];
       tc::tmem_ld32(tmem + (uint32_t)b * kTileM + c * 32, v);
       if (lane < W) {
@@ -304,9 +374,9 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
       }
     }
     tc::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&ts.acc_empty[b]);
-    publish_tile_partial<32>(p, t, lane);
+    group_sync<kDrainThreads>();
+    if (gtid == 0) tc::mbar_arrive(&ts.acc_empty[b]);
+    publish_tile_partial<kDrainThreads>(p, t, gtid);
   }
 }
 
@@ -320,12 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   uint8_t* sX = sW + (size_t)kStages * kWBytes;
   uint8_t* sWin = sX + (size_t)kMaxBSlots * kXBytes + kXPad;
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
-  const int ub = p.unit_begin[cta], nunits = p.unit_begin[cta + 1] - ub;
+  const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
 
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
     tc::prefetch_tensormap(&p.tm_ba);
     sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
+    // Launch number: every CTA of the previous launches has published, none
+    // of this one has, so the count is in [L * G, (L + 1) * G).
+    sm.L = (int)(ld_relaxed_u64(&p.ctr->norm_arrive) / (unsigned long long)p.num_ctas);
     ts.abort = 0;
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
@@ -342,25 +415,28 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   if (!sm.flag) return;  // sticky error: every later launch returns at once
   tl_stamp(p, TL_START);
 
-  // Start the weight stream before any wait.
-  uint64_t pol = 0;
-  int issued = 0;
-  if (tid == 0 && nunits > 0) {
-    pol = tc::policy_evict_first();
-    issued = min(nunits, kStages);
+  // x and the residual first (few bytes; they would queue behind the weight
+  // stream in HBM), then the weight stream starts, then the norm partials go
+  // out. The sums of squares use the A operand's pad as scratch.
+  float* sq = reinterpret_cast<float*>(sX + (size_t)kMaxBSlots * kXBytes);
+  stage_residual_slices<HAS_RES>(p, sX, sWin, sq);
+  tl_stamp(p, TL_R_STAGED);
+  // The first weight tiles come from warp 1: thread 0 publishes the norm
+  // partials with a release that must not wait for these bulk copies.
+  const int issued = min(nunits, kStages);
+  if (tid == 32 && nunits > 0) {
+    const uint64_t pol0 = tc::policy_evict_first();
     UnitIter it(p, ub);
-    for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, pol);
+    for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, pol0);
     for (int n = issued; n < min(nunits, issued + kPrefetchUnits); ++n, it.next()) prefetch_weight_tile(p, it);
     tl_stamp_here(p, TL_ISSUED);
   }
-
-  phase_norm_partials<HAS_RES>(p, sm);
+  publish_norm_partials(p, sq);
   const int L = sm.L;
   if (tid == 64) prefetch_states<DK, STATE_BF16>(p);
-  stage_residual_slices<HAS_RES>(p, sX, sWin);
-  tl_stamp(p, TL_R_STAGED);
+  write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
-    if (tid == 0)  // let the weight tiles in flight land before the CTA exits
+    if (tid == 32)  // let the weight tiles in flight land before the CTA exits
       for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
     return;
   }
@@ -372,13 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tc::tc_fence_after();
   const uint32_t tmem = ts.tmem_base;
   tl_stamp(p, TL_PROJ_START);
+  int issued_total = issued;
   if (nunits > 0) {
     if (tid == 0)
-      issued = producer_loop(p, ts, sW, ub, nunits, issued, pol);
+      issued_total = producer_loop(p, ts, sW, ub, nunits, issued, tc::policy_evict_first());
     else if (tid == 32)
       mma_loop(p, ts, sW, sX, ub, nunits, tmem);
-    else if (warp == 4)
-      drain_loop(p, ts, ub, nunits, tmem, tid & 31);
+    else if (warp == 4 || warp == 8)
+      drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31));
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -387,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     // the last tile issued into each stage must land before the CTA exits
     for (int s = 0; s < kStages; ++s) {
       int last = -1;
-      for (int n = s; n < issued; n += kStages) last = n;
+      for (int n = s; n < issued_total; n += kStages) last = n;
       if (last >= 0) cleanup_wait(&ts.full[s], (last / kStages) & 1);
     }
   }

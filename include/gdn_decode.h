@@ -153,7 +153,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
  * 3 projection tile), 15..0 the CTA (deadline) or row (index error). */
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail);
 
-/* Zero the workspace on `stream` (clears the error word and all counters). */
+/* Clear the error word and all counters of the workspace on `stream`. */
 gdn_status gdn_decode_reset(gdn_decode_t* h, void* stream);
 
 /* Free the host handle. The workspace stays the caller's. */
