@@ -13,7 +13,7 @@ from . import _native
 from ._native import (GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05, GDN_OK,
                       GDN_STATE_BF16, GDN_STATE_F32, GDN_W_BF16, GDN_W_MXFP4, GdnError)
 
-__all__ = ["GdnDecode", "GdnError", "ENGINES"]
+__all__ = ["GdnDecode", "GdnError", "ENGINES", "step_static"]
 
 ENGINES = {"auto": GDN_ENGINE_AUTO, "cuda_core": GDN_ENGINE_CUDA_CORE, "tcgen05": GDN_ENGINE_TCGEN05}
 _WEIGHT_KEYS = ("input_norm_w", "qkvz", "qkvz_scales", "ba", "conv_w", "A_log", "dt_bias", "gated_norm_w")
@@ -130,3 +130,31 @@ class GdnDecode:
         st = _native.lib().gdn_decode_reset(self._h, _stream_ptr(stream))
         if st != GDN_OK:
             raise GdnError("gdn_decode_reset", st)
+
+
+def step_static(shape, x, residual, weights, state_indices, conv_state, ssm_state, core_out, residual_out,
+                *, stream=None, check: bool = False, engine: str = "auto", deadline_us: int = 0,
+                num_ctas: int = 0, debug_flags: int = 0, max_rows: int | None = None):
+    """One decode step through gdn_decode_step_static, for callers that cannot
+    allocate device memory: the library's fixed device scratch stands in for
+    the workspace and there is no handle. Every tensor, outputs included, is
+    the caller's; this call allocates nothing. `weights` is a dict of tensors
+    or a prepared `_native.Weights`. With check=True the call waits for the
+    launch and returns (status, detail word) of the device error word (read
+    and cleared); else it returns None."""
+    for t in (x, residual, state_indices, conv_state, ssm_state, core_out, residual_out):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    cfg = make_config(shape, engine=engine, deadline_us=deadline_us, num_ctas=num_ctas,
+                      debug_flags=debug_flags, max_rows=max_rows)
+    ws = weights if isinstance(weights, _native.Weights) else GdnDecode.weights_struct(weights)
+    d = ctypes.c_uint32()
+    st = _native.lib().gdn_decode_step_static(
+        ctypes.byref(cfg), x.shape[0], _ptr(x), _ptr(residual), ctypes.byref(ws), _ptr(state_indices),
+        _ptr(conv_state), _ptr(ssm_state), _ptr(core_out), _ptr(residual_out), _stream_ptr(stream),
+        ctypes.byref(d) if check else None)
+    if check and st in (GDN_OK, _native.GDN_ERR_DEADLINE, _native.GDN_ERR_INDEX, _native.GDN_ERR_FAILED):
+        return st, d.value
+    if st != GDN_OK:
+        raise GdnError("gdn_decode_step_static", st)
+    return None

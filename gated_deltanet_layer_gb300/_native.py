@@ -22,8 +22,11 @@ GDN_DEBUG_TIMELINE = 0x2
 EXPORTS = (
     "gdn_decode_workspace_bytes", "gdn_decode_create", "gdn_decode_step", "gdn_decode_check",
     "gdn_decode_reset", "gdn_decode_destroy", "gdn_status_string", "gdn_decode_launch_info",
-    "gdn_decode_plan", "gdn_decode_debug_timeline",
+    "gdn_decode_plan", "gdn_decode_debug_timeline", "gdn_decode_step_static",
 )
+
+# Size of the library's fixed device scratch (gdn_decode_step_static).
+GDN_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class Config(ctypes.Structure):
@@ -84,6 +87,9 @@ def lib() -> ctypes.CDLL:
     u64p = ctypes.POINTER(ctypes.c_uint64)
     L.gdn_decode_debug_timeline.argtypes = [vp, vp, u64p, i32, u64p, i32, i32p, i32p]
     L.gdn_decode_debug_timeline.restype = ctypes.c_int
+    L.gdn_decode_step_static.argtypes = [cfgp, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
+                                         u32p]
+    L.gdn_decode_step_static.restype = ctypes.c_int
     _lib = L
     return L
 

@@ -548,3 +548,213 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gdn_decode_step_static: the step with a fixed device scratch in place of a
+// caller workspace. It serves callers that cannot allocate device memory: a
+// host program with no PyTorch or other device allocator to hand over a
+// workspace, or a runtime whose device memory all belongs to its own pool
+// (a cudaMalloc would fail there, or fragment the pool). Nothing on this
+// path allocates: the scratch is a file-scope device array, reserved when
+// this module's device code is loaded, and the host state is file-scope too.
+// ---------------------------------------------------------------------------
+
+// One scratch per device: the layout of a caller workspace (counters, error
+// word, plan tables, norm and projection partials) for configs that fit. In
+// host code this name is only a handle for cudaGetSymbolAddress, never a
+// device address.
+static __device__ __align__(256) unsigned char g_static_scratch[GDN_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kStaticMaxDevices = 32;
+
+struct StaticDevice {
+  bool ready;                // set up for `cfg`
+  gdn_decode_config cfg;     // the caller's config the scratch is set up for
+  gdn_decode_config run;     // the same with defaults filled in
+  void* scratch;             // this device's address of g_static_scratch
+  Layout lay;
+  Plan plan;
+  PlanDev staging;           // host image of the plan tables
+  const void* map_qkvz_ptr;  // weights the cached tile maps describe
+  const void* map_ba_ptr;
+  CUtensorMap map_qkvz;
+  CUtensorMap map_ba;
+};
+StaticDevice g_static[kStaticMaxDevices];
+
+// Set the current device's scratch up for `cfg` unless it already is:
+// validate, plan, zero the counters and the error word and copy the plan
+// tables in, ordered on `stream`.
+gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stream, StaticDevice** out) {
+  if (dev < 0 || dev >= kStaticMaxDevices) return GDN_ERR_UNSUPPORTED;
+  StaticDevice& d = g_static[dev];
+  *out = &d;
+  if (d.ready && memcmp(&d.cfg, cfg, sizeof(*cfg)) == 0) return GDN_OK;
+  d.ready = false;
+  gdn_status st = validate(cfg);
+  if (st != GDN_OK) return st;
+  d.run = *cfg;
+  if (d.run.deadline_us == 0) d.run.deadline_us = 200000;
+  int device, sms, G;
+  st = device_grid(d.run, &device, &sms, &G);
+  if (st == GDN_OK) st = resolve_plan(d.run, G, &d.plan);
+  if (st != GDN_OK) return st;
+  d.lay = make_layout(d.run, d.plan);
+  if (d.lay.total > GDN_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED;  // needs a caller workspace
+  int coop = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+    return GDN_ERR_UNSUPPORTED;
+  const size_t smem = kernel_smem(d.plan.engine);
+  for (int r = 0; r < 2; ++r) {
+    const void* k = pick_kernel(d.run, d.plan.engine, r == 1);
+    int per_sm = 0;
+    if (!k || (smem && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                           cudaSuccess) ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess || per_sm < 1)
+      return GDN_ERR_UNSUPPORTED;
+  }
+  if (!d.scratch) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return GDN_ERR_CUDA;
+    d.scratch = ptr;
+  }
+  PlanDev& pd = d.staging;
+  memset(&pd, 0, sizeof(pd));
+  memcpy(pd.unit_begin, d.plan.unit_begin, sizeof(int) * (d.plan.G + 1));
+  memcpy(pd.seg_slot, d.plan.seg_slot, sizeof(d.plan.seg_slot[0]) * d.plan.G);
+  memcpy(pd.ks_first, d.plan.ks_first, sizeof(unsigned short) * d.plan.G);
+  memcpy(pd.nb_slots, d.plan.nb_slots, d.plan.G);
+  memcpy(pd.tile_num_ctas, d.plan.tile_count, d.plan.num_tiles);
+  memcpy(pd.own_mask, d.plan.own_mask, sizeof(unsigned int) * d.plan.G);
+  char* base = (char*)d.scratch;
+  // pageable source: the copy has staged it when the call returns
+  if (cudaMemsetAsync(base + d.lay.ctr, 0, sizeof(WsCounters), stream) != cudaSuccess ||
+      cudaMemcpyAsync(base + d.lay.plan, &pd, sizeof(PlanDev), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
+  d.cfg = *cfg;
+  d.ready = true;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32_t rows, const void* x,
+                                             const void* residual, const gdn_decode_weights* w,
+                                             const int32_t* state_indices, void* conv_state, void* ssm_state,
+                                             void* core_out, void* residual_out, void* stream,
+                                             uint32_t* detail) {
+  if (!cfg || !w) return GDN_ERR_ARG;
+  if (rows < 1 || rows > cfg->max_rows || cfg->max_rows > kMaxRows) return GDN_ERR_ARG;
+  if (!x || !state_indices || !conv_state || !ssm_state || !core_out || !residual_out) return GDN_ERR_ARG;
+  if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
+    return GDN_ERR_ARG;
+  const void* a16[] = {x, residual, core_out, residual_out, conv_state, ssm_state, w->input_norm_w,
+                       w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return GDN_ERR_ARG;
+  if (!aligned(state_indices, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  StaticDevice* dp = nullptr;
+  gdn_status st = static_setup(dev, cfg, s, &dp);
+  if (st != GDN_OK) return st;
+  StaticDevice& d = *dp;
+  const gdn_decode_config& c = d.run;
+  const size_t H = (size_t)c.hidden;
+  const size_t xb = (size_t)rows * H * 2;
+  const size_t coreb = (size_t)rows * c.num_v_heads * c.head_v_dim * 2;
+  const size_t sdt = c.ssm_dtype == GDN_STATE_BF16 ? 2 : 4;
+  const size_t ssmb = (size_t)c.num_slots * c.num_v_heads * c.head_v_dim * c.head_k_dim * sdt;
+  const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
+  struct Rg { const void* p; size_t n; };
+  const Rg ins[] = {{x, xb}, {residual, residual ? xb : 0}, {state_indices, (size_t)rows * 4},
+                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, (size_t)n_qkvz(c) * H * 2},
+                    {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
+                    {d.scratch, d.lay.total}};
+  const Rg outs[] = {{core_out, coreb}, {residual_out, xb}};
+  for (const Rg& o : outs)
+    for (const Rg& i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return GDN_ERR_ARG;
+  if (overlaps(core_out, coreb, residual_out, xb)) return GDN_ERR_ARG;
+  if (overlaps(conv_state, convb, ssm_state, ssmb)) return GDN_ERR_ARG;
+
+  const Plan& pl = d.plan;
+  StepParams p;
+  memset(&p, 0, sizeof(p));
+  p.H = c.hidden; p.Hk = c.num_k_heads; p.Hv = c.num_v_heads;
+  p.dk = c.head_k_dim; p.dv = c.head_v_dim; p.C = n_conv(c);
+  p.Nqkvz = n_qkvz(c); p.Nba = n_ba(c); p.num_slots = c.num_slots; p.rows = rows;
+  p.group = c.num_v_heads / c.num_k_heads;
+  p.tiles_qkvz = pl.tiles_qkvz; p.num_tiles = pl.num_tiles; p.ksteps = pl.ksteps;
+  p.norm_chunk = pl.norm_chunk; p.max_contrib = pl.max_contrib; p.num_ctas = pl.G;
+  p.norm_eps = c.norm_eps; p.gnorm_eps = c.gated_norm_eps; p.l2_eps = c.l2_eps; p.q_scale = c.q_scale;
+  p.deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
+  p.debug_flags = c.debug_flags;
+  p.x = (const __nv_bfloat16*)x;
+  p.res = (const __nv_bfloat16*)residual;
+  p.res_out = (__nv_bfloat16*)residual_out;
+  p.core_out = (__nv_bfloat16*)core_out;
+  p.idx = state_indices;
+  p.conv_state = (__nv_bfloat16*)conv_state;
+  p.ssm_state = ssm_state;
+  p.w_in = (const __nv_bfloat16*)w->input_norm_w;
+  p.w_qkvz = (const __nv_bfloat16*)w->qkvz;
+  p.w_qkvz_scales = w->qkvz_scales;
+  p.w_ba = (const __nv_bfloat16*)w->ba;
+  p.conv_w = (const __nv_bfloat16*)w->conv_w;
+  p.A_log = w->A_log;
+  p.dt_bias = (const __nv_bfloat16*)w->dt_bias;
+  p.gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
+  char* base = (char*)d.scratch;
+  p.ctr = (WsCounters*)(base + d.lay.ctr);
+  p.norm_part = (float*)(base + d.lay.norm_part);
+  p.xn = (__nv_bfloat16*)(base + d.lay.xn);
+  p.proj_part = (float*)(base + d.lay.proj_part);
+  p.kblock = pl.kblock;
+  p.plan = (const PlanDev*)(base + d.lay.plan);
+  if (d.map_qkvz_ptr != w->qkvz || d.map_ba_ptr != w->ba) {
+    if (!encode_weight_map(&d.map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
+        !encode_weight_map(&d.map_ba, w->ba, n_ba(c), c.hidden)) {
+      d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
+      return GDN_ERR_CUDA;
+    }
+    d.map_qkvz_ptr = w->qkvz;
+    d.map_ba_ptr = w->ba;
+  }
+  p.tm_qkvz = d.map_qkvz;
+  p.tm_ba = d.map_ba;
+
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(pl.G);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = kernel_smem(pl.engine);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&lc, pick_kernel(c, pl.engine, residual != nullptr), args) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (!detail) return GDN_OK;
+
+  uint32_t word = 0;
+  const char* err = base + d.lay.ctr + offsetof(WsCounters, error);
+  if (cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  *detail = word;
+  if (word == 0) return GDN_OK;
+  // read and cleared: the next call starts from zero counters
+  if (cudaMemsetAsync(base + d.lay.ctr, 0, sizeof(WsCounters), s) != cudaSuccess) return GDN_ERR_CUDA;
+  const uint32_t code = word >> 24;
+  if (code == GDN_ERR_DEADLINE) return GDN_ERR_DEADLINE;
+  if (code == GDN_ERR_INDEX) return GDN_ERR_INDEX;
+  return GDN_ERR_FAILED;
+}

@@ -196,6 +196,52 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
                            uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
                            int32_t* kblock);
 
+/* Largest scratch gdn_decode_step_static can use, in bytes (4 MiB). */
+#define GDN_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* One decode step, computed exactly as gdn_decode_step computes it, for
+ * callers that cannot allocate device memory: a C or C++ host program with no
+ * PyTorch or other device allocator to provide a workspace, or a runtime
+ * whose device memory is all handed out by its own pool, so that a
+ * cudaMalloc would fail or fragment it. The pages this library follows have
+ * no counterpart of this call.
+ *
+ * No handle and no workspace: the scratch (counters, sticky error word, plan
+ * tables, norm and projection partials) is a fixed device array of
+ * GDN_STATIC_SCRATCH_BYTES inside the library, one per device, held by every
+ * GPU that loads the library's device code until the process exits. The call
+ * allocates nothing on the host or the device, through no API or library.
+ *
+ * Set-up: the first call on a device (with that device current), and every
+ * later call whose *cfg differs from the previous call's on that device,
+ * first validates the config, looks up the scratch array's device address,
+ * zeroes its counters and error word (they must start at zero: each launch
+ * waits for counts that grow from zero) and copies the plan tables into it,
+ * stream-ordered on `stream`. That first call must come before any stream
+ * capture on `stream`. The other parts of the scratch need no initial value;
+ * they keep whatever the last call left there.
+ *
+ * Arguments, layouts and the launch are those of gdn_decode_step; `cfg` takes
+ * the place of the handle. The scratch is shared by every call on a device:
+ * two calls whose launches overlap on the GPU (on different streams, or from
+ * different host threads) race on it and give wrong results or deadline
+ * errors. Calls from several host threads must be serialised by the caller.
+ *
+ * Errors: GDN_ERR_ARG and GDN_ERR_UNSUPPORTED as for gdn_decode_create and
+ * gdn_decode_step, before any launch; GDN_ERR_UNSUPPORTED also when the
+ * config's scratch would exceed GDN_STATIC_SCRATCH_BYTES (the layer front of
+ * one tensor-parallel shard fits; a full 8192-wide layer with 64 value heads
+ * does not: use gdn_decode_create with a workspace). Device errors are sticky
+ * in the scratch as for a handle: if `detail` is not NULL the call waits for
+ * its launch, stores the error word in *detail (layout of gdn_decode_check),
+ * returns its status, and if it is non-zero clears the word and the counters
+ * so the next call runs. With detail == NULL the call does not synchronise. */
+gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32_t rows, const void* x,
+                                  const void* residual, const gdn_decode_weights* w,
+                                  const int32_t* state_indices, void* conv_state,
+                                  void* ssm_state, void* core_out, void* residual_out,
+                                  void* stream, uint32_t* detail);
+
 #ifdef __cplusplus
 }
 #endif
