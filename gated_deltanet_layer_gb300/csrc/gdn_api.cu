@@ -42,6 +42,7 @@ struct gdn_decode {
   size_t ws_bytes;
   Layout lay;
   Plan plan;
+  bool pdl;  // launch with programmatic stream serialisation
   // TMA maps of the last weights a step used
   const void* map_qkvz_ptr;
   const void* map_ba_ptr;
@@ -309,6 +310,7 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
   if (!h) return GDN_ERR_ARG;
   h->cfg = *cfg;
   h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
+  h->pdl = true;
   if (h->cfg.deadline_us == 0) h->cfg.deadline_us = 200000;
   int G;
   st = device_grid(h->cfg, &h->device, &h->num_sms, &G);
@@ -455,13 +457,26 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = kernel_smem(pl.engine);
   lc.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
+  // Cooperative: every CTA resident at once (they wait on one another).
+  // Programmatic stream serialisation: the launch may start while the
+  // previous launch in the stream finishes; the kernel reads nothing but the
+  // weights before its griddepcontrol.wait.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = h->pdl ? 2 : 1;
   void* args[] = {p};
-  const cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
+  cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
+  if (e != cudaSuccess && h->pdl) {
+    // the runtime refused the pair of attributes: launch without overlap
+    (void)cudaGetLastError();
+    h->pdl = false;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelExC(&lc, kern, args);
+  }
   delete p;
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -186,6 +186,16 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long
   return old;
 }
 
+// Programmatic dependent launch. wait: block until the launches this one
+// depends on in the stream have completed and their writes are visible (a
+// no-op when the launch was not made with programmatic serialisation).
+// launch_dependents: let the next such launch in the stream be scheduled
+// (its CTAs still need an SM that this launch's CTAs free).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   __shared__ SmemTask st;
   extern __shared__ __align__(16) uint8_t cc_dyn[];
   CcDynSmem& ds = *reinterpret_cast<CcDynSmem*>(cc_dyn);
+  griddep_wait();  // the previous step's writes first
+  griddep_launch_dependents();
   if (threadIdx.x == 0) sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
   __syncthreads();
   if (!sm.flag) return;  // sticky error: every later launch returns at once

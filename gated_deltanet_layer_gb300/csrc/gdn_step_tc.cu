@@ -40,7 +40,7 @@ constexpr uint32_t kXBytes = kMaxRows * kKStep * 2;     // 2 KB normed-input sli
 constexpr uint32_t kXPad = (128 - kMaxRows) * 128;      // 14 KB an M = 128 MMA reads past the last slice
 constexpr uint32_t kWinBytes = kKStep * 2;              // input-norm weights of one k-step
 constexpr uint32_t kTmemCols = 2 * kTileM;              // two 128 x 256 f32 accumulators
-constexpr int kPrefetchUnits = 4;                       // units prefetched to L2 ahead of the ring
+constexpr int kPrefetchUnits = 12;                      // units prefetched to L2 ahead of the ring
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileM);
 constexpr size_t kDynSmem = (size_t)kStages * kWBytes + (size_t)kMaxBSlots * kXBytes + kXPad +
                             (size_t)kMaxBSlots * kWinBytes + 1024;
@@ -395,10 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
     tc::prefetch_tensormap(&p.tm_ba);
-    sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
-    // Launch number: every CTA of the previous launches has published, none
-    // of this one has, so the count is in [L * G, (L + 1) * G).
-    sm.L = (int)(ld_relaxed_u64(&p.ctr->norm_arrive) / (unsigned long long)p.num_ctas);
     ts.abort = 0;
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
@@ -412,25 +408,41 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     tc::fence_mbar_init();
   }
   __syncthreads();
-  if (!sm.flag) return;  // sticky error: every later launch returns at once
-  tl_stamp(p, TL_START);
 
-  // x and the residual first (few bytes; they would queue behind the weight
-  // stream in HBM), then the weight stream starts, then the norm partials go
-  // out. The sums of squares use the A operand's pad as scratch.
-  float* sq = reinterpret_cast<float*>(sX + (size_t)kMaxBSlots * kXBytes);
-  stage_residual_slices<HAS_RES>(p, sX, sWin, sq);
-  tl_stamp(p, TL_R_STAGED);
-  // The first weight tiles come from warp 1: thread 0 publishes the norm
-  // partials with a release that must not wait for these bulk copies.
+  // The weights are the one input no step writes, so their stream starts
+  // before the previous step is known to be done: with programmatic
+  // dependent launch this CTA runs as soon as the previous step's CTA on its
+  // SM has exited, and the first weight tiles (into the ring) and an L2
+  // prefetch of the following units overlap the previous step's tail.
   const int issued = min(nunits, kStages);
   if (tid == 32 && nunits > 0) {
     const uint64_t pol0 = tc::policy_evict_first();
     UnitIter it(p, ub);
     for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, pol0);
     for (int n = issued; n < min(nunits, issued + kPrefetchUnits); ++n, it.next()) prefetch_weight_tile(p, it);
-    tl_stamp_here(p, TL_ISSUED);
   }
+  griddep_wait();  // from here on the previous step's writes are visible
+  griddep_launch_dependents();
+  if (tid == 0) {
+    sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
+    // Launch number: every CTA of the previous launches has published, none
+    // of this one has, so the count is in [L * G, (L + 1) * G).
+    sm.L = (int)(ld_relaxed_u64(&p.ctr->norm_arrive) / (unsigned long long)p.num_ctas);
+  }
+  __syncthreads();
+  if (!sm.flag) {  // sticky error: every later launch returns at once
+    if (tid == 32)  // once the weight tiles in flight have landed
+      for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
+    return;
+  }
+  tl_stamp(p, TL_START);
+  if (tid == 32) tl_stamp_here(p, TL_ISSUED);
+
+  // x and the residual, then the norm partials go out. The sums of squares
+  // use the A operand's pad as scratch.
+  float* sq = reinterpret_cast<float*>(sX + (size_t)kMaxBSlots * kXBytes);
+  stage_residual_slices<HAS_RES>(p, sX, sWin, sq);
+  tl_stamp(p, TL_R_STAGED);
   publish_norm_partials(p, sq);
   const int L = sm.L;
   if (tid == 64) prefetch_states<DK, STATE_BF16>(p);
