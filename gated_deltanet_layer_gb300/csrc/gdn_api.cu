@@ -30,7 +30,15 @@ struct Plan {
   unsigned char nb_slots[kMaxCtas];
   unsigned char tile_count[kMaxTiles];
   unsigned int own_mask[kMaxCtas];
+  // tensor-core engine: weight ring depth, normed-input window (k-steps),
+  // the pad past it, and the launch's dynamic shared memory
+  int stages, xslots;
+  unsigned int xpad;
+  size_t smem;
 };
+
+// Shared memory a CTA may use on sm_100-class GPUs (opt-in limit per block).
+constexpr size_t kSmemOptin = 232448;
 
 }  // namespace
 
@@ -184,6 +192,23 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
     maxc = std::max(maxc, count[t]);
   }
   pl->max_contrib = maxc;
+  if (engine == GDN_ENGINE_TCGEN05) {
+    // the ring takes what the window leaves: 2..6 tiles of 32 KB
+    int xs = 1;
+    for (int cta = 0; cta < G; ++cta) xs = std::max(xs, (int)pl->nb_slots[cta]);
+    pl->xslots = xs;
+    pl->xpad = tensor_core_xpad(xs);
+    const size_t fixed = tensor_core_smem_bytes(0, xs);
+    const size_t avail = kSmemOptin - tensor_core_static_smem() - 1024;
+    if (fixed + 2 * (size_t)kTileM * kKStep * 2 > avail) return GDN_ERR_UNSUPPORTED;
+    pl->stages = (int)std::min<size_t>((avail - fixed) / ((size_t)kTileM * kKStep * 2),
+                                       (size_t)tensor_core_max_stages());
+    pl->smem = tensor_core_smem_bytes(pl->stages, xs);
+  } else {
+    pl->stages = pl->xslots = 0;
+    pl->xpad = 0;
+    pl->smem = cuda_core_smem_bytes();
+  }
   return GDN_OK;
 }
 
@@ -223,8 +248,14 @@ const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
                                       : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
-size_t kernel_smem(int engine) {
-  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_smem_bytes() : cuda_core_smem_bytes();
+size_t kernel_smem(const Plan& pl) { return pl.smem; }
+
+// Launch fields of the plan that the kernels read.
+void set_plan_params(const Plan& pl, StepParams* p) {
+  p->tiles_qkvz = pl.tiles_qkvz; p->num_tiles = pl.num_tiles; p->ksteps = pl.ksteps;
+  p->norm_chunk = pl.norm_chunk; p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
+  p->kblock = pl.kblock;
+  p->stages = pl.stages; p->xslots = pl.xslots; p->xpad = pl.xpad;
 }
 
 // The engine a config runs with and its plan: the requested engine, or for
@@ -330,7 +361,7 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
     return GDN_ERR_UNSUPPORTED;
   }
   // Every CTA of the persistent grid must be co-resident.
-  const size_t smem = kernel_smem(h->plan.engine);
+  const size_t smem = kernel_smem(h->plan);
   for (int r = 0; r < 2; ++r) {
     const void* k = pick_kernel(h->cfg, h->plan.engine, r == 1);
     int per_sm = 0;
@@ -409,8 +440,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->dk = c.head_k_dim; p->dv = c.head_v_dim; p->C = n_conv(c);
   p->Nqkvz = n_qkvz(c); p->Nba = n_ba(c); p->num_slots = c.num_slots; p->rows = rows;
   p->group = c.num_v_heads / c.num_k_heads;
-  p->tiles_qkvz = pl.tiles_qkvz; p->num_tiles = pl.num_tiles; p->ksteps = pl.ksteps;
-  p->norm_chunk = pl.norm_chunk; p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
+  set_plan_params(pl, p);
   p->norm_eps = c.norm_eps; p->gnorm_eps = c.gated_norm_eps; p->l2_eps = c.l2_eps; p->q_scale = c.q_scale;
   p->deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
   p->debug_flags = c.debug_flags;
@@ -434,7 +464,6 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->norm_part = (float*)(base + h->lay.norm_part);
   p->xn = (__nv_bfloat16*)(base + h->lay.xn);
   p->proj_part = (float*)(base + h->lay.proj_part);
-  p->kblock = pl.kblock;
   p->plan = (const PlanDev*)(base + h->lay.plan);
   // weight tile maps (cached for the last weights seen)
   if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
@@ -455,7 +484,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(pl.G);
   lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = kernel_smem(pl.engine);
+  lc.dynamicSmemBytes = kernel_smem(pl);
   lc.stream = (cudaStream_t)stream;
   // Cooperative: every CTA resident at once (they wait on one another).
   // Programmatic stream serialisation: the launch may start while the
@@ -621,7 +650,7 @@ gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stre
   int coop = 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
     return GDN_ERR_UNSUPPORTED;
-  const size_t smem = kernel_smem(d.plan.engine);
+  const size_t smem = kernel_smem(d.plan);
   for (int r = 0; r < 2; ++r) {
     const void* k = pick_kernel(d.run, d.plan.engine, r == 1);
     int per_sm = 0;
@@ -704,8 +733,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   p.dk = c.head_k_dim; p.dv = c.head_v_dim; p.C = n_conv(c);
   p.Nqkvz = n_qkvz(c); p.Nba = n_ba(c); p.num_slots = c.num_slots; p.rows = rows;
   p.group = c.num_v_heads / c.num_k_heads;
-  p.tiles_qkvz = pl.tiles_qkvz; p.num_tiles = pl.num_tiles; p.ksteps = pl.ksteps;
-  p.norm_chunk = pl.norm_chunk; p.max_contrib = pl.max_contrib; p.num_ctas = pl.G;
+  set_plan_params(pl, &p);
   p.norm_eps = c.norm_eps; p.gnorm_eps = c.gated_norm_eps; p.l2_eps = c.l2_eps; p.q_scale = c.q_scale;
   p.deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
   p.debug_flags = c.debug_flags;
@@ -729,7 +757,6 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   p.norm_part = (float*)(base + d.lay.norm_part);
   p.xn = (__nv_bfloat16*)(base + d.lay.xn);
   p.proj_part = (float*)(base + d.lay.proj_part);
-  p.kblock = pl.kblock;
   p.plan = (const PlanDev*)(base + d.lay.plan);
   if (d.map_qkvz_ptr != w->qkvz || d.map_ba_ptr != w->ba) {
     if (!encode_weight_map(&d.map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
@@ -747,7 +774,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(pl.G);
   lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = kernel_smem(pl.engine);
+  lc.dynamicSmemBytes = kernel_smem(pl);
   lc.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

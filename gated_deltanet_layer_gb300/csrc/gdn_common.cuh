@@ -42,6 +42,8 @@ struct WsCounters {
   unsigned long long pad1[15];
   unsigned int error;               // sticky error word
   unsigned int pad2[63];
+  unsigned long long exit_count;    // +1 per CTA as it ends a step (a hint only)
+  unsigned long long pad3[15];
   unsigned long long tile_arrive[kMaxTiles];  // +1 per partial delivered to a tile
   // +1 per recurrence task of (row, key head) once it has read the old q/k
   // conv state; every launch adds the group size G or nothing, so the task
@@ -69,6 +71,9 @@ struct StepParams {
   int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
   int max_contrib;     // most CTAs contributing to one tile
   int num_ctas;
+  int stages;          // weight tiles in flight per CTA (tensor-core engine)
+  int xslots;          // normed-input k-steps a CTA keeps in shared memory
+  unsigned int xpad;   // bytes past the window an MMA may read (and norm-sum scratch)
   float norm_eps, gnorm_eps, l2_eps, q_scale;
   unsigned long long deadline_ns;
   int debug_flags;
@@ -194,6 +199,13 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// A CTA ends its step: count it out (relaxed; read by the next step's CTAs
+// only to decide when to start their weight stream).
+__device__ __forceinline__ void count_exit(const StepParams& p) {
+  if (threadIdx.x == 0)
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(&p.ctr->exit_count) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {

@@ -11,9 +11,14 @@ namespace gdn {
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk);
 size_t cuda_core_smem_bytes();
 
-// The same for the tensor-core (tcgen05) projection engine, and the dynamic
-// shared memory its launch needs.
+// The same for the tensor-core (tcgen05) projection engine. Its dynamic
+// shared memory depends on the weight ring's depth (stages) and the normed
+// input window (xslots k-steps); the pad past the window; the static shared
+// memory of the kernel; the deepest ring it supports.
 const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk);
-size_t tensor_core_smem_bytes();
+size_t tensor_core_smem_bytes(int stages, int xslots);
+uint32_t tensor_core_xpad(int xslots);
+size_t tensor_core_static_smem();
+int tensor_core_max_stages();
 
 }  // namespace gdn

@@ -1,21 +1,25 @@
 // GDN decode-step launch with the projections on the 5th-generation tensor
 // cores (tcgen05.mma, accumulators in TMEM, weight tiles fed by TMA).
 //
-// The MMA is D[m][n] += A[m][k] B[n][k] with A = the normed input xn (M = 128:
-// the step's up to 16 rows; the MMA also reads 112 rows of whatever lies past
+// The MMA is D[m][n] += A[m][k] B[n][k] with A = the normed input xn (M = 64:
+// the step's up to 16 rows; the MMA also reads 48 rows of whatever lies past
 // a slice, whose results land in TMEM lanes nobody reads) and B = a 256-row
-// weight tile (N = 256, K-major, 128-byte swizzle). A 128x16x16 MMA costs the
-// tensor core about as much issue time as a 128x256x16 one, so the weights
-// take the wide N side: one instruction consumes 8 KB of weights.
+// weight tile (N = 256, K-major, 128-byte swizzle). The tensor core's time
+// per instruction follows N x K alone (128 cycles at N = 256, the same for
+// M = 64 and M = 128; 64 cycles at N = 128), so the weights take the wide N
+// side, one instruction consumes 8 KB of weights, and M is the smallest
+// shape whose D rows 0..15 sit in TMEM lanes 0..15.
 //
 // One persistent CTA per SM. Roles during the projection:
-//   thread 0 (warp 0)   TMA producer: 256-row x 64-column bf16 weight tiles
-//                       into a ring of shared-memory stages; the first stages
-//                       and an L2 prefetch of the following units are issued
-//                       as soon as the CTA has published its norm partials,
-//                       so HBM streams weights while the norm hand-off runs
+//   thread 32           fills the ring's first stages (2..6 tiles of 256 rows
+//                       x 64 columns, as shared memory allows) before the norm
+//                       hand-off: as soon as the CTA starts when the previous
+//                       step is still running (programmatic dependent
+//                       launch), else right after issuing its x and residual
+//                       loads, so HBM streams weights while the hand-off runs
+//   thread 0 (warp 0)   TMA producer: refills each stage the MMAs release
 //   warp 1              allocates TMEM; its thread 0 issues tcgen05.mma into
-//                       one of two 128 x 256 f32 accumulators
+//                       one of two 64 x 256 f32 accumulators (512 columns)
 //   warps 4 and 8       drain an accumulator with tcgen05.ld (lane w holds
 //                       row w of the step; each warp half of the columns),
 //                       write the CTA's partial of the tile and publish it;
@@ -34,30 +38,27 @@
 namespace gdn {
 
 namespace {
-constexpr int kStages = 3;                              // weight tiles in flight per CTA
+constexpr int kMaxStages = 6;                           // weight tiles in flight per CTA (the plan picks)
 constexpr uint32_t kWBytes = kTileM * kKStep * 2;       // 32 KB weight tile (B operand)
 constexpr uint32_t kXBytes = kMaxRows * kKStep * 2;     // 2 KB normed-input slice (A rows 0..15)
-constexpr uint32_t kXPad = (128 - kMaxRows) * 128;      // 14 KB an M = 128 MMA reads past the last slice
+constexpr uint32_t kXPadMin = (64 - kMaxRows) * 128;    // 6 KB an M = 64 MMA reads past the last slice
 constexpr uint32_t kWinBytes = kKStep * 2;              // input-norm weights of one k-step
 constexpr uint32_t kTmemCols = 2 * kTileM;              // two 128 x 256 f32 accumulators
-constexpr int kPrefetchUnits = 12;                      // units prefetched to L2 ahead of the ring
-constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileM);
-constexpr size_t kDynSmem = (size_t)kStages * kWBytes + (size_t)kMaxBSlots * kXBytes + kXPad +
-                            (size_t)kMaxBSlots * kWinBytes + 1024;
-static_assert(kMaxRows * kMaxBSlots * 8 * sizeof(float) <= kXPad, "norm sums fit the A operand pad");
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(64, kTileM);
 static_assert(kMaxBSlots <= 32, "one owner bit per window slot");
 constexpr uint32_t kWaitPipe = 4;                       // error-word id of a pipeline wait
 constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on the abort path
 }  // namespace
 
 struct TcShared {
-  uint64_t full[kStages];   // weight tile landed (TMA complete_tx)
-  uint64_t empty[kStages];  // MMAs of the stage done (tcgen05.commit)
+  uint64_t full[kMaxStages];   // weight tile landed (TMA complete_tx)
+  uint64_t empty[kMaxStages];  // MMAs of the stage done (tcgen05.commit)
   uint64_t acc_full[2];     // accumulator ready for the drain
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
   uint32_t tmem_base;
   int abort;
+  int early;   // the weight stream started before the previous step was done
 };
 
 // Walks a CTA's units in plan order without divisions: unit u is k-step
@@ -121,19 +122,25 @@ __device__ __forceinline__ const CUtensorMap* weight_map(const StepParams& p, in
   return &p.tm_ba;
 }
 
+// Unit n's weight tile into ring stage s.
 __device__ __forceinline__ void issue_weight_tile(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                  const UnitIter& it, int n, uint64_t pol) {
+                                                  const UnitIter& it, int n, int s, uint64_t pol) {
   int row0;
   const CUtensorMap* m = weight_map(p, it.t, row0);
-  const int s = n % kStages;
   tc::mbar_arrive_expect_tx(&ts.full[s], kWBytes);
   tc::tma_load_2d(sW + (size_t)s * kWBytes, m, it.ks * kKStep, row0, &ts.full[s], pol);
   if (n < 16) tl_stamp_here(p, TL_UNIT_ISSUED + n);
 }
 
-__device__ __forceinline__ void prefetch_weight_tile(const StepParams& p, const UnitIter& it) {
-  int row0;
-  tc::tma_prefetch_2d(weight_map(p, it.t, row0), it.ks * kKStep, row0);
+// The CTA's weight stream: the first `issued` units into the ring (one
+// thread).
+static __device__ __forceinline__ void start_weight_stream(const StepParams& p, TcShared& ts, uint8_t* sW,
+                                                           int ub, int nunits, int issued) {
+  if (nunits <= 0) return;
+  const uint64_t pol0 = tc::policy_evict_first();
+  UnitIter it(p, ub);
+  for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, n, pol0);
+  tl_stamp_here(p, TL_ISSUED);
 }
 
 // L2 prefetch of the state this CTA's recurrence tasks read, and of the conv
@@ -171,15 +178,18 @@ static __device__ __forceinline__ void prefetch_states(const StepParams& p) {
 // partials and the MMA operand (vLLM #60833, Details, "x without an LDS
 // tile": each consumer builds the part of x it reads; the sums of squares
 // are handed between CTAs).
-template <bool HAS_RES>
+// `after_issue` runs once every thread has issued the loads of the first
+// batch (before any of them is used), so what it starts queues behind them.
+template <bool HAS_RES, typename F>
 static __device__ __forceinline__ void stage_residual_slices(const StepParams& p, uint8_t* sX, uint8_t* sWin,
-                                                            float* sq) {
+                                                            float* sq, F after_issue) {
   const int cta = blockIdx.x, W = p.rows;
   const int nb = p.plan->nb_slots[cta], ks0 = p.plan->ks_first[cta];
   const unsigned own = p.plan->own_mask[cta];
   const int ntask = nb * kMaxRows * 8;  // (slot, row, 16-byte chunk)
   constexpr int B = 4;                  // tasks per thread in flight
-  for (int i0 = threadIdx.x; i0 < ntask; i0 += kThreads * B) {
+  for (int b0 = 0; b0 == 0 || b0 < ntask; b0 += kThreads * B) {  // the first batch runs even if empty
+    const int i0 = b0 + threadIdx.x;
     uint4 xv[B], qv[B];
 #pragma unroll
     for (int k = 0; k < B; ++k) {
@@ -190,6 +200,10 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
         xv[k] = ld_stream_v4(p.x + (size_t)w * p.H + col);
         qv[k] = HAS_RES ? ld_stream_v4(p.res + (size_t)w * p.H + col) : xv[k];
       }
+    }
+    if (b0 == 0) {
+      __syncthreads();
+      after_issue();
     }
 #pragma unroll
     for (int k = 0; k < B; ++k) {
@@ -208,7 +222,7 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
               s2 = fmaf(lo, lo, s2);
               s2 = fmaf(hi, hi, s2);
             }
-            sq[w * (kMaxBSlots * 8) + j * 8 + c] = s2;
+            sq[w * (p.xslots * 8) + j * 8 + c] = s2;
           }
         }
         *reinterpret_cast<uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4)) = r;
@@ -252,7 +266,7 @@ static __device__ __forceinline__ void publish_norm_partials(const StepParams& p
   for (int w = warp; w < W; w += kWarps) {
     float s = 0.f;
     for (int e = lane; e < nb * 8; e += 32)
-      if ((own >> (e >> 3)) & 1u) s += sq[w * (kMaxBSlots * 8) + e];
+      if ((own >> (e >> 3)) & 1u) s += sq[w * (p.xslots * 8) + e];
     s = warp_sum(s);
     if (lane == 31) {  // not lane 0: thread 32 has bulk copies in flight that a fence would wait for
       p.norm_part[w * p.num_ctas + cta] = s;
@@ -277,21 +291,20 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
 }
 
 // TMA producer: weight tiles `issued`.. into the ring, each into a stage the
-// MMAs have released; keeps an L2 prefetch kPrefetchUnits units ahead.
-// Returns the number of units issued.
+// MMAs have released. Returns the number of units issued. (An L2 prefetch
+// ahead of the ring was measured: the tensor form does not bring tiles in
+// early, and per-row prefetches delay the latency-bound norm hand-off more
+// than they shorten the projection.)
 static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, int ub,
                                                    int nunits, int issued, uint64_t pol) {
   UnitIter it(p, ub + issued);
-  UnitIter pf(p, min(ub + issued + kPrefetchUnits, ub + nunits - 1));
+  int s = issued % p.stages;
+  uint32_t ph = (uint32_t)(issued / p.stages) & 1;
   for (int n = issued; n < nunits; ++n) {
-    const int s = n % kStages;
-    if (!pipe_wait(p, ts, &ts.empty[s], ((n / kStages) & 1) ^ 1)) return n;
-    issue_weight_tile(p, ts, sW, it, n, pol);
+    if (!pipe_wait(p, ts, &ts.empty[s], ph ^ 1)) return n;
+    issue_weight_tile(p, ts, sW, it, n, s, pol);
     it.next();
-    if (n + kPrefetchUnits < nunits) {
-      prefetch_weight_tile(p, pf);
-      pf.next();
-    }
+    if (++s == p.stages) { s = 0; ph ^= 1; }
   }
   return nunits;
 }
@@ -302,29 +315,35 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
 // accumulator to the drain.
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                 uint8_t* sX, int ub, int nunits, uint32_t tmem) {
-  const int ks0 = p.plan->ks_first[blockIdx.x], KS = p.ksteps;
+  // Stage and phase advance incrementally: a division per unit by the
+  // runtime ring depth costs the loop more than the tensor core's own time.
+  const int ks0 = p.plan->ks_first[blockIdx.x], KS = p.ksteps, S = p.stages;
   UnitIter it(p, ub);
   int seg = -1;
   bool seg_open = false;
+  int s = 0;
+  uint32_t ph = 0;
+  const uint32_t sw0 = tc::smem_u32(sW), sx0 = tc::smem_u32(sX);
   for (int n = 0; n < nunits; ++n) {
-    const int s = n % kStages;
     const bool first = !seg_open;
     if (first) {
       ++seg;
       seg_open = true;
       if (!pipe_wait(p, ts, &ts.acc_empty[seg & 1], ((seg >> 1) & 1) ^ 1)) break;
+      tc::tc_fence_after();  // these MMAs come after the drain's tcgen05.ld of this accumulator
     }
-    if (!pipe_wait(p, ts, &ts.full[s], (n / kStages) & 1)) break;
-    tc::tc_fence_after();
-    if (n == 0) tl_stamp_here(p, TL_MMA_FIRST);
-    if (n < 16) tl_stamp_here(p, TL_UNIT_READY + n);
+    // The phase makes the stage's TMA bytes visible to the MMA (both async
+    // proxy): no tcgen05 fence per unit.
+    if (!tc::mbar_try_wait(&ts.full[s], ph))
+      if (!pipe_wait(p, ts, &ts.full[s], ph)) break;
     int slot = it.ks - ks0;
     if (slot < 0) slot += KS;
-    const uint64_t ad = tc::sdesc_k_sw128(tc::smem_u32(sX + (size_t)slot * kXBytes));
-    const uint64_t bd = tc::sdesc_k_sw128(tc::smem_u32(sW + (size_t)s * kWBytes));
+    if (n == 0) tl_stamp_here(p, TL_MMA_FIRST);
+    const uint64_t ad = tc::sdesc_k_sw128(sx0 + (uint32_t)slot * kXBytes);
+    const uint64_t bd = tc::sdesc_k_sw128(sw0 + (uint32_t)s * kWBytes);
     const uint32_t d = tmem + (uint32_t)(seg & 1) * kTileM;
 #pragma unroll
-    for (int k = 0; k < kKStep / 16; ++k)  // +32 bytes along K inside the swizzle atom
+    for (int k = 0; k < kKStep / 16; ++k)
       tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdesc, (first && k == 0) ? 0u : 1u);
     tc::mma_commit(&ts.empty[s]);
     if (n + 1 == nunits || it.group_end()) {
@@ -332,6 +351,7 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
       seg_open = false;
     }
     it.next();
+    if (++s == S) { s = 0; ph ^= 1; }
   }
   tc::mma_commit(&ts.mma_done);
   cleanup_wait(&ts.mma_done, 0);
@@ -387,16 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   __shared__ SmemTask st;
   __shared__ TcShared ts;
   uint8_t* sW = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* sX = sW + (size_t)kStages * kWBytes;
-  uint8_t* sWin = sX + (size_t)kMaxBSlots * kXBytes + kXPad;
+  uint8_t* sX = sW + (size_t)p.stages * kWBytes;
+  uint8_t* sWin = sX + (size_t)p.xslots * kXBytes + p.xpad;
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
   const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
 
+  if (tid == 32)  // whether the previous step still has CTAs running (see below)
+    ts.early = ld_relaxed_u64(&p.ctr->exit_count) < ld_relaxed_u64(&p.ctr->norm_arrive);
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
     tc::prefetch_tensormap(&p.tm_ba);
     ts.abort = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
       tc::mbar_init(&ts.empty[s], 1);
     }
@@ -409,18 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
 
-  // The weights are the one input no step writes, so their stream starts
-  // before the previous step is known to be done: with programmatic
+  // The weights are the one input no step writes. With programmatic
   // dependent launch this CTA runs as soon as the previous step's CTA on its
-  // SM has exited, and the first weight tiles (into the ring) and an L2
-  // prefetch of the following units overlap the previous step's tail.
-  const int issued = min(nunits, kStages);
-  if (tid == 32 && nunits > 0) {
-    const uint64_t pol0 = tc::policy_evict_first();
-    UnitIter it(p, ub);
-    for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, pol0);
-    for (int n = issued; n < min(nunits, issued + kPrefetchUnits); ++n, it.next()) prefetch_weight_tile(p, it);
-  }
+  // SM has ended; if other CTAs of the previous step still run (they count
+  // themselves out as they end), the weight stream starts now and overlaps
+  // their tail. Otherwise x and the residual go out first (a few KB that
+  // would queue behind 40 MB of weights in HBM) and the weights right after.
+  const int issued = min(nunits, p.stages);
+  if (ts.early && tid == 32) start_weight_stream(p, ts, sW, ub, nunits, issued);
   griddep_wait();  // from here on the previous step's writes are visible
   griddep_launch_dependents();
   if (tid == 0) {
@@ -431,17 +449,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
   if (!sm.flag) {  // sticky error: every later launch returns at once
-    if (tid == 32)  // once the weight tiles in flight have landed
+    if (tid == 32 && ts.early)  // once the weight tiles in flight have landed
       for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
+    count_exit(p);
     return;
   }
   tl_stamp(p, TL_START);
-  if (tid == 32) tl_stamp_here(p, TL_ISSUED);
+  if (warp == 1) tc::tmem_alloc(&ts.tmem_base, kTmemCols);  // read after the barriers below
 
-  // x and the residual, then the norm partials go out. The sums of squares
-  // use the A operand's pad as scratch.
-  float* sq = reinterpret_cast<float*>(sX + (size_t)kMaxBSlots * kXBytes);
-  stage_residual_slices<HAS_RES>(p, sX, sWin, sq);
+  // x and the residual (and the weights, unless already streaming), then the
+  // norm partials go out. The sums of squares use the A operand's pad as
+  // scratch.
+  float* sq = reinterpret_cast<float*>(sX + (size_t)p.xslots * kXBytes);
+  stage_residual_slices<HAS_RES>(p, sX, sWin, sq, [&] {
+    if (!ts.early && tid == 32) start_weight_stream(p, ts, sW, ub, nunits, issued);
+  });
   tl_stamp(p, TL_R_STAGED);
   publish_norm_partials(p, sq);
   const int L = sm.L;
@@ -450,9 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   if (!phase_wait_rstd(p, sm, L)) {
     if (tid == 32)  // let the weight tiles in flight land before the CTA exits
       for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
+    if (warp == 1) {
+      tc::tc_fence_after();
+      tc::tmem_dealloc(ts.tmem_base, kTmemCols);
+    }
+    count_exit(p);
     return;
   }
-  if (warp == 1) tc::tmem_alloc(&ts.tmem_base, kTmemCols);
   finish_normed_slices(p, sm, sX, sWin);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -474,10 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const bool aborted = ts.abort != 0;
   if (aborted && tid == 0) {
     // the last tile issued into each stage must land before the CTA exits
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       int last = -1;
-      for (int n = s; n < issued_total; n += kStages) last = n;
-      if (last >= 0) cleanup_wait(&ts.full[s], (last / kStages) & 1);
+      for (int n = s; n < issued_total; n += p.stages) last = n;
+      if (last >= 0) cleanup_wait(&ts.full[s], (last / p.stages) & 1);
     }
   }
   if (warp == 1) {
@@ -485,9 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     tc::tmem_dealloc(tmem, kTmemCols);
   }
   tl_stamp(p, TL_PROJ_END);
-  if (aborted) return;
-  phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
-  tl_stamp(p, TL_END);
+  if (!aborted) {
+    phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
+    tl_stamp(p, TL_END);
+  }
+  count_exit(p);
 }
 
 const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk) {
@@ -499,6 +527,18 @@ const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk) {
   return nullptr;
 }
 
-size_t tensor_core_smem_bytes() { return kDynSmem; }
+// Dynamic shared memory of a launch: the weight ring, the normed-input
+// window with the pad an M = 64 MMA reads past its last slice (also the norm
+// sums' scratch), the window's input-norm weights, and 1 KB of alignment.
+uint32_t tensor_core_xpad(int xslots) {
+  const uint32_t sums = (uint32_t)(kMaxRows * xslots * 8 * sizeof(float));
+  return sums > kXPadMin ? (sums + 127) / 128 * 128 : kXPadMin;
+}
+size_t tensor_core_smem_bytes(int stages, int xslots) {
+  return (size_t)stages * kWBytes + (size_t)xslots * kXBytes + tensor_core_xpad(xslots) +
+         (size_t)xslots * kWinBytes + 1024;
+}
+size_t tensor_core_static_smem() { return sizeof(SmemPhases) + sizeof(SmemTask) + sizeof(TcShared); }
+int tensor_core_max_stages() { return kMaxStages; }
 
 }  // namespace gdn
