@@ -26,7 +26,7 @@ EXPORTS = (
 )
 
 # Size of the library's fixed device scratch (gdn_decode_step_static).
-GDN_STATIC_SCRATCH_BYTES = 4 << 20
+GDN_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class Config(ctypes.Structure):

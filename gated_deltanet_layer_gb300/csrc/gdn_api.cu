@@ -217,9 +217,10 @@ Layout make_layout(const gdn_decode_config& c, const Plan& pl) {
   size_t off = 0;
   l.ctr = off;        off += align_up(sizeof(WsCounters), 256);
   l.plan = off;       off += align_up(sizeof(PlanDev), 256);
-  l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(float), 256);
+  l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(unsigned long long), 256);
   l.xn = off;         off += align_up((size_t)kMaxRows * c.hidden * 2, 256);
-  l.proj_part = off;  off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(float), 256);
+  l.proj_part = off;
+  off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(unsigned long long), 256);
   l.total = off;
   return l;
 }
@@ -249,6 +250,14 @@ const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
 }
 
 size_t kernel_smem(const Plan& pl) { return pl.smem; }
+
+// Zero what a workspace's launches count on: the counters and error word, and
+// the tagged partials (a zero tag is no launch's; with the counters back at
+// zero, old tags would otherwise match new launches). The plan stays.
+bool clear_launch_state(char* base, const Layout& l, cudaStream_t s) {
+  return cudaMemsetAsync(base + l.ctr, 0, sizeof(WsCounters), s) == cudaSuccess &&
+         cudaMemsetAsync(base + l.norm_part, 0, l.total - l.norm_part, s) == cudaSuccess;
+}
 
 // Launch fields of the plan that the kernels read.
 void set_plan_params(const Plan& pl, StepParams* p) {
@@ -461,9 +470,9 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
   char* base = (char*)h->ws;
   p->ctr = (WsCounters*)(base + h->lay.ctr);
-  p->norm_part = (float*)(base + h->lay.norm_part);
+  p->norm_part = (unsigned long long*)(base + h->lay.norm_part);
   p->xn = (__nv_bfloat16*)(base + h->lay.xn);
-  p->proj_part = (float*)(base + h->lay.proj_part);
+  p->proj_part = (unsigned long long*)(base + h->lay.proj_part);
   p->plan = (const PlanDev*)(base + h->lay.plan);
   // weight tile maps (cached for the last weights seen)
   if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
@@ -528,10 +537,7 @@ gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail) {
 
 gdn_status gdn_decode_reset(gdn_decode_t* h, void* stream) {
   if (!h) return GDN_ERR_ARG;
-  // counters and the error word only; the plan stays
-  return cudaMemsetAsync((char*)h->ws + h->lay.ctr, 0, sizeof(WsCounters), (cudaStream_t)stream) == cudaSuccess
-             ? GDN_OK
-             : GDN_ERR_CUDA;
+  return clear_launch_state((char*)h->ws, h->lay, (cudaStream_t)stream) ? GDN_OK : GDN_ERR_CUDA;
 }
 
 void gdn_decode_destroy(gdn_decode_t* h) { delete h; }
@@ -674,7 +680,7 @@ gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stre
   memcpy(pd.own_mask, d.plan.own_mask, sizeof(unsigned int) * d.plan.G);
   char* base = (char*)d.scratch;
   // pageable source: the copy has staged it when the call returns
-  if (cudaMemsetAsync(base + d.lay.ctr, 0, sizeof(WsCounters), stream) != cudaSuccess ||
+  if (!clear_launch_state(base, d.lay, stream) ||
       cudaMemcpyAsync(base + d.lay.plan, &pd, sizeof(PlanDev), cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return GDN_ERR_CUDA;
   d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
@@ -754,9 +760,9 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   p.gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
   char* base = (char*)d.scratch;
   p.ctr = (WsCounters*)(base + d.lay.ctr);
-  p.norm_part = (float*)(base + d.lay.norm_part);
+  p.norm_part = (unsigned long long*)(base + d.lay.norm_part);
   p.xn = (__nv_bfloat16*)(base + d.lay.xn);
-  p.proj_part = (float*)(base + d.lay.proj_part);
+  p.proj_part = (unsigned long long*)(base + d.lay.proj_part);
   p.plan = (const PlanDev*)(base + d.lay.plan);
   if (d.map_qkvz_ptr != w->qkvz || d.map_ba_ptr != w->ba) {
     if (!encode_weight_map(&d.map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
@@ -794,7 +800,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   *detail = word;
   if (word == 0) return GDN_OK;
   // read and cleared: the next call starts from zero counters
-  if (cudaMemsetAsync(base + d.lay.ctr, 0, sizeof(WsCounters), s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (!clear_launch_state(base, d.lay, s)) return GDN_ERR_CUDA;
   const uint32_t code = word >> 24;
   if (code == GDN_ERR_DEADLINE) return GDN_ERR_DEADLINE;
   if (code == GDN_ERR_INDEX) return GDN_ERR_INDEX;

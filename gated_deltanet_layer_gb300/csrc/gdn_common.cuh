@@ -33,24 +33,25 @@ constexpr int kDebugTimeline = 0x2;
 constexpr int kTlSlots = 48;  // timeline stamps per CTA: 16 phase points, then 16 + 16 per-unit stamps
 
 // Workspace header: counters on separate 128-byte lines. Every counter only
-// grows; launch L waits for (L+1) * arrivals, so nothing is reset between
-// launches.
+// grows; nothing is reset between launches. The launch number L of a step is
+// norm_arrive / num_ctas at its start. The norm and projection partials are
+// tagged words (tag = L + 1 beside the value, see tagged()), so a reader
+// polls the data itself and no counter or fence guards them.
 struct WsCounters {
   unsigned long long norm_arrive;   // +1 per CTA once its norm partials are out
   unsigned long long pad0[15];
-  unsigned long long xn_arrive;     // +1 per CTA once its normed columns are out
+  unsigned long long xn_arrive;     // +1 per CTA once its normed columns are out (CUDA-core engine)
   unsigned long long pad1[15];
   unsigned int error;               // sticky error word
   unsigned int pad2[63];
   unsigned long long exit_count;    // +1 per CTA as it ends a step (a hint only)
   unsigned long long pad3[15];
-  unsigned long long tile_arrive[kMaxTiles];  // +1 per partial delivered to a tile
   // +1 per recurrence task of (row, key head) once it has read the old q/k
   // conv state; every launch adds the group size G or nothing, so the task
   // that makes the count a multiple of G is the group's last reader
   unsigned int conv_group[kMaxRows][kMaxKHeads];
   // Debug timeline (kDebugTimeline): %globaltimer stamps per CTA at phase
-  // boundaries, and per tile when its last partial arrived.
+  // boundaries (tl_tile is no longer written and reads as zeros).
   unsigned long long tl_cta[kMaxCtas][kTlSlots];
   unsigned long long tl_tile[kMaxTiles][2];
 };
@@ -96,9 +97,9 @@ struct StepParams {
   const __nv_bfloat16* gnorm_w;
   // workspace
   WsCounters* ctr;
-  float* norm_part;        // [kMaxRows][num_ctas]
-  __nv_bfloat16* xn;       // [kMaxRows][H]
-  float* proj_part;        // [num_tiles][max_contrib][kMaxRows][kTileM]
+  unsigned long long* norm_part;  // [kMaxRows][num_ctas] tagged words
+  __nv_bfloat16* xn;              // [kMaxRows][H] (CUDA-core engine)
+  unsigned long long* proj_part;  // [num_tiles][max_contrib][kMaxRows][kTileM] tagged words
   // TMA descriptors of the bf16 weights (box 64 columns x 256 rows, 128-byte
   // swizzle); used by the tensor-core engine and for L2 prefetches.
   CUtensorMap tm_qkvz;
@@ -175,6 +176,10 @@ __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long
   asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
   return old;
 }
+// Relaxed add without a result (a count nobody orders data by).
+__device__ __forceinline__ void red_add_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 // Release add without a result: the issuing thread does not wait for it.
 __device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -191,6 +196,29 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long
   return old;
 }
 
+// Tagged words. A partial handed between CTAs is one 64-bit word: the launch
+// tag L + 1 in the high half, the f32 value in the low half, written and read
+// with relaxed gpu-scope 64-bit accesses (each single-copy atomic). A reader
+// that sees its launch's tag sees that launch's value: no counter, no fence
+// (vLLM #60833, Details, "Shared helpers": a tagged mailbox with bounded
+// waits). The workspace starts zeroed (tag 0); reset zeroes it again.
+__device__ __forceinline__ unsigned long long tagged(int L, float v) {
+  return ((unsigned long long)(unsigned)(L + 1) << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ bool tag_is(unsigned long long w, int L) { return (unsigned)(w >> 32) == (unsigned)(L + 1); }
+__device__ __forceinline__ float tagged_value(unsigned long long w) { return __uint_as_float((unsigned)w); }
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long w) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ void st_tagged2(unsigned long long* p, unsigned long long a, unsigned long long b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
 // Programmatic dependent launch. wait: block until the launches this one
 // depends on in the stream have completed and their writes are visible (a
 // no-op when the launch was not made with programmatic serialisation).
@@ -204,8 +232,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // A CTA ends its step: count it out (relaxed; read by the next step's CTAs
 // only to decide when to start their weight stream).
 __device__ __forceinline__ void count_exit(const StepParams& p) {
-  if (threadIdx.x == 0)
-    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(&p.ctr->exit_count) : "memory");
+  if (threadIdx.x == 0) red_add_relaxed_u64(&p.ctr->exit_count, 1ull);
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -257,28 +284,38 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
-// Spin (one thread) until every counter ctrs[i] >= targets[i] (i < n <= 8),
-// polling them together (relaxed loads in flight at once, then one acquire
-// fence). Same deadline and error behaviour as wait_counter.
-static __device__ __noinline__ bool wait_counters(const StepParams& p, const unsigned long long* const* ctrs,
-                                                  const unsigned long long* targets, int n, uint32_t wait_id) {
+// Bounded poll of tagged words this thread has loaded (w[j] from
+// base + j * stride, j < n): reloads the ones whose tag is not yet this
+// launch's until all are. Gives up at the deadline (recording it) or once
+// another CTA recorded a deadline error; returns false then.
+template <int N>
+__device__ __forceinline__ bool poll_tagged(const StepParams& p, unsigned long long (&w)[N],
+                                            const unsigned long long* base, size_t stride, int n, int L,
+                                            uint32_t wait_id) {
+  static_assert(N <= 32, "one stale bit per word");
+  uint32_t stale = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    if (j < n && !tag_is(w[j], L)) stale |= 1u << j;
+  if (!stale) return true;
   const unsigned long long t0 = globaltimer_ns();
-  const unsigned long long cap = p.deadline_ns / 32 + 4096;
+  const unsigned long long cap = p.deadline_ns / 64 + 4096;
   for (unsigned long long it = 0;; ++it) {
-    unsigned long long v[8];
-    for (int i = 0; i < n; ++i) v[i] = ld_relaxed_u64(ctrs[i]);
-    bool all = true;
-    for (int i = 0; i < n; ++i) all = all && (v[i] >= targets[i]);
-    if (all) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      return true;
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if ((stale >> j) & 1u) w[j] = ld_tagged(base + (size_t)j * stride);
+    stale = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (j < n && !tag_is(w[j], L)) stale |= 1u << j;
+    if (!stale) return true;
+    if ((it & 15) == 15) {
+      if ((ld_relaxed_u32(&p.ctr->error) >> 24) == kStatusDeadline) return false;
+      if (globaltimer_ns() - t0 > p.deadline_ns || it > cap) {
+        record_error(p.ctr, kStatusDeadline, wait_id, blockIdx.x);
+        return false;
+      }
     }
-    if ((ld_relaxed_u32(&p.ctr->error) >> 24) == kStatusDeadline) return false;
-    if (globaltimer_ns() - t0 > p.deadline_ns || it > cap) {
-      record_error(p.ctr, kStatusDeadline, wait_id, blockIdx.x);
-      return false;
-    }
-    __nanosleep(32);
   }
 }
 

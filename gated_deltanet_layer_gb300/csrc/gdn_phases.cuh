@@ -15,7 +15,7 @@ struct SmemPhases {
   alignas(16) float rstd[kMaxRows];
   alignas(16) float red[kWarps];
   int L;                 // launch number on this workspace
-  int flag;              // CTA-wide decision broadcast by thread 0
+  int flag;              // CTA-wide decision (set by thread 0, cleared by any thread that gives up)
 };
 
 // xn = bf16(r * rstd * (1 + w_in)) of 8 consecutive columns (r, w_in as bf16x2 words).
@@ -42,14 +42,14 @@ __device__ __forceinline__ uint4 residual8(uint4 xv, uint4 qv) {
 }
 
 // ---------------------------------------------------------------------------
-// Phase 1: r = x + residual (bf16), residual_out, and each row's sum of r^2
-// over this CTA's hidden columns. The sums are handed to every CTA through
-// global memory and a release counter (vLLM #60833, Details, "x without an
-// LDS tile": the norm CTAs publish their columns' sums of squares and each
-// consumer builds the x it reads). Returns the launch number.
+// Phase 1 (CUDA-core engine): r = x + residual (bf16), residual_out, and each
+// row's sum of r^2 over this CTA's hidden columns, handed to every CTA as
+// tagged words (vLLM #60833, Details, "x without an LDS tile": the norm CTAs
+// publish their columns' sums of squares and each consumer builds the x it
+// reads).
 // ---------------------------------------------------------------------------
 template <bool HAS_RES>
-__device__ __forceinline__ void phase_norm_partials(const StepParams& p, SmemPhases& sm) {
+__device__ __forceinline__ void phase_norm_partials(const StepParams& p, SmemPhases& sm, int L) {
   const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int c0 = cta * p.norm_chunk;
@@ -74,58 +74,47 @@ __device__ __forceinline__ void phase_norm_partials(const StepParams& p, SmemPha
     sm.part8[w * (kMaxNormChunk / 8) + v] = s;
   }
   __syncthreads();
+  const bool publish = !((p.debug_flags & kDebugSkipNormPublish) && cta == 0);  // test hook: never publish
   for (int w = warp; w < W; w += kWarps) {
     float s = 0.f;
     for (int v = lane; v < nvec; v += 32) s += sm.part8[w * (kMaxNormChunk / 8) + v];
     s = warp_sum(s);
-    if (lane == 0) p.norm_part[w * p.num_ctas + cta] = s;
+    if (lane == 0 && publish) st_tagged(p.norm_part + w * p.num_ctas + cta, tagged(L, s));
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long old;
-    if ((p.debug_flags & kDebugSkipNormPublish) && cta == 0)
-      old = ld_acquire_u64(&p.ctr->norm_arrive);  // test hook: never publish
-    else
-      old = atom_add_release_u64(&p.ctr->norm_arrive, 1ull);
-    sm.L = (int)(old / (unsigned long long)p.num_ctas);
-  }
+  if (tid == 0 && publish) red_add_relaxed_u64(&p.ctr->norm_arrive, 1ull);  // counts launches only
   tl_stamp(p, TL_NORM_OUT);
   __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
-// Phase 1b: wait for every CTA's sums, form rstd per row (Gemma RMSNorm:
-// rstd = 1/sqrt(mean(r^2) + eps), xn = r * rstd * (1 + w)) and write this
-// CTA's columns of the normed input xn (bf16) to the workspace image.
+// Phase 1b: every CTA's sums (polled as tagged words of this launch), rstd
+// per row (Gemma RMSNorm: rstd = 1/sqrt(mean(r^2) + eps)). The sums are added
+// in CTA order, so every CTA forms the same rstd bit for bit.
 // ---------------------------------------------------------------------------
 static __device__ __forceinline__ bool phase_wait_rstd(const StepParams& p, SmemPhases& sm, int L) {
   const int W = p.rows, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  if (tid == 0)
-    sm.flag = wait_counter(p, &p.ctr->norm_arrive,
-                           (unsigned long long)(L + 1) * p.num_ctas, kWaitNorm);
-  tl_stamp(p, TL_NORM_IN);
+  if (tid == 0) sm.flag = 1;
   __syncthreads();
-  if (!sm.flag) return false;
   for (int w = warp; w < W; w += kWarps) {
-    // all of this lane's partials in flight at once, added in CTA order
+    // lane l holds CTAs l, l + 32, ...: all in flight at once
     constexpr int M = (kMaxCtas + 31) / 32;
-    float v[M];
+    const unsigned long long* src = p.norm_part + w * p.num_ctas + lane;
+    const int n = lane < p.num_ctas ? (p.num_ctas - lane + 31) / 32 : 0;
+    unsigned long long v[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const int c = lane + 32 * m;
-      v[m] = c < p.num_ctas ? ld_cg_f(p.norm_part + w * p.num_ctas + c) : 0.f;
-    }
+    for (int m = 0; m < M; ++m) v[m] = m < n ? ld_tagged(src + 32 * m) : 0ull;
+    if (!poll_tagged<M>(p, v, src, 32, n, L, kWaitNorm)) sm.flag = 0;
     float s = 0.f;
 #pragma unroll
     for (int m = 0; m < M; ++m)
-      if (lane + 32 * m < p.num_ctas) s += v[m];
+      if (m < n) s += tagged_value(v[m]);
     s = warp_sum(s);
     if (lane == 0) sm.rstd[w] = 1.0f / sqrtf(s / (float)p.H + p.norm_eps);
   }
+  tl_stamp(p, TL_NORM_IN);
   __syncthreads();
-  return true;
+  return sm.flag != 0;
 }
 
 static __device__ __forceinline__ bool phase_normed_input(const StepParams& p, SmemPhases& sm, int L) {
@@ -161,18 +150,6 @@ __device__ __forceinline__ void group_sync() {
     __syncwarp();
   else
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-}
-
-// Publish a finished partial of tile t: called by all NT threads of a group
-// after they wrote it; group thread 0 counts it with a release add.
-template <int NT>
-static __device__ __forceinline__ void publish_tile_partial(const StepParams& p, int t, int gtid) {
-  __threadfence();
-  group_sync<NT>();
-  if (gtid == 0) {
-    atom_add_release_u64(&p.ctr->tile_arrive[t], 1ull);
-    if (p.debug_flags & kDebugTimeline) p.ctr->tl_tile[t][0] = globaltimer_ns();
-  }
 }
 
 // Shared memory of one recurrence task.
@@ -212,8 +189,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
   constexpr int LPR = DK / 4;              // lanes per state row, 4 elements each
   constexpr int RPW = 32 / LPR;            // rows per warp per step
   constexpr int NR = DK / (kWarps * RPW);  // rows per lane (dv == dk)
-  constexpr int NOUT = 4 * DK + 2;         // q, k, v, z, then b, a
-  static_assert(NR >= 1 && NOUT <= 2 * kThreads, "task layout");
+  static_assert(NR >= 1 && 4 * DK <= kThreads, "task layout");
   const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int sub = lane % LPR, rw = lane / LPR;
@@ -259,58 +235,57 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     auto tile_of = [&](int n) -> int {
       return n < p.Nqkvz ? (n >> kTileShift) : p.tiles_qkvz + ((n - p.Nqkvz) >> kTileShift);
     };
-    if (tid == 0) {
-      const int tiles[6] = {tile_of(proj_row(0)), tile_of(proj_row(DK)), tile_of(proj_row(2 * DK)),
-                            tile_of(proj_row(3 * DK)), tile_of(proj_row(4 * DK)), tile_of(proj_row(4 * DK + 1))};
-      const unsigned long long* ctrs[6];
-      unsigned long long tgt[6];
-      for (int i = 0; i < 6; ++i) {
-        ctrs[i] = &p.ctr->tile_arrive[tiles[i]];
-        tgt[i] = (unsigned long long)(L + 1) * p.plan->tile_num_ctas[tiles[i]];
-      }
-      sm.flag = wait_counters(p, ctrs, tgt, 6, kWaitTile);
-      if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
-    }
+    if (tid == 0) sm.flag = 1;
     __syncthreads();
-    if (!sm.flag) return false;
 
-    // Projection outputs: partials in slot order; conv for q/k/v channels.
-    // A thread with two outputs (there are 4*dk + 2 of them) issues the loads
-    // of both before using any, so it costs one round trip like the others.
+    // Projection outputs, each the sum of its tile's partials in slot order,
+    // polled as tagged words of this launch. Thread i < 4*dk takes output i
+    // (q, k, v, z); b and a take one slot per lane of the last two warps.
     constexpr size_t kSlot = (size_t)kMaxRows * kTileM;
-    constexpr int kMaxSlots = 24;  // partials per tile handled in one batch
-    struct OutLoads {
-      float pv[kMaxSlots];
+    constexpr int kMaxSlots = 24;  // partials per tile (the plan's bound)
+    auto part_src = [&](int n, int& nc) {
+      const int t = tile_of(n);
+      const int r = (n < p.Nqkvz ? n : n - p.Nqkvz) & (kTileM - 1);
+      nc = p.plan->tile_num_ctas[t];
+      return p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
+    };
+    const bool ba_warp = warp >= kWarps - 2;
+    int ba_nc = 0;
+    const unsigned long long* ba_src = nullptr;
+    unsigned long long ba_w[1] = {0ull};
+    if (ba_warp) {  // issued first: these lanes also have an output of their own
+      ba_src = part_src(proj_row(4 * DK + (warp - (kWarps - 2))), ba_nc) + (size_t)lane * kSlot;
+      if (lane < ba_nc) ba_w[0] = ld_tagged(ba_src);
+    }
+    if (tid < 4 * DK) {
+      const int i = tid;
+      const int n = proj_row(i);
+      int nc;
+      const unsigned long long* src = part_src(n, nc);
       __nv_bfloat16 cb0, cb1, cb2;
       uint2 cwv;
-      int n, nc;
-    };
-    auto issue = [&](int i, OutLoads& L) {
-      L.n = proj_row(i);
-      const int t = tile_of(L.n);
-      const int r = (L.n < p.Nqkvz ? L.n : L.n - p.Nqkvz) & (kTileM - 1);
-      L.nc = p.plan->tile_num_ctas[t];
-      const float* src = p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
       if (i < 3 * DK) {  // old taps and weights of channel n
-        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + L.n) * 3;
-        L.cb0 = cs[0]; L.cb1 = cs[1]; L.cb2 = cs[2];
-        L.cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)L.n * 4);
+        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+        cb0 = cs[0]; cb1 = cs[1]; cb2 = cs[2];
+        cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)n * 4);
       }
+      unsigned long long pw[kMaxSlots];
 #pragma unroll
-      for (int jj = 0; jj < kMaxSlots; ++jj) L.pv[jj] = jj < L.nc ? ld_cg_f(src + (size_t)jj * kSlot) : 0.f;
-    };
-    auto finish = [&](int i, const OutLoads& L) {
+      for (int jj = 0; jj < kMaxSlots; ++jj) pw[jj] = jj < nc ? ld_tagged(src + (size_t)jj * kSlot) : 0ull;
+      if (!poll_tagged<kMaxSlots>(p, pw, src, kSlot, nc, L, kWaitTile)) sm.flag = 0;
+      if (i == 0 && (p.debug_flags & kDebugTimeline) && task == t0)
+        p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
       float acc = 0.f;
 #pragma unroll
       for (int jj = 0; jj < kMaxSlots; ++jj)
-        if (jj < L.nc) acc += L.pv[jj];
+        if (jj < nc) acc += tagged_value(pw[jj]);
       const float pv = round_bf16(acc);
       if (i < 3 * DK) {
-        const float c0 = bf16_to_f(L.cb0), c1 = bf16_to_f(L.cb1), c2 = bf16_to_f(L.cb2);
-        float y = bf16_lo(L.cwv.x) * c0;
-        y = fmaf(bf16_hi(L.cwv.x), c1, y);
-        y = fmaf(bf16_lo(L.cwv.y), c2, y);
-        y = fmaf(bf16_hi(L.cwv.y), pv, y);
+        const float c0 = bf16_to_f(cb0), c1 = bf16_to_f(cb1), c2 = bf16_to_f(cb2);
+        float y = bf16_lo(cwv.x) * c0;
+        y = fmaf(bf16_hi(cwv.x), c1, y);
+        y = fmaf(bf16_lo(cwv.y), c2, y);
+        y = fmaf(bf16_hi(cwv.y), pv, y);
         y = silu_f(y);
         if (i < DK) {
           st.q[i] = y;
@@ -318,7 +293,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
           st.k[i - DK] = y;
         } else {
           st.v[i - 2 * DK] = y;
-          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + L.n) * 3;  // this head's own channel
+          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;  // this head's own channel
           cs[0] = __float2bfloat16_rn(c1);
           cs[1] = __float2bfloat16_rn(c2);
           cs[2] = __float2bfloat16_rn(pv);
@@ -328,21 +303,23 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
           st.cnew[i][1] = c2;
           st.cnew[i][2] = pv;
         }
-      } else if (i < 4 * DK) {
-        st.z[i - 3 * DK] = pv;
       } else {
-        st.ba[i - 4 * DK] = pv;
+        st.z[i - 3 * DK] = pv;
       }
-    };
-    if (tid < NOUT) {
-      OutLoads L0, L1;
-      const bool two = tid + kThreads < NOUT;
-      issue(tid, L0);
-      if (two) issue(tid + kThreads, L1);
-      finish(tid, L0);
-      if (two) finish(tid + kThreads, L1);
+    }
+    if (ba_warp) {
+      if (!poll_tagged<1>(p, ba_w, ba_src, 0, lane < ba_nc ? 1 : 0, L, kWaitTile)) sm.flag = 0;
+      const float v = tagged_value(ba_w[0]);
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kMaxSlots; ++jj) {  // slot order, as for the other outputs
+        const float x = __shfl_sync(0xffffffffu, v, jj);
+        if (jj < ba_nc) acc += x;
+      }
+      if (lane == 0) st.ba[warp - (kWarps - 2)] = round_bf16(acc);
     }
     __syncthreads();
+    if (!sm.flag) return false;
     unsigned int group_old = 0;
     if (tid == 0) {
       // every thread's reads of the old q/k taps are done (their values are

@@ -6,9 +6,11 @@
 // work units (a stream-K split of (256-row tile, 64-column step) units, so
 // every CTA streams the same number of weight bytes), publishing a partial
 // per tile it touched, and its share of the (row, value head) recurrence
-// tasks, which reduce the partials they need. Cross-CTA hand-offs go through release/acquire counters with bounded
-// waits (vLLM #60833, Claims and Limitations: every wait is bounded and a
-// failed wait leaves a sticky failed word).
+// tasks, which reduce the partials they need. The norm sums and the
+// projection partials are handed over as tagged words, the normed input
+// image through a release/acquire counter; every wait is bounded and a
+// failed wait leaves a sticky failed word (vLLM #60833, Details,
+// "Limitations / follow-ups").
 #include "gdn_kernels.h"
 #include "gdn_phases.cuh"
 
@@ -73,15 +75,14 @@ static __device__ __forceinline__ bool phase_proj_cuda_core(const StepParams& p,
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) acc[w] += __shfl_xor_sync(0xffffffffu, acc[w], 1);
     const int j = p.plan->seg_slot[cta][seg];
-    float* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
+    unsigned long long* dst = p.proj_part + ((size_t)t * p.max_contrib + j) * kMaxRows * kTileM;
     if (sub == 0) {
 #pragma unroll
       for (int w = 0; w < kMaxRows; ++w)
-        if (w < W) dst[w * kTileM + row] = acc[w];
+        if (w < W) st_tagged(dst + w * kTileM + row, tagged(L, acc[w]));
     }
 #pragma unroll
     for (int w = 0; w < kMaxRows; ++w) acc[w] = 0.f;
-    publish_tile_partial<kThreads>(p, t, tid);
   };
 
   constexpr int D = 2;  // units of weights in flight per thread
@@ -153,12 +154,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   CcDynSmem& ds = *reinterpret_cast<CcDynSmem*>(cc_dyn);
   griddep_wait();  // the previous step's writes first
   griddep_launch_dependents();
-  if (threadIdx.x == 0) sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
+  if (threadIdx.x == 0) {
+    sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);
+    // launch number: every CTA of the previous launches has counted itself
+    sm.L = (int)(ld_relaxed_u64(&p.ctr->norm_arrive) / (unsigned long long)p.num_ctas);
+  }
   __syncthreads();
   if (!sm.flag) return;  // sticky error: every later launch returns at once
   tl_stamp(p, TL_START);
-  phase_norm_partials<HAS_RES>(p, sm);
   const int L = sm.L;
+  phase_norm_partials<HAS_RES>(p, sm, L);
   if (!phase_normed_input(p, sm, L)) return;
   if (!phase_proj_cuda_core(p, sm, ds.xs, L)) return;
   phase_recurrence<DK, STATE_BF16>(p, sm, st, L);

@@ -254,28 +254,23 @@ static __device__ __forceinline__ void write_residual_out(const StepParams& p, c
 }
 
 // Each row's sum of r^2 over the owned k-steps (slot-major, a fixed order),
-// published to every CTA through the norm counter. Only the threads that
-// store a partial fence; thread 0 publishes with a release add it does not
-// wait for (the launch number was read at kernel entry).
-static __device__ __forceinline__ void publish_norm_partials(const StepParams& p, const float* sq) {
+// published to every CTA as a tagged word: no fence, no release (the launch
+// number L was read at kernel entry). The norm counter only counts launches.
+static __device__ __forceinline__ void publish_norm_partials(const StepParams& p, const float* sq, int L) {
   const int cta = blockIdx.x, W = p.rows, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nb = p.plan->nb_slots[cta];
   const unsigned own = p.plan->own_mask[cta];
+  const bool publish = !((p.debug_flags & kDebugSkipNormPublish) && cta == 0);  // test hook: never publish
   __syncthreads();
   for (int w = warp; w < W; w += kWarps) {
     float s = 0.f;
     for (int e = lane; e < nb * 8; e += 32)
       if ((own >> (e >> 3)) & 1u) s += sq[w * (p.xslots * 8) + e];
     s = warp_sum(s);
-    if (lane == 31) {  // not lane 0: thread 32 has bulk copies in flight that a fence would wait for
-      p.norm_part[w * p.num_ctas + cta] = s;
-      __threadfence();
-    }
+    if (lane == 0 && publish) st_tagged(p.norm_part + w * p.num_ctas + cta, tagged(L, s));
   }
-  __syncthreads();
-  if (tid == 0 && !((p.debug_flags & kDebugSkipNormPublish) && cta == 0))  // test hook: never publish
-    red_add_release_u64(&p.ctr->norm_arrive, 1ull);
+  if (tid == 0 && publish) red_add_relaxed_u64(&p.ctr->norm_arrive, 1ull);
   tl_stamp(p, TL_NORM_OUT);
 }
 
@@ -364,7 +359,7 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
 // partial of the tile is written and published.
 constexpr int kDrainThreads = 64;
 static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared& ts, int ub, int nunits,
-                                                  uint32_t tmem, int gtid) {
+                                                  uint32_t tmem, int gtid, int L) {
   const int W = p.rows, lane = gtid & 31, half = gtid >> 5;
   UnitIter it(p, ub);
   int seg = 0;
@@ -381,22 +376,22 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
     if (lane == 0) ok = pipe_wait(p, ts, &ts.acc_full[b], (seg >> 1) & 1);
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     tc::tc_fence_after();
-    float* dst = p.proj_part + ((size_t)t * p.max_contrib + p.plan->seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
-                 (size_t)lane * kTileM;
+    unsigned long long* dst = p.proj_part +
+                              ((size_t)t * p.max_contrib + p.plan->seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
+                              (size_t)lane * kTileM;
 #pragma unroll 1
     for (int c = half * (kTileM / 64); c < (half + 1) * (kTileM / 64); ++c) {
       float v[32];
       tc::tmem_ld32(tmem + (uint32_t)b * kTileM + c * 32, v);
-      if (lane < W) {
+      if (lane < W) {  // the partial as tagged words: readers poll them directly
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4*>(dst + c * 32)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 16; ++q)
+          st_tagged2(dst + c * 32 + 2 * q, tagged(L, v[2 * q]), tagged(L, v[2 * q + 1]));
       }
     }
     tc::tc_fence_before();
     group_sync<kDrainThreads>();
     if (gtid == 0) tc::mbar_arrive(&ts.acc_empty[b]);
-    publish_tile_partial<kDrainThreads>(p, t, gtid);
   }
 }
 
@@ -465,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     if (!ts.early && tid == 32) start_weight_stream(p, ts, sW, ub, nunits, issued);
   });
   tl_stamp(p, TL_R_STAGED);
-  publish_norm_partials(p, sq);
   const int L = sm.L;
+  publish_norm_partials(p, sq, L);
   if (tid == 64) prefetch_states<DK, STATE_BF16>(p);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
@@ -493,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     else if (tid == 32)
       mma_loop(p, ts, sW, sX, ub, nunits, tmem);
     else if (warp == 4 || warp == 8)
-      drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31));
+      drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31), L);
   }
   tc::tc_fence_before();
   __syncthreads();

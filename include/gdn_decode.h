@@ -153,7 +153,8 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
  * 3 projection tile), 15..0 the CTA (deadline) or row (index error). */
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail);
 
-/* Clear the error word and all counters of the workspace on `stream`. */
+/* Clear the error word, all counters and the partial buffers of the
+ * workspace on `stream` (the plan stays). */
 gdn_status gdn_decode_reset(gdn_decode_t* h, void* stream);
 
 /* Free the host handle. The workspace stays the caller's. */
@@ -168,21 +169,23 @@ gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows,
 
 /* Diagnostics: synchronise `stream` and copy the phase timeline the last
  * step recorded (handle created with GDN_DEBUG_TIMELINE). cta_stamps receives
- * num_ctas x 48 uint64 nanosecond stamps: 0 start, 1 norm partials out,
- * 2 norm wait done, 3 normed input out, 4 projection start, 5 projection end,
- * 6 first recurrence task's inputs ready, 7 end, 8 epilogues run (a count),
- * 9 first MMA, 10 last MMA done, 11 first weight tiles issued, 12 residual
- * staged, 13 epilogues done; 16+n the n-th weight tile ready for the MMA and
- * 32+n the n-th weight tile issued (n < 16, tensor-core engine);
- * tile_stamps receives num_tiles x 2 (epilogue start, end). Capacities are in
- * elements; *num_ctas and *num_tiles receive the sizes. */
+ * num_ctas x 48 uint64 nanosecond stamps: 0 start (after the previous step),
+ * 1 norm partials out, 2 norm sums in (rstd known), 3 normed input out
+ * (CUDA-core engine), 4 projection start, 5 projection end, 6 the first
+ * recurrence task's projection partials in, 7 end, 8 that task's inputs
+ * done, 9 first MMA, 10 last MMA done, 11 first weight tiles issued,
+ * 12 x and residual staged, 13 that task's state written; 32+n the n-th
+ * weight tile issued (n < 16, tensor-core engine); other slots unused.
+ * tile_stamps receives num_tiles x 2 zeros (kept for the layout of this
+ * call). Capacities are in elements; *num_ctas and *num_tiles receive the
+ * sizes. */
 gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
                                      int32_t cta_cap, uint64_t* tile_stamps, int32_t tile_cap,
                                      int32_t* num_ctas, int32_t* num_tiles);
 
 /* Host-only diagnostics of the stream-K split of the projection work units
  * (no device call) for a grid of num_ctas CTAs. A unit is one 64-column step
- * (k-step) of one 128-row projection tile (tiles: in_proj_qkvz rows first,
+ * (k-step) of one 256-row projection tile (tiles: in_proj_qkvz rows first,
  * then in_proj_ba rows); units are ordered by group g = (k-block g / T,
  * tile g % T) of `kblock` k-steps. Fills *engine (the engine the config runs
  * with), unit_begin[num_ctas+1] (CTA c takes units [unit_begin[c],
@@ -196,8 +199,8 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
                            uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
                            int32_t* kblock);
 
-/* Largest scratch gdn_decode_step_static can use, in bytes (4 MiB). */
-#define GDN_STATIC_SCRATCH_BYTES (4u << 20)
+/* Largest scratch gdn_decode_step_static can use, in bytes (8 MiB). */
+#define GDN_STATIC_SCRATCH_BYTES (8u << 20)
 
 /* One decode step, computed exactly as gdn_decode_step computes it, for
  * callers that cannot allocate device memory: a C or C++ host program with no
