@@ -44,8 +44,6 @@ struct WsCounters {
   unsigned long long pad1[15];
   unsigned int error;               // sticky error word
   unsigned int pad2[63];
-  unsigned long long exit_count;    // +1 per CTA as it ends a step (a hint only)
-  unsigned long long pad3[15];
   // +1 per recurrence task of (row, key head) once it has read the old q/k
   // conv state; every launch adds the group size G or nothing, so the task
   // that makes the count a multiple of G is the group's last reader
@@ -227,12 +225,6 @@ __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// A CTA ends its step: count it out (relaxed; read by the next step's CTAs
-// only to decide when to start their weight stream).
-__device__ __forceinline__ void count_exit(const StepParams& p) {
-  if (threadIdx.x == 0) red_add_relaxed_u64(&p.ctr->exit_count, 1ull);
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {

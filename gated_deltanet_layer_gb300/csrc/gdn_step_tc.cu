@@ -39,6 +39,7 @@ namespace gdn {
 
 namespace {
 constexpr int kMaxStages = 6;                           // weight tiles in flight per CTA (the plan picks)
+constexpr int kFirstTiles = 2;                          // of them issued before the norm hand-off
 constexpr uint32_t kWBytes = kTileM * kKStep * 2;       // 32 KB weight tile (B operand)
 constexpr uint32_t kXBytes = kMaxRows * kKStep * 2;     // 2 KB normed-input slice (A rows 0..15)
 constexpr uint32_t kXPadMin = (64 - kMaxRows) * 128;    // 6 KB an M = 64 MMA reads past the last slice
@@ -58,7 +59,6 @@ struct TcShared {
   uint64_t mma_done;        // every MMA issued by the CTA done
   uint32_t tmem_base;
   int abort;
-  int early;   // the weight stream started before the previous step was done
 };
 
 // Walks a CTA's units in plan order without divisions: unit u is k-step
@@ -132,15 +132,15 @@ __device__ __forceinline__ void issue_weight_tile(const StepParams& p, TcShared&
   if (n < 16) tl_stamp_here(p, TL_UNIT_ISSUED + n);
 }
 
-// The CTA's weight stream: the first `issued` units into the ring (one
-// thread).
+// Units [from, to) of the CTA's weight stream into the ring's first stages
+// (one thread; to <= the ring depth).
 static __device__ __forceinline__ void start_weight_stream(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                           int ub, int nunits, int issued) {
-  if (nunits <= 0) return;
+                                                           int ub, int from, int to) {
+  if (from >= to) return;
   const uint64_t pol0 = tc::policy_evict_first();
-  UnitIter it(p, ub);
-  for (int n = 0; n < issued; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, n, pol0);
-  tl_stamp_here(p, TL_ISSUED);
+  UnitIter it(p, ub + from);
+  for (int n = from; n < to; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, n, pol0);
+  if (from == 0) tl_stamp_here(p, TL_ISSUED);
 }
 
 // L2 prefetch of the state this CTA's recurrence tasks read, and of the conv
@@ -170,9 +170,9 @@ static __device__ __forceinline__ void prefetch_states(const StepParams& p) {
 // columns bf16 in the 128-byte swizzled K-major layout (row r at r * 128
 // bytes, its 16-byte chunk c at position c ^ (r % 8)); rows past the step's
 // rows are 0. Built in two passes around the norm hand-off:
-//   stage_residual_slices: r = bf16(x + residual) of the window and the norm
-//     weights; for the k-steps this CTA owns it also writes residual_out and
-//     the sums of r^2 of 8 columns into `sq` ([row][slot * 8 + chunk])
+//   stage_residual_slices: r = bf16(x + residual) of the window; for the
+//     k-steps this CTA owns, the sums of r^2 of 8 columns into `sq`
+//     ([row][slot * 8 + chunk]); write_residual_out stores them later
 //   finish_normed_slices: xn = bf16(r * rstd * (1 + w)) in place.
 // One pass over x and the residual serves the residual add, the norm
 // partials and the MMA operand (vLLM #60833, Details, "x without an LDS
@@ -229,11 +229,22 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
       }
     }
   }
-  for (int i = threadIdx.x; i < nb * 8; i += kThreads) {
-    const int j = i >> 3, c = i & 7;
-    reinterpret_cast<uint4*>(sWin + (size_t)j * kWinBytes)[c] =
-        ld_stream_v4(p.w_in + (size_t)((ks0 + j) % p.ksteps) * kKStep + c * 8);
-  }
+}
+
+// The input-norm weights of the window, one 16-byte chunk per thread (at
+// most 24 k-steps x 8 chunks < 512 threads). A weight no step writes: the
+// load goes out before the previous step is done, the value is stored to
+// shared memory once the x and residual loads are out, off the norm path.
+static_assert(kMaxBSlots * 8 <= kThreads, "one norm-weight chunk per thread");
+static __device__ __forceinline__ uint4 load_norm_weights(const StepParams& p) {
+  const int cta = blockIdx.x, i = threadIdx.x;
+  const int nb = p.plan->nb_slots[cta], ks0 = p.plan->ks_first[cta];
+  if (i >= nb * 8) return make_uint4(0, 0, 0, 0);
+  return ld_stream_v4(p.w_in + (size_t)((ks0 + (i >> 3)) % p.ksteps) * kKStep + (i & 7) * 8);
+}
+static __device__ __forceinline__ void store_norm_weights(const StepParams& p, uint8_t* sWin, uint4 v) {
+  const int i = threadIdx.x;
+  if (i < p.plan->nb_slots[blockIdx.x] * 8) reinterpret_cast<uint4*>(sWin + (size_t)(i >> 3) * kWinBytes)[i & 7] = v;
 }
 
 // residual_out of the owned k-steps, from the staged r (after the norm
@@ -407,8 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
   const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
 
-  if (tid == 32)  // whether the previous step still has CTAs running (see below)
-    ts.early = ld_relaxed_u64(&p.ctr->exit_count) < ld_relaxed_u64(&p.ctr->norm_arrive);
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
     tc::prefetch_tensormap(&p.tm_ba);
@@ -426,14 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
 
-  // The weights are the one input no step writes. With programmatic
+  // The weights are the one input no step writes, so their stream starts
+  // before the previous step is known to be done: with programmatic
   // dependent launch this CTA runs as soon as the previous step's CTA on its
-  // SM has ended; if other CTAs of the previous step still run (they count
-  // themselves out as they end), the weight stream starts now and overlaps
-  // their tail. Otherwise x and the residual go out first (a few KB that
-  // would queue behind 40 MB of weights in HBM) and the weights right after.
+  // SM has ended, and its first tiles overlap the previous step's tail. Only
+  // kFirstTiles go out now: the x and residual loads that start the norm
+  // hand-off would otherwise queue behind a whole ring's worth of weights in
+  // HBM. The rest of the ring follows once the norm partials are out.
   const int issued = min(nunits, p.stages);
-  if (ts.early && tid == 32) start_weight_stream(p, ts, sW, ub, nunits, issued);
+  const int first = min(issued, kFirstTiles);
+  if (tid == 32) start_weight_stream(p, ts, sW, ub, 0, first);
+  const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
   griddep_wait();  // from here on the previous step's writes are visible
   griddep_launch_dependents();
   if (tid == 0) {
@@ -444,9 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
   if (!sm.flag) {  // sticky error: every later launch returns at once
-    if (tid == 32 && ts.early)  // once the weight tiles in flight have landed
-      for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
-    count_exit(p);
+    if (tid == 32)  // once the weight tiles in flight have landed
+      for (int n = 0; n < first; ++n) cleanup_wait(&ts.full[n], 0);
     return;
   }
   tl_stamp(p, TL_START);
@@ -456,12 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // norm partials go out. The sums of squares use the A operand's pad as
   // scratch.
   float* sq = reinterpret_cast<float*>(sX + (size_t)p.xslots * kXBytes);
-  stage_residual_slices<HAS_RES>(p, sX, sWin, sq, [&] {
-    if (!ts.early && tid == 32) start_weight_stream(p, ts, sW, ub, nunits, issued);
-  });
+  stage_residual_slices<HAS_RES>(p, sX, sWin, sq, [&] { store_norm_weights(p, sWin, wnorm); });
   tl_stamp(p, TL_R_STAGED);
   const int L = sm.L;
   publish_norm_partials(p, sq, L);
+  if (tid == 32) start_weight_stream(p, ts, sW, ub, first, issued);
   if (tid == 64) prefetch_states<DK, STATE_BF16>(p);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
@@ -471,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
       tc::tc_fence_after();
       tc::tmem_dealloc(ts.tmem_base, kTmemCols);
     }
-    count_exit(p);
     return;
   }
   finish_normed_slices(p, sm, sX, sWin);
@@ -510,7 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
     tl_stamp(p, TL_END);
   }
-  count_exit(p);
 }
 
 const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk) {
