@@ -318,7 +318,8 @@ def native(args):
                    "l2": f"inputs larger than L2: weights rotated over {ncopy} copies "
                          f"({ncopy * wbytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2), fresh slots per launch",
                    "timing": "CUDA graph of K launches, CUDA events on the launching stream",
-                   "grid": n_ctas, "engine": engine},
+                   "grid": n_ctas, "engine": engine,
+                   "launch": "persistent grid, one CTA per SM; programmatic dependent launch between steps"},
         "achieved_GBps": round(bytes_launch / us / 1e3, 1),
         "widths": table,
         "roofline": {"bound": "hbm", "achieved": round(bytes_launch / us / 1e3, 1), "peak": peak,

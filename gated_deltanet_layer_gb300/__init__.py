@@ -31,7 +31,7 @@ def _ptr(t):
 
 
 def make_config(shape, *, engine: str = "auto", deadline_us: int = 0, num_ctas: int = 0,
-                debug_flags: int = 0, max_rows: int | None = None) -> _native.Config:
+                debug_flags: int = 0, max_rows: int | None = None, launch_flags: int = 0) -> _native.Config:
     """C config from a layer description (any object with the LayerShape fields)."""
     q_scale = shape.q_scale if shape.q_scale is not None else float(shape.head_k_dim) ** -0.5
     return _native.Config(
@@ -42,19 +42,19 @@ def make_config(shape, *, engine: str = "auto", deadline_us: int = 0, num_ctas: 
         qkvz_format=GDN_W_MXFP4 if shape.qkvz_format == "mxfp4" else GDN_W_BF16,
         engine=ENGINES[engine], norm_eps=shape.norm_eps, gated_norm_eps=shape.gated_norm_eps,
         l2_eps=shape.l2_eps, q_scale=q_scale, deadline_us=deadline_us, num_ctas=num_ctas,
-        debug_flags=debug_flags)
+        debug_flags=debug_flags, launch_flags=launch_flags)
 
 
 class GdnDecode:
     """A GDN layer front's decode step, bound to one workspace on one device."""
 
     def __init__(self, shape, *, engine: str = "auto", deadline_us: int = 0, num_ctas: int = 0,
-                 debug_flags: int = 0, max_rows: int | None = None, stream=None):
+                 debug_flags: int = 0, max_rows: int | None = None, launch_flags: int = 0, stream=None):
         import torch
         L = _native.lib()
         self.shape = shape
         self.cfg = make_config(shape, engine=engine, deadline_us=deadline_us, num_ctas=num_ctas,
-                               debug_flags=debug_flags, max_rows=max_rows)
+                               debug_flags=debug_flags, max_rows=max_rows, launch_flags=launch_flags)
         n = L.gdn_decode_workspace_bytes(ctypes.byref(self.cfg))
         if n == 0:
             raise GdnError("gdn_decode_workspace_bytes", _native.GDN_ERR_UNSUPPORTED)
@@ -134,7 +134,7 @@ class GdnDecode:
 
 def step_static(shape, x, residual, weights, state_indices, conv_state, ssm_state, core_out, residual_out,
                 *, stream=None, check: bool = False, engine: str = "auto", deadline_us: int = 0,
-                num_ctas: int = 0, debug_flags: int = 0, max_rows: int | None = None):
+                num_ctas: int = 0, debug_flags: int = 0, max_rows: int | None = None, launch_flags: int = 0):
     """One decode step through gdn_decode_step_static, for callers that cannot
     allocate device memory: the library's fixed device scratch stands in for
     the workspace and there is no handle. Every tensor, outputs included, is
@@ -146,7 +146,7 @@ def step_static(shape, x, residual, weights, state_indices, conv_state, ssm_stat
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
     cfg = make_config(shape, engine=engine, deadline_us=deadline_us, num_ctas=num_ctas,
-                      debug_flags=debug_flags, max_rows=max_rows)
+                      debug_flags=debug_flags, max_rows=max_rows, launch_flags=launch_flags)
     ws = weights if isinstance(weights, _native.Weights) else GdnDecode.weights_struct(weights)
     d = ctypes.c_uint32()
     st = _native.lib().gdn_decode_step_static(

@@ -17,6 +17,7 @@ GDN_W_BF16, GDN_W_MXFP4 = 0, 1
 GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05 = 0, 1, 2
 GDN_DEBUG_SKIP_NORM_PUBLISH = 0x1
 GDN_DEBUG_TIMELINE = 0x2
+GDN_LAUNCH_COOPERATIVE = 0x1
 
 # Every symbol the header declares.
 EXPORTS = (
@@ -37,7 +38,7 @@ class Config(ctypes.Structure):
         ("qkvz_format", ctypes.c_int32), ("engine", ctypes.c_int32),
         ("norm_eps", ctypes.c_float), ("gated_norm_eps", ctypes.c_float), ("l2_eps", ctypes.c_float),
         ("q_scale", ctypes.c_float), ("deadline_us", ctypes.c_uint32), ("num_ctas", ctypes.c_int32),
-        ("debug_flags", ctypes.c_int32),
+        ("debug_flags", ctypes.c_int32), ("launch_flags", ctypes.c_int32),
     ]
 
 

@@ -78,6 +78,7 @@ gdn_status validate(const gdn_decode_config* c) {
   if (c->engine < GDN_ENGINE_AUTO || c->engine > GDN_ENGINE_TCGEN05) return GDN_ERR_ARG;
   if (!(c->norm_eps >= 0.f) || !(c->gated_norm_eps >= 0.f) || !(c->l2_eps >= 0.f)) return GDN_ERR_ARG;
   if (c->num_ctas < 0 || c->num_ctas > kMaxCtas) return GDN_ERR_ARG;
+  if (c->launch_flags & ~GDN_LAUNCH_COOPERATIVE) return GDN_ERR_ARG;
   // Shapes this build runs.
   if (c->conv_kernel != 4) return GDN_ERR_UNSUPPORTED;
   if (c->head_k_dim != c->head_v_dim) return GDN_ERR_UNSUPPORTED;
@@ -495,24 +496,29 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = kernel_smem(pl);
   lc.stream = (cudaStream_t)stream;
-  // Cooperative: every CTA resident at once (they wait on one another).
   // Programmatic stream serialisation: the launch may start while the
   // previous launch in the stream finishes; the kernel reads nothing but the
-  // weights before its griddepcontrol.wait.
+  // weights before its griddepcontrol.wait. Cooperative (on request): every
+  // CTA resident at once, guaranteed by the runtime.
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  if (c.launch_flags & GDN_LAUNCH_COOPERATIVE) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
+  if (h->pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
   lc.attrs = attr;
-  lc.numAttrs = h->pdl ? 2 : 1;
+  lc.numAttrs = na;
   void* args[] = {p};
   cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
   if (e != cudaSuccess && h->pdl) {
-    // the runtime refused the pair of attributes: launch without overlap
+    // the runtime refused programmatic serialisation here: launch without it
     (void)cudaGetLastError();
     h->pdl = false;
-    lc.numAttrs = 1;
+    lc.numAttrs = na - 1;
     e = cudaLaunchKernelExC(&lc, kern, args);
   }
   delete p;
@@ -782,14 +788,23 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = kernel_smem(pl);
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (c.launch_flags & GDN_LAUNCH_COOPERATIVE) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na++].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = na;
   void* args[] = {&p};
-  if (cudaLaunchKernelExC(&lc, pick_kernel(c, pl.engine, residual != nullptr), args) != cudaSuccess)
-    return GDN_ERR_CUDA;
+  const void* kern = pick_kernel(c, pl.engine, residual != nullptr);
+  if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
+    (void)cudaGetLastError();  // without programmatic serialisation
+    lc.numAttrs = na - 1;
+    if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) return GDN_ERR_CUDA;
+  }
   if (!detail) return GDN_OK;
 
   uint32_t word = 0;

@@ -86,6 +86,17 @@ typedef enum {
 #define GDN_DEBUG_TIMELINE 0x2          /* record %globaltimer stamps of each CTA's
                                            phases (read with gdn_decode_debug_timeline) */
 
+/* Launch options (launch_flags). By default a step is an ordinary launch
+ * with programmatic stream serialisation: a step's CTAs start as soon as
+ * SMs free up at the end of the previous step in the stream, and stream the
+ * step's weights before the previous step's results are needed. The step's
+ * CTAs wait on one another, so all of them must be resident at once; create
+ * checks that one CTA per SM fits. If other work holds SMs while a step runs,
+ * its bounded waits run out and it reports GDN_ERR_DEADLINE (it cannot hang).
+ * GDN_LAUNCH_COOPERATIVE makes the runtime guarantee co-residency instead
+ * (cooperative launch), at the cost of that overlap. */
+#define GDN_LAUNCH_COOPERATIVE 0x1
+
 typedef struct {
   int32_t hidden;
   int32_t num_k_heads;
@@ -105,6 +116,7 @@ typedef struct {
   uint32_t deadline_us;    /* bound of every cross-CTA wait; 0 = 200000 */
   int32_t num_ctas;        /* persistent grid size; 0 = one CTA per SM */
   int32_t debug_flags;     /* GDN_DEBUG_*; 0 in production */
+  int32_t launch_flags;    /* GDN_LAUNCH_*; 0 = overlapped launches */
 } gdn_decode_config;
 
 typedef struct {

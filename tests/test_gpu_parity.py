@@ -111,3 +111,14 @@ def test_all_rows_pad(engine):
 def test_auto_engine_is_tensor_core(shape):
     from gated_deltanet_layer_gb300 import GDN_ENGINE_TCGEN05
     assert GdnDecode(shape).launch_info(1)[1] == GDN_ENGINE_TCGEN05
+
+
+@pytest.mark.parametrize("rows", [1, 16])
+def test_cooperative_launch_option(rows):
+    """The opt-in cooperative launch computes the same step."""
+    from gated_deltanet_layer_gb300 import _native
+    case = Case(WL.SHARD, rows, 6000 + rows).to_device()
+    layer = GdnDecode(WL.SHARD, launch_flags=_native.GDN_LAUNCH_COOPERATIVE)
+    core, res_out = case.run_gpu(layer)
+    assert layer.check()[0] == 0
+    compare(case, case.run_oracle(), core, res_out)
