@@ -182,6 +182,11 @@ __device__ __forceinline__ void red_add_relaxed_u64(unsigned long long* p, unsig
 __device__ __forceinline__ void red_add_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ unsigned int atom_add_relaxed_u32(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.relaxed.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ unsigned int atom_add_release_u32(unsigned int* p, unsigned int v) {
   unsigned int old;
   asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

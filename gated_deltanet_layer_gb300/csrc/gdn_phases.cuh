@@ -184,18 +184,62 @@ struct SmemTask {
 // recurrence, state stored in f32 or bf16 in place; pad rows write a zero
 // core row and no state).
 // ---------------------------------------------------------------------------
+// A thread's share of one (row, value head) state tile: NR rows of 4
+// elements (lanes sub = 0..LPR-1 of a row hold 4 consecutive elements each).
+template <int DK>
+struct StateRegs {
+  static constexpr int LPR = DK / 4;              // lanes per state row, 4 elements each
+  static constexpr int RPW = 32 / LPR;            // rows per warp per step
+  static constexpr int NR = DK / (kWarps * RPW);  // rows per lane (dv == dk)
+  uint2 b[NR];   // bf16 state
+  float4 f[NR];  // f32 state
+};
+
+// The CTA's recurrence tasks: (row w, value head h) = task / Hv, task % Hv
+// for task in [t0, t1).
+__device__ __forceinline__ void task_range(const StepParams& p, int& t0, int& t1) {
+  const int T = p.rows * p.Hv;
+  t0 = (int)(((long long)blockIdx.x * T) / p.num_ctas);
+  t1 = (int)(((long long)(blockIdx.x + 1) * T) / p.num_ctas);
+}
+
+// Issue the loads of this thread's share of a task's state tile (nothing for
+// a pad row).
 template <int DK, bool STATE_BF16>
-__device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, SmemTask& st, int L) {
-  constexpr int LPR = DK / 4;              // lanes per state row, 4 elements each
-  constexpr int RPW = 32 / LPR;            // rows per warp per step
-  constexpr int NR = DK / (kWarps * RPW);  // rows per lane (dv == dk)
+__device__ __forceinline__ void load_state(const StepParams& p, int task, StateRegs<DK>& r) {
+  constexpr int NR = StateRegs<DK>::NR, LPR = StateRegs<DK>::LPR, RPW = StateRegs<DK>::RPW;
+  const int w = task / p.Hv, h = task - w * p.Hv;
+  const int slot = p.idx[w];
+  if (!row_is_live(p, slot)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t sbase = ((size_t)slot * p.Hv + h) * (size_t)DK * DK;
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    const int v = (j * kWarps + warp) * RPW + lane / LPR;
+    const size_t off = sbase + (size_t)v * DK + (lane % LPR) * 4;
+    if (STATE_BF16)
+      r.b[j] = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.ssm_state) + off);
+    else
+      r.f[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
+  }
+}
+
+// `raw` holds the first task's state when `have_first` (loaded early, so
+// that its latency hides under the projection); later tasks load into it.
+// sm.flag is 1 on entry (every earlier phase of the launch succeeded); a
+// thread whose wait runs out clears it.
+template <int DK, bool STATE_BF16>
+__device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, SmemTask& st, int L,
+                                                 StateRegs<DK>& raw, bool have_first) {
+  constexpr int LPR = StateRegs<DK>::LPR;
+  constexpr int RPW = StateRegs<DK>::RPW;
+  constexpr int NR = StateRegs<DK>::NR;
   static_assert(NR >= 1 && 4 * DK <= kThreads, "task layout");
-  const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
+  const int cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int sub = lane % LPR, rw = lane / LPR;
-  const int T = W * p.Hv;
-  const int t0 = (int)(((long long)cta * T) / p.num_ctas);
-  const int t1 = (int)(((long long)(cta + 1) * T) / p.num_ctas);
+  int t0, t1;
+  task_range(p, t0, t1);
   for (int task = t0; task < t1; ++task) {
     const int w = task / p.Hv, h = task - w * p.Hv;
     const int slot = p.idx[w];
@@ -207,19 +251,9 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     }
     const int kh = h / p.group;
     // The state rows go into registers first, so their latency overlaps the
-    // wait for the projections.
+    // wait for the projections (the first task's were loaded earlier still).
     const size_t sbase = ((size_t)slot * p.Hv + h) * (size_t)DK * DK;
-    uint2 rawb[NR];
-    float4 rawf[NR];
-#pragma unroll
-    for (int j = 0; j < NR; ++j) {
-      const int v = (j * kWarps + warp) * RPW + rw;
-      const size_t off = sbase + (size_t)v * DK + sub * 4;
-      if (STATE_BF16)
-        rawb[j] = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.ssm_state) + off);
-      else
-        rawf[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
-    }
+    if (!(have_first && task == t0)) load_state<DK, STATE_BF16>(p, task, raw);
     // Per-head constants, also loaded now.
     const float A_log_h = p.A_log[h];
     const float dt_bias_h = bf16_to_f(p.dt_bias[h]);
@@ -235,9 +269,6 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     auto tile_of = [&](int n) -> int {
       return n < p.Nqkvz ? (n >> kTileShift) : p.tiles_qkvz + ((n - p.Nqkvz) >> kTileShift);
     };
-    if (tid == 0) sm.flag = 1;
-    __syncthreads();
-
     // Projection outputs, each the sum of its tile's partials in slot order,
     // polled as tagged words of this launch. Thread i < 4*dk takes output i
     // (q, k, v, z); b and a take one slot per lane of the last two warps.
@@ -322,24 +353,24 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     if (!sm.flag) return false;
     unsigned int group_old = 0;
     if (tid == 0) {
-      // every thread's reads of the old q/k taps are done (their values are
-      // used): count this reader; the result is needed only at the end
-      group_old = atom_add_release_u32(&p.ctr->conv_group[w][kh], 1u);
+      // Every thread's reads of the old q/k taps are done: their values were
+      // used before the barrier above, so no later store can reach them. The
+      // count needs no release (a release here waits for every store the CTA
+      // has in flight); its result is needed only at the end.
+      group_old = atom_add_relaxed_u32(&p.ctr->conv_group[w][kh], 1u);
       if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
     }
-    // L2 norms of q and k: warps 0..DK/32-1 sum q^2, the next as many k^2
-    if (warp < 2 * (DK / 32)) {
-      const bool isq = warp < DK / 32;
-      const float y = isq ? st.q[warp * 32 + lane] : st.k[(warp - DK / 32) * 32 + lane];
-      const float s = warp_sum(y * y);
-      if (lane == 0) sm.red[warp] = s;
-    }
-    __syncthreads();
+    // L2 norms of q and k: every warp sums all of q^2 and k^2 itself (the
+    // same order in every warp), which saves a CTA barrier
     float sq = 0.f, sk = 0.f;
+#pragma unroll
     for (int i = 0; i < DK / 32; ++i) {
-      sq += sm.red[i];
-      sk += sm.red[DK / 32 + i];
+      const float a = st.q[i * 32 + lane], b = st.k[i * 32 + lane];
+      sq = fmaf(a, a, sq);
+      sk = fmaf(b, b, sk);
     }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
     const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
     const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
     const float4 kq = *reinterpret_cast<const float4*>(&st.k[sub * 4]);
@@ -356,10 +387,10 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
       if (STATE_BF16) {
-        s[j][0] = bf16_lo(rawb[j].x); s[j][1] = bf16_hi(rawb[j].x);
-        s[j][2] = bf16_lo(rawb[j].y); s[j][3] = bf16_hi(rawb[j].y);
+        s[j][0] = bf16_lo(raw.b[j].x); s[j][1] = bf16_hi(raw.b[j].x);
+        s[j][2] = bf16_lo(raw.b[j].y); s[j][3] = bf16_hi(raw.b[j].y);
       } else {
-        s[j][0] = rawf[j].x; s[j][1] = rawf[j].y; s[j][2] = rawf[j].z; s[j][3] = rawf[j].w;
+        s[j][0] = raw.f[j].x; s[j][1] = raw.f[j].y; s[j][2] = raw.f[j].z; s[j][3] = raw.f[j].w;
       }
     }
     // S k over all rows of this lane at once (independent butterflies)
@@ -406,13 +437,14 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       if (sub == 0) st.o[(j * kWarps + warp) * RPW + rw] = ov[j];
     if (tid == 0) st.last = ((group_old + 1) % (unsigned)p.group) == 0;
     __syncthreads();
-    if (warp == 0) {
+    float rn = 0.f;
+    if (warp < DK / 32) {  // the warps that write core: each sums o^2 itself (same order)
       float q = 0.f;
-      for (int i = lane; i < DK; i += 32) q = fmaf(st.o[i], st.o[i], q);
+#pragma unroll
+      for (int i = 0; i < DK / 32; ++i) q = fmaf(st.o[i * 32 + lane], st.o[i * 32 + lane], q);
       q = warp_sum(q);
-      if (lane == 0) sm.red[0] = 1.0f / sqrtf(q / (float)DK + p.gnorm_eps);
+      rn = 1.0f / sqrtf(q / (float)DK + p.gnorm_eps);
     }
-    __syncthreads();
     if (st.last) {  // the last reader of the group writes the new q/k taps
       for (int i = tid; i < 2 * DK; i += kThreads) {
         const int n = proj_row(i);
@@ -422,7 +454,6 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
         cs[2] = __float2bfloat16_rn(st.cnew[i][2]);
       }
     }
-    const float rn = sm.red[0];
     if (tid < DK) core[tid] = __float2bfloat16_rn(st.o[tid] * rn * gw * silu_f(st.z[tid]));
     if ((p.debug_flags & kDebugTimeline) && task == t0 && tid == 0)
       p.ctr->tl_cta[cta][TL_REC_STATE] = globaltimer_ns();

@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   phase_norm_partials<HAS_RES>(p, sm, L);
   if (!phase_normed_input(p, sm, L)) return;
   if (!phase_proj_cuda_core(p, sm, ds.xs, L)) return;
-  phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
+  StateRegs<DK> none;
+  phase_recurrence<DK, STATE_BF16>(p, sm, st, L, none, false);
   tl_stamp(p, TL_END);
 }
 

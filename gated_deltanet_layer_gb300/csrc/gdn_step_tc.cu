@@ -143,28 +143,6 @@ static __device__ __forceinline__ void start_weight_stream(const StepParams& p, 
   if (from == 0) tl_stamp_here(p, TL_ISSUED);
 }
 
-// L2 prefetch of the state this CTA's recurrence tasks read, and of the conv
-// state rows of the step (read by the recurrence tasks of each row).
-template <int DK, bool STATE_BF16>
-static __device__ __forceinline__ void prefetch_states(const StepParams& p) {
-  const int cta = blockIdx.x;
-  const int T = p.rows * p.Hv;
-  const int t0 = (int)(((long long)cta * T) / p.num_ctas);
-  const int t1 = (int)(((long long)(cta + 1) * T) / p.num_ctas);
-  constexpr uint32_t bytes = DK * DK * (STATE_BF16 ? 2 : 4);
-  for (int task = t0; task < t1; ++task) {
-    const int w = task / p.Hv, h = task - w * p.Hv;
-    const int slot = p.idx[w];
-    if (row_is_live(p, slot))
-      tc::prefetch_l2_bulk(static_cast<const char*>(p.ssm_state) + ((size_t)slot * p.Hv + h) * bytes, bytes);
-  }
-  if (cta < p.rows) {
-    const int slot = p.idx[cta];
-    if (row_is_live(p, slot))
-      tc::prefetch_l2_bulk(p.conv_state + (size_t)slot * p.C * 3, (uint32_t)p.C * 6);
-  }
-}
-
 // The A operand of this CTA: the normed input xn of its k-steps as slices in
 // shared memory. Slot j holds k-step (ks_first + j) mod ksteps, 16 rows x 64
 // columns bf16 in the 128-byte swizzled K-major layout (row r at r * 128
@@ -472,7 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const int L = sm.L;
   publish_norm_partials(p, sq, L);
   if (tid == 32) start_weight_stream(p, ts, sW, ub, first, issued);
-  if (tid == 64) prefetch_states<DK, STATE_BF16>(p);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
     if (tid == 32)  // let the weight tiles in flight land before the CTA exits
@@ -490,6 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tc::tc_fence_after();
   const uint32_t tmem = ts.tmem_base;
   tl_stamp(p, TL_PROJ_START);
+  // The first recurrence task's state goes into registers now: its latency
+  // hides under the projection, which leaves most threads idle.
+  StateRegs<DK> first_state;
+  int rt0, rt1;
+  task_range(p, rt0, rt1);
+  if (rt0 < rt1) load_state<DK, STATE_BF16>(p, rt0, first_state);
   int issued_total = issued;
   if (nunits > 0) {
     if (tid == 0)
@@ -516,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   tl_stamp(p, TL_PROJ_END);
   if (!aborted) {
-    phase_recurrence<DK, STATE_BF16>(p, sm, st, L);
+    phase_recurrence<DK, STATE_BF16>(p, sm, st, L, first_state, rt0 < rt1);
     tl_stamp(p, TL_END);
   }
 }
