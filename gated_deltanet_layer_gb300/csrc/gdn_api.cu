@@ -30,9 +30,10 @@ struct Plan {
   unsigned char nb_slots[kMaxCtas];
   unsigned char tile_count[kMaxTiles];
   unsigned int own_mask[kMaxCtas];
-  // tensor-core engine: weight ring depth, normed-input window (k-steps),
-  // the pad past it, and the launch's dynamic shared memory
-  int stages, xslots;
+  // tensor-core engine: weight ring depth (bf16 tiles), raw ring depth (MXFP4
+  // code tiles), normed-input window (k-steps), the pad past it, and the
+  // launch's dynamic shared memory
+  int stages, rstages, xslots;
   unsigned int xpad;
   size_t smem;
 };
@@ -89,7 +90,8 @@ gdn_status validate(const gdn_decode_config* c) {
   if ((c->num_k_heads * c->head_k_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if ((c->num_v_heads * c->head_v_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if (c->hidden % kKStep != 0 || c->hidden > (1 << 20)) return GDN_ERR_UNSUPPORTED;
-  if (c->qkvz_format == GDN_W_MXFP4) return GDN_ERR_UNSUPPORTED;
+  // MXFP4: a row's e8m0 scales for 8 k-steps are one aligned 16-byte load
+  if (c->qkvz_format == GDN_W_MXFP4 && (c->hidden % 512 != 0 || c->head_k_dim != 128)) return GDN_ERR_UNSUPPORTED;
   const int tiles = n_qkvz(*c) / kTileM + (n_ba(*c) + kTileM - 1) / kTileM;
   if (tiles > kMaxTiles) return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
@@ -194,19 +196,22 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
   }
   pl->max_contrib = maxc;
   if (engine == GDN_ENGINE_TCGEN05) {
-    // the ring takes what the window leaves: 2..6 tiles of 32 KB
+    // the ring takes what the window (two windows with MXFP4 weights: xn and
+    // its quantised copy) and the raw ring leave: 2..6 tiles of 32 KB
+    const bool fp4 = c.qkvz_format == GDN_W_MXFP4;
     int xs = 1;
     for (int cta = 0; cta < G; ++cta) xs = std::max(xs, (int)pl->nb_slots[cta]);
     pl->xslots = xs;
     pl->xpad = tensor_core_xpad(xs);
-    const size_t fixed = tensor_core_smem_bytes(0, xs);
     const size_t avail = kSmemOptin - tensor_core_static_smem() - 1024;
-    if (fixed + 2 * (size_t)kTileM * kKStep * 2 > avail) return GDN_ERR_UNSUPPORTED;
-    pl->stages = (int)std::min<size_t>((avail - fixed) / ((size_t)kTileM * kKStep * 2),
-                                       (size_t)tensor_core_max_stages());
-    pl->smem = tensor_core_smem_bytes(pl->stages, xs);
+    const size_t wtile = (size_t)kTileM * kKStep * 2;
+    pl->rstages = fp4 ? tensor_core_max_rstages() : 0;
+    const size_t fixed = tensor_core_smem_bytes(0, pl->rstages, xs, fp4);
+    if (fixed + 2 * wtile > avail) return GDN_ERR_UNSUPPORTED;
+    pl->stages = (int)std::min<size_t>((avail - fixed) / wtile, (size_t)tensor_core_max_stages());
+    pl->smem = tensor_core_smem_bytes(pl->stages, pl->rstages, xs, fp4);
   } else {
-    pl->stages = pl->xslots = 0;
+    pl->stages = pl->rstages = pl->xslots = 0;
     pl->xpad = 0;
     pl->smem = cuda_core_smem_bytes();
   }
@@ -246,7 +251,7 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
   const bool b16 = c.ssm_dtype == GDN_STATE_BF16;
-  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim)
+  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format == GDN_W_MXFP4)
                                       : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
@@ -265,12 +270,17 @@ void set_plan_params(const Plan& pl, StepParams* p) {
   p->tiles_qkvz = pl.tiles_qkvz; p->num_tiles = pl.num_tiles; p->ksteps = pl.ksteps;
   p->norm_chunk = pl.norm_chunk; p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
   p->kblock = pl.kblock;
-  p->stages = pl.stages; p->xslots = pl.xslots; p->xpad = pl.xpad;
+  p->stages = pl.stages; p->rstages = pl.rstages; p->xslots = pl.xslots; p->xpad = pl.xpad;
 }
 
 // The engine a config runs with and its plan: the requested engine, or for
-// GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA cores.
+// GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA
+// cores. MXFP4 weights run on the tensor-core engine only.
 gdn_status resolve_plan(const gdn_decode_config& c, int G, Plan* pl) {
+  if (c.qkvz_format == GDN_W_MXFP4) {
+    if (c.engine == GDN_ENGINE_CUDA_CORE) return GDN_ERR_UNSUPPORTED;
+    return make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
+  }
   if (c.engine == GDN_ENGINE_CUDA_CORE) return make_plan(c, G, GDN_ENGINE_CUDA_CORE, pl);
   const gdn_status st = make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
   if (st == GDN_OK || c.engine == GDN_ENGINE_TCGEN05) return st;
@@ -309,6 +319,34 @@ bool encode_weight_map(CUtensorMap* m, const void* base, int rows, int H) {
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tile map of MXFP4 codes [rows][H/2] uint8: box 32 bytes (64 codes) x 256
+// rows, no swizzle (the decoding warps read each row's 32 bytes).
+bool encode_code_map(CUtensorMap* m, const void* base, int rows, int H) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)H / 2, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)H / 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kKStep / 2, (cuuint32_t)kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Bytes of in_proj_qkvz as the config stores it.
+size_t qkvz_bytes(const gdn_decode_config& c) {
+  const size_t n = (size_t)n_qkvz(c), H = (size_t)c.hidden;
+  return c.qkvz_format == GDN_W_MXFP4 ? n * H / 2 : n * H * 2;
+}
+
+// The weight tile maps of a step: in_proj_qkvz (bf16, or MXFP4 codes) and
+// in_proj_ba (bf16).
+bool encode_maps(const gdn_decode_config& c, const gdn_decode_weights* w, CUtensorMap* mq, CUtensorMap* mba) {
+  const bool okq = c.qkvz_format == GDN_W_MXFP4 ? encode_code_map(mq, w->qkvz, n_qkvz(c), c.hidden)
+                                                : encode_weight_map(mq, w->qkvz, n_qkvz(c), c.hidden);
+  return okq && encode_weight_map(mba, w->ba, n_ba(c), c.hidden);
 }
 
 }  // namespace
@@ -419,6 +457,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   if (!x || !state_indices || !conv_state || !ssm_state || !core_out || !residual_out) return GDN_ERR_ARG;
   if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
     return GDN_ERR_ARG;
+  if (c.qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
   const void* a16[] = {x, residual, core_out, residual_out, conv_state, ssm_state, w->input_norm_w,
                        w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
   for (const void* p : a16)
@@ -432,8 +471,9 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
   struct Rg { const void* p; size_t n; };
   const Rg ins[] = {{x, xb}, {residual, residual ? xb : 0}, {state_indices, (size_t)rows * 4},
-                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, (size_t)n_qkvz(c) * H * 2},
+                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
                     {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
+                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
                     {h->ws, h->lay.total}};
   const Rg outs[] = {{core_out, coreb}, {residual_out, xb}};
   for (const Rg& o : outs)
@@ -464,6 +504,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->w_in = (const __nv_bfloat16*)w->input_norm_w;
   p->w_qkvz = (const __nv_bfloat16*)w->qkvz;
   p->w_qkvz_scales = w->qkvz_scales;
+  p->fp4 = c.qkvz_format == GDN_W_MXFP4;
   p->w_ba = (const __nv_bfloat16*)w->ba;
   p->conv_w = (const __nv_bfloat16*)w->conv_w;
   p->A_log = w->A_log;
@@ -477,8 +518,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   p->plan = (const PlanDev*)(base + h->lay.plan);
   // weight tile maps (cached for the last weights seen)
   if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
-    if (!encode_weight_map(&h->map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
-        !encode_weight_map(&h->map_ba, w->ba, n_ba(c), c.hidden)) {
+    if (!encode_maps(c, w, &h->map_qkvz, &h->map_ba)) {
       h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
       delete p;
       return GDN_ERR_CUDA;
@@ -707,6 +747,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   if (!x || !state_indices || !conv_state || !ssm_state || !core_out || !residual_out) return GDN_ERR_ARG;
   if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
     return GDN_ERR_ARG;
+  if (cfg->qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
   const void* a16[] = {x, residual, core_out, residual_out, conv_state, ssm_state, w->input_norm_w,
                        w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
   for (const void* p : a16)
@@ -728,8 +769,9 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
   struct Rg { const void* p; size_t n; };
   const Rg ins[] = {{x, xb}, {residual, residual ? xb : 0}, {state_indices, (size_t)rows * 4},
-                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, (size_t)n_qkvz(c) * H * 2},
+                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
                     {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
+                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
                     {d.scratch, d.lay.total}};
   const Rg outs[] = {{core_out, coreb}, {residual_out, xb}};
   for (const Rg& o : outs)
@@ -759,6 +801,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   p.w_in = (const __nv_bfloat16*)w->input_norm_w;
   p.w_qkvz = (const __nv_bfloat16*)w->qkvz;
   p.w_qkvz_scales = w->qkvz_scales;
+  p.fp4 = c.qkvz_format == GDN_W_MXFP4;
   p.w_ba = (const __nv_bfloat16*)w->ba;
   p.conv_w = (const __nv_bfloat16*)w->conv_w;
   p.A_log = w->A_log;
@@ -771,8 +814,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   p.proj_part = (unsigned long long*)(base + d.lay.proj_part);
   p.plan = (const PlanDev*)(base + d.lay.plan);
   if (d.map_qkvz_ptr != w->qkvz || d.map_ba_ptr != w->ba) {
-    if (!encode_weight_map(&d.map_qkvz, w->qkvz, n_qkvz(c), c.hidden) ||
-        !encode_weight_map(&d.map_ba, w->ba, n_ba(c), c.hidden)) {
+    if (!encode_maps(c, w, &d.map_qkvz, &d.map_ba)) {
       d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
       return GDN_ERR_CUDA;
     }

@@ -70,7 +70,9 @@ struct StepParams {
   int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
   int max_contrib;     // most CTAs contributing to one tile
   int num_ctas;
-  int stages;          // weight tiles in flight per CTA (tensor-core engine)
+  int fp4;             // in_proj_qkvz is MXFP4 (codes + e8m0 scales; tensor-core engine)
+  int stages;          // bf16 weight tiles in flight per CTA (tensor-core engine)
+  int rstages;         // MXFP4 code tiles in flight per CTA
   int xslots;          // normed-input k-steps a CTA keeps in shared memory
   unsigned int xpad;   // bytes past the window an MMA may read (and norm-sum scratch)
   float norm_eps, gnorm_eps, l2_eps, q_scale;
@@ -98,8 +100,9 @@ struct StepParams {
   unsigned long long* norm_part;  // [kMaxRows][num_ctas] tagged words
   __nv_bfloat16* xn;              // [kMaxRows][H] (CUDA-core engine)
   unsigned long long* proj_part;  // [num_tiles][max_contrib][kMaxRows][kTileM] tagged words
-  // TMA descriptors of the bf16 weights (box 64 columns x 256 rows, 128-byte
-  // swizzle); used by the tensor-core engine and for L2 prefetches.
+  // TMA descriptors of the weights: bf16 boxes of 64 columns x 256 rows with
+  // 128-byte swizzle, or for MXFP4 in_proj_qkvz uint8 boxes of 32 bytes (64
+  // codes) x 256 rows (tensor-core engine).
   CUtensorMap tm_qkvz;
   CUtensorMap tm_ba;
   const struct PlanDev* plan;  // stream-K plan, in the workspace (written once at create)

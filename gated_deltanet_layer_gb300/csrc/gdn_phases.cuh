@@ -149,7 +149,7 @@ __device__ __forceinline__ void group_sync() {
   else if (NT == 32)
     __syncwarp();
   else
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+    asm volatile("barrier.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
 // Shared memory of one recurrence task.

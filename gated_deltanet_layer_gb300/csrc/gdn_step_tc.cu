@@ -47,13 +47,26 @@ constexpr uint32_t kWinBytes = kKStep * 2;              // input-norm weights of
 constexpr uint32_t kTmemCols = 2 * kTileM;              // two 128 x 256 f32 accumulators
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(64, kTileM);
 static_assert(kMaxBSlots <= 32, "one owner bit per window slot");
+constexpr uint32_t kRBytes = kTileM * kKStep / 2;      // 8 KB MXFP4 code tile (256 rows x 32 bytes)
+constexpr int kMaxRStages = 4;                          // code tiles in flight per CTA (MXFP4)
+// Warps that decode MXFP4 code tiles into bf16 tiles: thread i of them owns
+// row i of the 256-row tile. (Warp 0 holds the TMA producer, warp 1 the MMA
+// issuer, warps 4 and 8 the drain.)
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps;
+__device__ __forceinline__ int conv_index(int warp) {
+  // warps 2, 3, 5, 6, 7, 9, 10, 11 -> 0..7
+  return warp == 2 ? 0 : warp == 3 ? 1 : (warp >= 5 && warp <= 7) ? warp - 3 : (warp >= 9 && warp <= 11) ? warp - 4 : -1;
+}
 constexpr uint32_t kWaitPipe = 4;                       // error-word id of a pipeline wait
 constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on the abort path
 }  // namespace
 
 struct TcShared {
-  uint64_t full[kMaxStages];   // weight tile landed (TMA complete_tx)
+  uint64_t full[kMaxStages];   // bf16 weight tile ready (TMA complete_tx, or the MXFP4 decode done)
   uint64_t empty[kMaxStages];  // MMAs of the stage done (tcgen05.commit)
+  uint64_t rfull[kMaxRStages];   // MXFP4 code tile landed (TMA complete_tx)
+  uint64_t rempty[kMaxRStages];  // MXFP4 code tile decoded
   uint64_t acc_full[2];     // accumulator ready for the drain
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
@@ -122,24 +135,75 @@ __device__ __forceinline__ const CUtensorMap* weight_map(const StepParams& p, in
   return &p.tm_ba;
 }
 
-// Unit n's weight tile into ring stage s.
-__device__ __forceinline__ void issue_weight_tile(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                  const UnitIter& it, int n, int s, uint64_t pol) {
+// A unit whose weights are MXFP4 codes (decoded to bf16 in shared memory
+// before the MMA); the others are bf16 tiles the MMA reads as loaded.
+__device__ __forceinline__ bool unit_coded(const StepParams& p, const UnitIter& it) {
+  return p.fp4 && it.t < p.tiles_qkvz;
+}
+
+// Ring positions along a CTA's units: every unit takes the next bf16 stage
+// (s, phase ph); a coded unit also the next code stage (r, phase rph).
+struct RingPos {
+  int s = 0, r = 0;
+  uint32_t ph = 0, rph = 0;
+  __device__ __forceinline__ void advance(const StepParams& p, bool coded) {
+    if (++s == p.stages) { s = 0; ph ^= 1; }
+    if (coded && ++r == p.rstages) { r = 0; rph ^= 1; }
+  }
+};
+
+// Unit n's weights: MXFP4 codes into code stage pos.r, else a bf16 tile into
+// stage pos.s (the caller has made sure the stage is free).
+__device__ __forceinline__ void issue_unit(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
+                                           const UnitIter& it, int n, const RingPos& pos, uint64_t pol) {
   int row0;
   const CUtensorMap* m = weight_map(p, it.t, row0);
-  tc::mbar_arrive_expect_tx(&ts.full[s], kWBytes);
-  tc::tma_load_2d(sW + (size_t)s * kWBytes, m, it.ks * kKStep, row0, &ts.full[s], pol);
+  if (unit_coded(p, it)) {
+    tc::mbar_arrive_expect_tx(&ts.rfull[pos.r], kRBytes);
+    tc::tma_load_2d(sR + (size_t)pos.r * kRBytes, m, it.ks * (kKStep / 2), row0, &ts.rfull[pos.r], pol);
+  } else {
+    tc::mbar_arrive_expect_tx(&ts.full[pos.s], kWBytes);
+    tc::tma_load_2d(sW + (size_t)pos.s * kWBytes, m, it.ks * kKStep, row0, &ts.full[pos.s], pol);
+  }
   if (n < 16) tl_stamp_here(p, TL_UNIT_ISSUED + n);
 }
 
-// Units [from, to) of the CTA's weight stream into the ring's first stages
-// (one thread; to <= the ring depth).
+// Ring positions after the CTA's first n units.
+__device__ __forceinline__ RingPos ring_pos_at(const StepParams& p, int ub, int n) {
+  RingPos pos;
+  UnitIter it(p, ub);
+  for (int j = 0; j < n; ++j, it.next()) pos.advance(p, unit_coded(p, it));
+  return pos;
+}
+
+// The CTA's leading units that fit the rings before any stage is reused (at
+// most `cap`): the ones issued without waiting.
+__device__ __forceinline__ int prefill_units(const StepParams& p, int ub, int nunits, int cap) {
+  UnitIter it(p, ub);
+  int coded = 0, n = 0;
+  for (; n < min(nunits, cap); ++n, it.next()) {
+    if (unit_coded(p, it)) {
+      if (coded == p.rstages) break;
+      ++coded;
+    } else if (n >= p.stages) {
+      break;
+    }
+  }
+  return n;
+}
+
+// Units [from, to) of the CTA's weight stream, all within the prefill (one
+// thread, no waits).
 static __device__ __forceinline__ void start_weight_stream(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                           int ub, int from, int to) {
+                                                           uint8_t* sR, int ub, int from, int to) {
   if (from >= to) return;
   const uint64_t pol0 = tc::policy_evict_first();
+  RingPos pos = ring_pos_at(p, ub, from);
   UnitIter it(p, ub + from);
-  for (int n = from; n < to; ++n, it.next()) issue_weight_tile(p, ts, sW, it, n, n, pol0);
+  for (int n = from; n < to; ++n, it.next()) {
+    issue_unit(p, ts, sW, sR, it, n, pos, pol0);
+    pos.advance(p, unit_coded(p, it));
+  }
   if (from == 0) tl_stamp_here(p, TL_ISSUED);
 }
 
@@ -263,34 +327,194 @@ static __device__ __forceinline__ void publish_norm_partials(const StepParams& p
   tl_stamp(p, TL_NORM_OUT);
 }
 
+// f32 2^e for e in [-127, 127] (exact; 2^-127 is subnormal).
+static __device__ __forceinline__ float exp2_int(int e) {
+  return e == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// MXFP4 quantisation of one row's block of 32 normed inputs, 8 of them in
+// this thread (the block's 4 chunks are 4 consecutive lanes): the block scale
+// 2^E from the block maximum with its mantissa rounded half up to one bit,
+// E = its exponent - 2 clamped to [-127, 127]; each value |x| / 2^E rounded
+// to the e2m1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} (ties to even, saturating at
+// 6), returned dequantised (exact in bf16). The dynamic MX quantiser of
+// vLLM #60833 (review "How to make the MXFP6 weights", step 2) with E2M1's
+// largest exponent, 2.
+static __device__ __forceinline__ uint4 quantize8_mxfp4(uint4 xv) {
+  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+  float v[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = bf16_lo(xs[e]);
+    v[2 * e + 1] = bf16_hi(xs[e]);
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
+  const unsigned mask = __activemask();
+  m = fmaxf(m, __shfl_xor_sync(mask, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(mask, m, 2));
+  int E = (int)(((__float_as_uint(m) + (1u << 21)) >> 23) & 0xffu) - 127 - 2;
+  E = max(-127, min(127, E));
+  const float inv = exp2_int(-E), scale = exp2_int(E);
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float q[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float a = fabsf(v[2 * e + h]) * inv;              // exact
+      const float st = a < 2.f ? 0.5f : (a < 4.f ? 1.f : 2.f);  // grid spacing
+      const float r = fminf(rintf(a / st) * st, 6.f);           // ties to even
+      q[h] = copysignf(r, v[2 * e + h]) * scale;
+    }
+    o[e] = pack_bf16x2(q[0], q[1]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// xn = bf16(r * rstd * (1 + w)) in place; with MXFP4 weights also its
+// quantised copy in the second window sXq (same layout).
 static __device__ __forceinline__ void finish_normed_slices(const StepParams& p, const SmemPhases& sm,
-                                                            uint8_t* sX, const uint8_t* sWin) {
+                                                            uint8_t* sX, uint8_t* sXq, const uint8_t* sWin) {
   const int cta = blockIdx.x, W = p.rows;
-  const int ntask = p.plan->nb_slots[cta] * W * 8;  // (slot, row < W, chunk)
+  const int ntask = p.plan->nb_slots[cta] * W * 8;  // (slot, row < W, chunk); a multiple of 8
   for (int i = threadIdx.x; i < ntask; i += kThreads) {
     const int j = i / (W * 8), rem = i - j * (W * 8), w = rem >> 3, c = rem & 7;
-    uint4* d = reinterpret_cast<uint4*>(sX + (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4));
-    *d = normed8(*d, reinterpret_cast<const uint4*>(sWin + (size_t)j * kWinBytes)[c], sm.rstd[w]);
+    const size_t off = (size_t)j * kXBytes + w * 128 + ((c ^ (w & 7)) << 4);
+    uint4* d = reinterpret_cast<uint4*>(sX + off);
+    const uint4 xv = normed8(*d, reinterpret_cast<const uint4*>(sWin + (size_t)j * kWinBytes)[c], sm.rstd[w]);
+    *d = xv;
+    if (p.fp4) *reinterpret_cast<uint4*>(sXq + off) = quantize8_mxfp4(xv);
   }
 }
 
-// TMA producer: weight tiles `issued`.. into the ring, each into a stage the
-// MMAs have released. Returns the number of units issued. (An L2 prefetch
-// ahead of the ring was measured: the tensor form does not bring tiles in
-// early, and per-row prefetches delay the latency-bound norm hand-off more
-// than they shorten the projection.)
-static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, int ub,
-                                                   int nunits, int issued, uint64_t pol) {
+// TMA producer: units `issued`.. into the rings, each into a stage that has
+// been released (a bf16 stage by the MMAs, a code stage by the decode).
+// Returns the number of units issued. (An L2 prefetch ahead of the ring was
+// measured: the tensor form does not bring tiles in early, and per-row
+// prefetches delay the latency-bound norm hand-off more than they shorten
+// the projection.)
+static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
+                                                   int ub, int nunits, int issued, uint64_t pol) {
   UnitIter it(p, ub + issued);
-  int s = issued % p.stages;
-  uint32_t ph = (uint32_t)(issued / p.stages) & 1;
+  RingPos pos = ring_pos_at(p, ub, issued);
   for (int n = issued; n < nunits; ++n) {
-    if (!pipe_wait(p, ts, &ts.empty[s], ph ^ 1)) return n;
-    issue_weight_tile(p, ts, sW, it, n, s, pol);
+    const bool coded = unit_coded(p, it);
+    if (coded) {
+      if (!pipe_wait(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
+    } else if (!pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
+      return n;
+    }
+    issue_unit(p, ts, sW, sR, it, n, pos, pol);
+    pos.advance(p, coded);
     it.next();
-    if (++s == p.stages) { s = 0; ph ^= 1; }
   }
   return nunits;
+}
+
+// MXFP4 decode (kConvThreads threads, thread i owns row i of the tile): per
+// coded unit, wait for its code tile and for its bf16 stage to be free, turn
+// each row's 64 e2m1 codes and their two e8m0 block scales into bf16
+// (code value x 2^(scale - 127), exact in bf16) in the 128-byte swizzled
+// K-major layout the MMA reads, then release the code stage and hand the bf16
+// stage to the MMA. A row's scales for 8 k-steps are one aligned 16-byte
+// load, issued a block ahead.
+static __device__ __forceinline__ float e8m0_scale(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);  // 2^(e - 127); e = 0: 2^-127
+}
+// Value of a 4-bit e2m1 code (sign bit 3, exponent bits 2..1 with bias 1,
+// mantissa bit 0; exponent 0: 0 or 0.5), built from its f32 bits.
+static __device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t m = c & 7u;
+  const uint32_t mag = m < 2u ? (m ? 0x3f000000u : 0u) : ((126u + (m >> 1)) << 23) | ((m & 1u) << 22);
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
+// All-threads-of-a-named-barrier AND of a predicate (every thread gets it).
+static __device__ __forceinline__ bool bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kConvThreads)
+      : "memory");
+  return r != 0;
+}
+static __device__ __forceinline__ uint4 scale_block(const StepParams& p, const UnitIter& it, int row) {
+  const int grow = (it.t * kTileM) + row;  // coded units are in_proj_qkvz rows
+  return ld_stream_v4(p.w_qkvz_scales + (size_t)grow * (p.H / 32) + (it.ks >> 3) * 16);
+}
+static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
+                                                   const uint8_t* sR, int ub, int nunits, int ci) {
+  UnitIter it(p, ub);
+  RingPos pos;
+  int blk_t = -1, blk_k = -1;  // the 8-k-step scale block held in `cur`
+  uint4 cur = make_uint4(0, 0, 0, 0), nxt = make_uint4(0, 0, 0, 0);
+  int nxt_t = -1, nxt_k = -1;
+  // the first coded unit's block
+  {
+    UnitIter f(p, ub);
+    for (int n = 0; n < nunits; ++n, f.next())
+      if (unit_coded(p, f)) {
+        nxt = scale_block(p, f, ci);
+        nxt_t = f.t;
+        nxt_k = f.ks >> 3;
+        break;
+      }
+  }
+  for (int n = 0; n < nunits; ++n) {
+    const bool coded = unit_coded(p, it);
+    if (coded) {
+      if (it.t != blk_t || (it.ks >> 3) != blk_k) {
+        // this unit starts a new scale block: take the prefetched one, prefetch the next
+        cur = nxt;
+        blk_t = nxt_t;
+        blk_k = nxt_k;
+        UnitIter f = it;
+        for (int j = n + 1; j < nunits; ++j) {
+          f.next();
+          if (unit_coded(p, f) && (f.t != blk_t || (f.ks >> 3) != blk_k)) {
+            nxt = scale_block(p, f, ci);
+            nxt_t = f.t;
+            nxt_k = f.ks >> 3;
+            break;
+          }
+        }
+      }
+      bool ok = pipe_wait(p, ts, &ts.rfull[pos.r], pos.rph);
+      ok = ok && pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1);
+      if (!bar_and(ok)) return;  // the same decision in every decoding thread (bounded waits)
+      const uint4* src = reinterpret_cast<const uint4*>(sR + (size_t)pos.r * kRBytes + ci * 32);
+      const uint4 c0 = src[0], c1 = src[1];
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const int kk = it.ks & 7;  // k-step within the block: scale bytes 2kk, 2kk + 1
+      const uint32_t sw4 = (kk >> 1) == 0 ? cur.x : (kk >> 1) == 1 ? cur.y : (kk >> 1) == 2 ? cur.z : cur.w;
+      const uint32_t sword = sw4 >> ((kk & 1) * 16);
+      const float sc[2] = {e8m0_scale(sword & 0xffu), e8m0_scale((sword >> 8) & 0xffu)};
+      uint8_t* dst = sW + (size_t)pos.s * kWBytes + ci * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // 8 columns per 16-byte chunk, from one 32-bit word of codes
+        const uint32_t wv = words[c];
+        const float scale = sc[c >> 2];
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = (wv >> (8 * e)) & 0xfu, hi = (wv >> (8 * e + 4)) & 0xfu;
+          o[e] = pack_bf16x2(e2m1_value(lo) * scale, e2m1_value(hi) * scale);  // exact in bf16
+        }
+        *reinterpret_cast<uint4*>(dst + ((c ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      tc::fence_proxy_async_smem();  // the generic-proxy writes, visible to the MMA
+      asm volatile("barrier.sync 2, %0;" ::"n"(kConvThreads) : "memory");
+      if (ci == 0) {
+        tc::mbar_arrive(&ts.rempty[pos.r]);
+        tc::mbar_arrive(&ts.full[pos.s]);
+      }
+    }
+    pos.advance(p, coded);
+    it.next();
+  }
 }
 
 // MMA issuer: per unit, 4 MMAs of K = 16 over the stage's 64 columns into the
@@ -298,7 +522,7 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
 // overwriting. Commits release the stage and, at a segment's end, hand the
 // accumulator to the drain.
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                uint8_t* sX, int ub, int nunits, uint32_t tmem) {
+                                                uint8_t* sX, uint8_t* sXq, int ub, int nunits, uint32_t tmem) {
   // Stage and phase advance incrementally: a division per unit by the
   // runtime ring depth costs the loop more than the tensor core's own time.
   const int ks0 = p.plan->ks_first[blockIdx.x], KS = p.ksteps, S = p.stages;
@@ -307,7 +531,7 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   bool seg_open = false;
   int s = 0;
   uint32_t ph = 0;
-  const uint32_t sw0 = tc::smem_u32(sW), sx0 = tc::smem_u32(sX);
+  const uint32_t sw0 = tc::smem_u32(sW), sx0 = tc::smem_u32(sX), sxq0 = tc::smem_u32(sXq);
   for (int n = 0; n < nunits; ++n) {
     const bool first = !seg_open;
     if (first) {
@@ -323,7 +547,8 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
     int slot = it.ks - ks0;
     if (slot < 0) slot += KS;
     if (n == 0) tl_stamp_here(p, TL_MMA_FIRST);
-    const uint64_t ad = tc::sdesc_k_sw128(sx0 + (uint32_t)slot * kXBytes);
+    // MXFP4 in_proj_qkvz: the quantised inputs; bf16 weights: xn itself
+    const uint64_t ad = tc::sdesc_k_sw128((unit_coded(p, it) ? sxq0 : sx0) + (uint32_t)slot * kXBytes);
     const uint64_t bd = tc::sdesc_k_sw128(sw0 + (uint32_t)s * kWBytes);
     const uint32_t d = tmem + (uint32_t)(seg & 1) * kTileM;
 #pragma unroll
@@ -384,15 +609,57 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
   }
 }
 
-template <bool HAS_RES, bool STATE_BF16, int DK>
+// On an exit that skips the projection: wait (bounded) for the TMA loads of
+// the CTA's first n units, all within the prefill (first use of each stage).
+static __device__ void land_prefill(const StepParams& p, TcShared& ts, int ub, int n) {
+  RingPos pos;
+  UnitIter it(p, ub);
+  for (int j = 0; j < n; ++j, it.next()) {
+    const bool coded = unit_coded(p, it);
+    cleanup_wait(coded ? &ts.rfull[pos.r] : &ts.full[pos.s], 0);
+    pos.advance(p, coded);
+  }
+}
+// On an aborted projection: wait (bounded) for the last TMA load issued into
+// each stage of either ring (units [0, issued)).
+static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, int issued) {
+  int last_s[kMaxStages], last_r[kMaxRStages];
+  uint32_t ph_s[kMaxStages], ph_r[kMaxRStages];
+  for (int i = 0; i < kMaxStages; ++i) last_s[i] = -1;
+  for (int i = 0; i < kMaxRStages; ++i) last_r[i] = -1;
+  RingPos pos;
+  UnitIter it(p, ub);
+  for (int j = 0; j < issued; ++j, it.next()) {
+    const bool coded = unit_coded(p, it);
+    if (coded) {
+      last_r[pos.r] = j;
+      ph_r[pos.r] = pos.rph;
+    } else {
+      last_s[pos.s] = j;
+      ph_s[pos.s] = pos.ph;
+    }
+    pos.advance(p, coded);
+  }
+  for (int i = 0; i < p.stages; ++i)
+    if (last_s[i] >= 0) cleanup_wait(&ts.full[i], ph_s[i]);
+  for (int i = 0; i < p.rstages; ++i)
+    if (last_r[i] >= 0) cleanup_wait(&ts.rfull[i], ph_r[i]);
+}
+
+// FP4: the instantiation for MXFP4 in_proj_qkvz (it alone carries the
+// decoding warps' code; p.fp4 equals FP4).
+template <bool HAS_RES, bool STATE_BF16, int DK, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemPhases sm;
   __shared__ SmemTask st;
   __shared__ TcShared ts;
   uint8_t* sW = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* sX = sW + (size_t)p.stages * kWBytes;
-  uint8_t* sWin = sX + (size_t)p.xslots * kXBytes + p.xpad;
+  uint8_t* sR = sW + (size_t)p.stages * kWBytes;                      // MXFP4 code ring
+  uint8_t* sX = sR + (size_t)p.rstages * kRBytes;                     // normed-input window
+  uint8_t* sXq = sX + (size_t)p.xslots * kXBytes;                     // its MXFP4-quantised copy
+  uint8_t* sPad = sX + (size_t)(p.fp4 ? 2 : 1) * p.xslots * kXBytes;  // read past the windows; scratch
+  uint8_t* sWin = sPad + p.xpad;
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
   const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
 
@@ -408,6 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
       tc::mbar_init(&ts.acc_full[b], 1);
       tc::mbar_init(&ts.acc_empty[b], 1);
     }
+    for (int r = 0; r < p.rstages; ++r) {
+      tc::mbar_init(&ts.rfull[r], 1);
+      tc::mbar_init(&ts.rempty[r], 1);
+    }
     tc::mbar_init(&ts.mma_done, 1);
     tc::fence_mbar_init();
   }
@@ -420,9 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // kFirstTiles go out now: the x and residual loads that start the norm
   // hand-off would otherwise queue behind a whole ring's worth of weights in
   // HBM. The rest of the ring follows once the norm partials are out.
-  const int issued = min(nunits, p.stages);
+  const int issued = prefill_units(p, ub, nunits, kMaxStages + kMaxRStages);
   const int first = min(issued, kFirstTiles);
-  if (tid == 32) start_weight_stream(p, ts, sW, ub, 0, first);
+  if (tid == 32) start_weight_stream(p, ts, sW, sR, ub, 0, first);
   const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
   griddep_wait();  // from here on the previous step's writes are visible
   griddep_launch_dependents();
@@ -434,8 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
   if (!sm.flag) {  // sticky error: every later launch returns at once
-    if (tid == 32)  // once the weight tiles in flight have landed
-      for (int n = 0; n < first; ++n) cleanup_wait(&ts.full[n], 0);
+    if (tid == 32) land_prefill(p, ts, ub, first);  // once the weight tiles in flight have landed
     return;
   }
   tl_stamp(p, TL_START);
@@ -444,23 +714,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // x and the residual (and the weights, unless already streaming), then the
   // norm partials go out. The sums of squares use the A operand's pad as
   // scratch.
-  float* sq = reinterpret_cast<float*>(sX + (size_t)p.xslots * kXBytes);
+  float* sq = reinterpret_cast<float*>(sPad);
   stage_residual_slices<HAS_RES>(p, sX, sWin, sq, [&] { store_norm_weights(p, sWin, wnorm); });
   tl_stamp(p, TL_R_STAGED);
   const int L = sm.L;
   publish_norm_partials(p, sq, L);
-  if (tid == 32) start_weight_stream(p, ts, sW, ub, first, issued);
+  if (tid == 32) start_weight_stream(p, ts, sW, sR, ub, first, issued);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
-    if (tid == 32)  // let the weight tiles in flight land before the CTA exits
-      for (int n = 0; n < issued; ++n) cleanup_wait(&ts.full[n], 0);
+    if (tid == 32) land_prefill(p, ts, ub, issued);  // let the weight tiles in flight land
     if (warp == 1) {
       tc::tc_fence_after();
       tc::tmem_dealloc(ts.tmem_base, kTmemCols);
     }
     return;
   }
-  finish_normed_slices(p, sm, sX, sWin);
+  finish_normed_slices(p, sm, sX, sXq, sWin);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -476,23 +745,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   int issued_total = issued;
   if (nunits > 0) {
     if (tid == 0)
-      issued_total = producer_loop(p, ts, sW, ub, nunits, issued, tc::policy_evict_first());
+      issued_total = producer_loop(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
     else if (tid == 32)
-      mma_loop(p, ts, sW, sX, ub, nunits, tmem);
+      mma_loop(p, ts, sW, sX, sXq, ub, nunits, tmem);
     else if (warp == 4 || warp == 8)
       drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31), L);
+    else if (FP4 && conv_index(warp) >= 0)
+      decode_loop(p, ts, sW, sR, ub, nunits, conv_index(warp) * 32 + (tid & 31));
   }
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
-  if (aborted && tid == 0) {
-    // the last tile issued into each stage must land before the CTA exits
-    for (int s = 0; s < p.stages; ++s) {
-      int last = -1;
-      for (int n = s; n < issued_total; n += p.stages) last = n;
-      if (last >= 0) cleanup_wait(&ts.full[s], (last / p.stages) & 1);
-    }
-  }
+  if (aborted && tid == 0) land_issued(p, ts, ub, issued_total);  // TMA in flight lands before exit
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -504,27 +768,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
 }
 
-const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk) {
-#define GDN_PICK(R, B, D) \
-  if (has_res == R && state_bf16 == B && dk == D) return (const void*)&gdn_step_tc_kernel<R, B, D>;
-  GDN_PICK(true, false, 128) GDN_PICK(true, true, 128) GDN_PICK(false, false, 128) GDN_PICK(false, true, 128)
-  GDN_PICK(true, false, 64) GDN_PICK(true, true, 64) GDN_PICK(false, false, 64) GDN_PICK(false, true, 64)
+const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, bool fp4) {
+#define GDN_PICK(R, B, D, F) \
+  if (has_res == R && state_bf16 == B && dk == D && fp4 == F) return (const void*)&gdn_step_tc_kernel<R, B, D, F>;
+  GDN_PICK(true, false, 128, false) GDN_PICK(true, true, 128, false) GDN_PICK(false, false, 128, false)
+  GDN_PICK(false, true, 128, false) GDN_PICK(true, false, 64, false) GDN_PICK(true, true, 64, false)
+  GDN_PICK(false, false, 64, false) GDN_PICK(false, true, 64, false)
+  // MXFP4 in_proj_qkvz: head dim 128
+  GDN_PICK(true, false, 128, true) GDN_PICK(true, true, 128, true) GDN_PICK(false, false, 128, true)
+  GDN_PICK(false, true, 128, true)
 #undef GDN_PICK
   return nullptr;
 }
 
-// Dynamic shared memory of a launch: the weight ring, the normed-input
-// window with the pad an M = 64 MMA reads past its last slice (also the norm
-// sums' scratch), the window's input-norm weights, and 1 KB of alignment.
+// Dynamic shared memory of a launch: the bf16 weight ring, the MXFP4 code
+// ring, the normed-input window (and with MXFP4 weights its quantised copy)
+// with the pad an M = 64 MMA reads past the last slice (also the norm sums'
+// scratch), the window's input-norm weights, and 1 KB of alignment.
 uint32_t tensor_core_xpad(int xslots) {
   const uint32_t sums = (uint32_t)(kMaxRows * xslots * 8 * sizeof(float));
   return sums > kXPadMin ? (sums + 127) / 128 * 128 : kXPadMin;
 }
-size_t tensor_core_smem_bytes(int stages, int xslots) {
-  return (size_t)stages * kWBytes + (size_t)xslots * kXBytes + tensor_core_xpad(xslots) +
-         (size_t)xslots * kWinBytes + 1024;
+size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, bool fp4) {
+  return (size_t)stages * kWBytes + (size_t)rstages * kRBytes + (size_t)(fp4 ? 2 : 1) * xslots * kXBytes +
+         tensor_core_xpad(xslots) + (size_t)xslots * kWinBytes + 1024;
 }
 size_t tensor_core_static_smem() { return sizeof(SmemPhases) + sizeof(SmemTask) + sizeof(TcShared); }
 int tensor_core_max_stages() { return kMaxStages; }
+int tensor_core_max_rstages() { return kMaxRStages; }
 
 }  // namespace gdn

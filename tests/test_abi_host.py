@@ -134,3 +134,16 @@ def test_stream_k_plan_invariants(lib, shape, G, engine):
     for t in range(nt):
         assert P["tile_count"][t] == len(slots[t]) >= 1
         assert sorted(slots[t]) == list(range(P["tile_count"][t]))
+
+
+@pytest.mark.parametrize("G", [148, 152])
+def test_mxfp4_plan_is_tensor_core_only(lib, G):
+    """MXFP4 in_proj_qkvz runs on the tensor-core engine (auto picks it; the
+    CUDA-core engine refuses it)."""
+    P = _native.plan(make_config(WL.DENSE_MXFP4), G)
+    assert P["engine"] == 2
+    assert P["num_tiles"] == WL.DENSE_MXFP4.n_qkvz // 256 + 1
+    with pytest.raises(_native.GdnError):
+        _native.plan(make_config(WL.DENSE_MXFP4, engine="cuda_core"), G)
+    with pytest.raises(_native.GdnError):  # the scale loads need H % 512 == 0
+        _native.plan(make_config(WL.DENSE_MXFP4.with_(hidden=5120 + 64)), G)

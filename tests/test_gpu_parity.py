@@ -122,3 +122,21 @@ def test_cooperative_launch_option(rows):
     core, res_out = case.run_gpu(layer)
     assert layer.check()[0] == 0
     compare(case, case.run_oracle(), core, res_out)
+
+
+# The dense layer with MXFP4 in_proj_qkvz (activations quantised per block of
+# 32, W4A4, in_proj_ba bf16 on the unquantised input).
+@pytest.mark.parametrize("rows", [1, 6, 16])
+def test_dense_mxfp4_layer(rows):
+    _run(WL.DENSE_MXFP4, rows, 8000 + rows, "auto")
+
+
+def test_dense_mxfp4_first_layer_with_pad_rows():
+    _run(WL.DENSE_MXFP4, 9, 8100, "tcgen05", first_layer=True, pad_rows=WL.default_pad_rows(9))
+
+
+def test_mxfp4_needs_the_tensor_core_engine():
+    from gated_deltanet_layer_gb300 import GdnError, _native
+    with pytest.raises(GdnError) as e:
+        GdnDecode(WL.DENSE_MXFP4, engine="cuda_core")
+    assert e.value.code == _native.GDN_ERR_UNSUPPORTED
