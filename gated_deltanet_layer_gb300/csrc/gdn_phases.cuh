@@ -149,7 +149,7 @@ __device__ __forceinline__ void group_sync() {
   else if (NT == 32)
     __syncwarp();
   else
-    asm volatile("barrier.sync 1, %0;" ::"n"(NT) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");  // callers reach it with converged warps
 }
 
 // Shared memory of one recurrence task.

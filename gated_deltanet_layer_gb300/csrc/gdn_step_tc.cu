@@ -137,8 +137,9 @@ __device__ __forceinline__ const CUtensorMap* weight_map(const StepParams& p, in
 
 // A unit whose weights are MXFP4 codes (decoded to bf16 in shared memory
 // before the MMA); the others are bf16 tiles the MMA reads as loaded.
+template <bool FP4>
 __device__ __forceinline__ bool unit_coded(const StepParams& p, const UnitIter& it) {
-  return p.fp4 && it.t < p.tiles_qkvz;
+  return FP4 && it.t < p.tiles_qkvz;
 }
 
 // Ring positions along a CTA's units: every unit takes the next bf16 stage
@@ -154,11 +155,12 @@ struct RingPos {
 
 // Unit n's weights: MXFP4 codes into code stage pos.r, else a bf16 tile into
 // stage pos.s (the caller has made sure the stage is free).
+template <bool FP4>
 __device__ __forceinline__ void issue_unit(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
                                            const UnitIter& it, int n, const RingPos& pos, uint64_t pol) {
   int row0;
   const CUtensorMap* m = weight_map(p, it.t, row0);
-  if (unit_coded(p, it)) {
+  if (unit_coded<FP4>(p, it)) {
     tc::mbar_arrive_expect_tx(&ts.rfull[pos.r], kRBytes);
     tc::tma_load_2d(sR + (size_t)pos.r * kRBytes, m, it.ks * (kKStep / 2), row0, &ts.rfull[pos.r], pol);
   } else {
@@ -169,20 +171,22 @@ __device__ __forceinline__ void issue_unit(const StepParams& p, TcShared& ts, ui
 }
 
 // Ring positions after the CTA's first n units.
+template <bool FP4>
 __device__ __forceinline__ RingPos ring_pos_at(const StepParams& p, int ub, int n) {
   RingPos pos;
   UnitIter it(p, ub);
-  for (int j = 0; j < n; ++j, it.next()) pos.advance(p, unit_coded(p, it));
+  for (int j = 0; j < n; ++j, it.next()) pos.advance(p, unit_coded<FP4>(p, it));
   return pos;
 }
 
 // The CTA's leading units that fit the rings before any stage is reused (at
 // most `cap`): the ones issued without waiting.
+template <bool FP4>
 __device__ __forceinline__ int prefill_units(const StepParams& p, int ub, int nunits, int cap) {
   UnitIter it(p, ub);
   int coded = 0, n = 0;
   for (; n < min(nunits, cap); ++n, it.next()) {
-    if (unit_coded(p, it)) {
+    if (unit_coded<FP4>(p, it)) {
       if (coded == p.rstages) break;
       ++coded;
     } else if (n >= p.stages) {
@@ -194,15 +198,16 @@ __device__ __forceinline__ int prefill_units(const StepParams& p, int ub, int nu
 
 // Units [from, to) of the CTA's weight stream, all within the prefill (one
 // thread, no waits).
+template <bool FP4>
 static __device__ __forceinline__ void start_weight_stream(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                            uint8_t* sR, int ub, int from, int to) {
   if (from >= to) return;
   const uint64_t pol0 = tc::policy_evict_first();
-  RingPos pos = ring_pos_at(p, ub, from);
+  RingPos pos = ring_pos_at<FP4>(p, ub, from);
   UnitIter it(p, ub + from);
   for (int n = from; n < to; ++n, it.next()) {
-    issue_unit(p, ts, sW, sR, it, n, pos, pol0);
-    pos.advance(p, unit_coded(p, it));
+    issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol0);
+    pos.advance(p, unit_coded<FP4>(p, it));
   }
   if (from == 0) tl_stamp_here(p, TL_ISSUED);
 }
@@ -375,6 +380,7 @@ static __device__ __forceinline__ uint4 quantize8_mxfp4(uint4 xv) {
 
 // xn = bf16(r * rstd * (1 + w)) in place; with MXFP4 weights also its
 // quantised copy in the second window sXq (same layout).
+template <bool FP4>
 static __device__ __forceinline__ void finish_normed_slices(const StepParams& p, const SmemPhases& sm,
                                                             uint8_t* sX, uint8_t* sXq, const uint8_t* sWin) {
   const int cta = blockIdx.x, W = p.rows;
@@ -385,7 +391,7 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
     uint4* d = reinterpret_cast<uint4*>(sX + off);
     const uint4 xv = normed8(*d, reinterpret_cast<const uint4*>(sWin + (size_t)j * kWinBytes)[c], sm.rstd[w]);
     *d = xv;
-    if (p.fp4) *reinterpret_cast<uint4*>(sXq + off) = quantize8_mxfp4(xv);
+    if (FP4) *reinterpret_cast<uint4*>(sXq + off) = quantize8_mxfp4(xv);
   }
 }
 
@@ -395,18 +401,19 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
 // measured: the tensor form does not bring tiles in early, and per-row
 // prefetches delay the latency-bound norm hand-off more than they shorten
 // the projection.)
+template <bool FP4>
 static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
                                                    int ub, int nunits, int issued, uint64_t pol) {
   UnitIter it(p, ub + issued);
-  RingPos pos = ring_pos_at(p, ub, issued);
+  RingPos pos = ring_pos_at<FP4>(p, ub, issued);
   for (int n = issued; n < nunits; ++n) {
-    const bool coded = unit_coded(p, it);
+    const bool coded = unit_coded<FP4>(p, it);
     if (coded) {
       if (!pipe_wait(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
     } else if (!pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
       return n;
     }
-    issue_unit(p, ts, sW, sR, it, n, pos, pol);
+    issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol);
     pos.advance(p, coded);
     it.next();
   }
@@ -456,7 +463,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
   {
     UnitIter f(p, ub);
     for (int n = 0; n < nunits; ++n, f.next())
-      if (unit_coded(p, f)) {
+      if (unit_coded<true>(p, f)) {
         nxt = scale_block(p, f, ci);
         nxt_t = f.t;
         nxt_k = f.ks >> 3;
@@ -464,7 +471,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
       }
   }
   for (int n = 0; n < nunits; ++n) {
-    const bool coded = unit_coded(p, it);
+    const bool coded = unit_coded<true>(p, it);
     if (coded) {
       if (it.t != blk_t || (it.ks >> 3) != blk_k) {
         // this unit starts a new scale block: take the prefetched one, prefetch the next
@@ -474,7 +481,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
         UnitIter f = it;
         for (int j = n + 1; j < nunits; ++j) {
           f.next();
-          if (unit_coded(p, f) && (f.t != blk_t || (f.ks >> 3) != blk_k)) {
+          if (unit_coded<true>(p, f) && (f.t != blk_t || (f.ks >> 3) != blk_k)) {
             nxt = scale_block(p, f, ci);
             nxt_t = f.t;
             nxt_k = f.ks >> 3;
@@ -521,6 +528,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
 // segment's accumulator; a segment (the units of one group) starts by
 // overwriting. Commits release the stage and, at a segment's end, hand the
 // accumulator to the drain.
+template <bool FP4>
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                 uint8_t* sX, uint8_t* sXq, int ub, int nunits, uint32_t tmem) {
   // Stage and phase advance incrementally: a division per unit by the
@@ -548,7 +556,7 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
     if (slot < 0) slot += KS;
     if (n == 0) tl_stamp_here(p, TL_MMA_FIRST);
     // MXFP4 in_proj_qkvz: the quantised inputs; bf16 weights: xn itself
-    const uint64_t ad = tc::sdesc_k_sw128((unit_coded(p, it) ? sxq0 : sx0) + (uint32_t)slot * kXBytes);
+    const uint64_t ad = tc::sdesc_k_sw128((unit_coded<FP4>(p, it) ? sxq0 : sx0) + (uint32_t)slot * kXBytes);
     const uint64_t bd = tc::sdesc_k_sw128(sw0 + (uint32_t)s * kWBytes);
     const uint32_t d = tmem + (uint32_t)(seg & 1) * kTileM;
 #pragma unroll
@@ -611,17 +619,19 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
 
 // On an exit that skips the projection: wait (bounded) for the TMA loads of
 // the CTA's first n units, all within the prefill (first use of each stage).
+template <bool FP4>
 static __device__ void land_prefill(const StepParams& p, TcShared& ts, int ub, int n) {
   RingPos pos;
   UnitIter it(p, ub);
   for (int j = 0; j < n; ++j, it.next()) {
-    const bool coded = unit_coded(p, it);
+    const bool coded = unit_coded<FP4>(p, it);
     cleanup_wait(coded ? &ts.rfull[pos.r] : &ts.full[pos.s], 0);
     pos.advance(p, coded);
   }
 }
 // On an aborted projection: wait (bounded) for the last TMA load issued into
 // each stage of either ring (units [0, issued)).
+template <bool FP4>
 static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, int issued) {
   int last_s[kMaxStages], last_r[kMaxRStages];
   uint32_t ph_s[kMaxStages], ph_r[kMaxRStages];
@@ -630,7 +640,7 @@ static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, in
   RingPos pos;
   UnitIter it(p, ub);
   for (int j = 0; j < issued; ++j, it.next()) {
-    const bool coded = unit_coded(p, it);
+    const bool coded = unit_coded<FP4>(p, it);
     if (coded) {
       last_r[pos.r] = j;
       ph_r[pos.r] = pos.rph;
@@ -691,9 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // kFirstTiles go out now: the x and residual loads that start the norm
   // hand-off would otherwise queue behind a whole ring's worth of weights in
   // HBM. The rest of the ring follows once the norm partials are out.
-  const int issued = prefill_units(p, ub, nunits, kMaxStages + kMaxRStages);
+  const int issued = prefill_units<FP4>(p, ub, nunits, kMaxStages + kMaxRStages);
   const int first = min(issued, kFirstTiles);
-  if (tid == 32) start_weight_stream(p, ts, sW, sR, ub, 0, first);
+  if (tid == 32) start_weight_stream<FP4>(p, ts, sW, sR, ub, 0, first);
   const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
   griddep_wait();  // from here on the previous step's writes are visible
   griddep_launch_dependents();
@@ -705,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
   if (!sm.flag) {  // sticky error: every later launch returns at once
-    if (tid == 32) land_prefill(p, ts, ub, first);  // once the weight tiles in flight have landed
+    if (tid == 32) land_prefill<FP4>(p, ts, ub, first);  // once the weight tiles in flight have landed
     return;
   }
   tl_stamp(p, TL_START);
@@ -719,17 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tl_stamp(p, TL_R_STAGED);
   const int L = sm.L;
   publish_norm_partials(p, sq, L);
-  if (tid == 32) start_weight_stream(p, ts, sW, sR, ub, first, issued);
+  if (tid == 32) start_weight_stream<FP4>(p, ts, sW, sR, ub, first, issued);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
-    if (tid == 32) land_prefill(p, ts, ub, issued);  // let the weight tiles in flight land
+    if (tid == 32) land_prefill<FP4>(p, ts, ub, issued);  // let the weight tiles in flight land
     if (warp == 1) {
       tc::tc_fence_after();
       tc::tmem_dealloc(ts.tmem_base, kTmemCols);
     }
     return;
   }
-  finish_normed_slices(p, sm, sX, sXq, sWin);
+  finish_normed_slices<FP4>(p, sm, sX, sXq, sWin);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -745,9 +755,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   int issued_total = issued;
   if (nunits > 0) {
     if (tid == 0)
-      issued_total = producer_loop(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
+      issued_total = producer_loop<FP4>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
     else if (tid == 32)
-      mma_loop(p, ts, sW, sX, sXq, ub, nunits, tmem);
+      mma_loop<FP4>(p, ts, sW, sX, sXq, ub, nunits, tmem);
     else if (warp == 4 || warp == 8)
       drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31), L);
     else if (FP4 && conv_index(warp) >= 0)
@@ -756,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
-  if (aborted && tid == 0) land_issued(p, ts, ub, issued_total);  // TMA in flight lands before exit
+  if (aborted && tid == 0) land_issued<FP4>(p, ts, ub, issued_total);  // TMA in flight lands before exit
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
