@@ -20,10 +20,12 @@
 //   thread 0 (warp 0)   TMA producer: refills each stage the MMAs release
 //   warp 1              allocates TMEM; its thread 0 issues tcgen05.mma into
 //                       one of two 64 x 256 f32 accumulators (512 columns)
-//   warps 4 and 8       drain an accumulator with tcgen05.ld (lane w holds
-//                       row w of the step; each warp half of the columns),
-//                       write the CTA's partial of the tile and publish it;
+//   warps 4, 8, 12      drain an accumulator with tcgen05.ld (lane w holds
+//                       row w of the step; the warps split the columns) and
+//                       write the CTA's partial of the tile as tagged words;
 //                       the recurrence tasks reduce the partials they need
+//   warps 2, 3, 5-7,    (MXFP4 in_proj_qkvz) decode each code tile into a
+//   9-11                bf16 tile for the MMA
 // The A operand (xn of the CTA's k-steps, 16 rows, rows past the step's row
 // count zero) is built per launch in shared memory: r = x + residual is
 // staged while the norm hand-off is in flight and normalised in place once
@@ -575,14 +577,15 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   tl_stamp_here(p, TL_MMA_LAST);
 }
 
-// Drain (warps 4 and 8, both in TMEM sub-partition 0, so lane w reads row w
-// of the step): per segment, each warp reads half of the 128 x 256
-// accumulator's columns (weight rows), the accumulator is released, the CTA's
-// partial of the tile is written and published.
-constexpr int kDrainThreads = 64;
+// Drain (warps 4, 8 and 12, all in TMEM sub-partition 0, so lane w reads row
+// w of the step): per segment, the warps split the accumulator's 8 chunks of
+// 32 columns (weight rows) and write the CTA's partial of the tile as tagged
+// words; then the accumulator is released.
+constexpr int kDrainWarps = 3;
+constexpr int kDrainThreads = 32 * kDrainWarps;
 static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared& ts, int ub, int nunits,
                                                   uint32_t tmem, int gtid, int L) {
-  const int W = p.rows, lane = gtid & 31, half = gtid >> 5;
+  const int W = p.rows, lane = gtid & 31, dw = gtid >> 5;
   UnitIter it(p, ub);
   int seg = 0;
   for (int n = 0; n < nunits; ++seg) {
@@ -602,7 +605,7 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
                               ((size_t)t * p.max_contrib + p.plan->seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
                               (size_t)lane * kTileM;
 #pragma unroll 1
-    for (int c = half * (kTileM / 64); c < (half + 1) * (kTileM / 64); ++c) {
+    for (int c = dw; c < kTileM / 32; c += kDrainWarps) {
       float v[32];
       tc::tmem_ld32(tmem + (uint32_t)b * kTileM + c * 32, v);
       if (lane < W) {  // the partial as tagged words: readers poll them directly
@@ -758,8 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
       issued_total = producer_loop<FP4>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
     else if (tid == 32)
       mma_loop<FP4>(p, ts, sW, sX, sXq, ub, nunits, tmem);
-    else if (warp == 4 || warp == 8)
-      drain_loop(p, ts, ub, nunits, tmem, (warp == 8 ? 32 : 0) + (tid & 31), L);
+    else if (warp == 4 || warp == 8 || warp == 12)
+      drain_loop(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
     else if (FP4 && conv_index(warp) >= 0)
       decode_loop(p, ts, sW, sR, ub, nunits, conv_index(warp) * 32 + (tid & 31));
   }
