@@ -101,6 +101,39 @@ def run_cpu_baseline(args, steps=None, seconds=None):
     return d, cores
 
 
+# ----------------------------------------------------------------- traffic
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+
+
+def kernel_source_hash() -> str:
+    """sha256 (16 hex digits) of the kernel sources and the C header."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "gated_deltanet_layer_gb300", "csrc", "*")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, rows: int):
+    """DRAM bytes (read + write) per launch of the step kernel from the
+    committed ncu record in profiles/, if it was taken on these kernel sources
+    with this workload and row count; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha") != kernel_source_hash() or rec.get("workload") != workload or rec.get("rows") != rows:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 # ----------------------------------------------------------------- clocks
 
 class Clocks:
@@ -176,11 +209,19 @@ def native(args):
         return (torch.randn(*s, generator=g, device="cuda") * std).to(torch.bfloat16)
 
     H, Hv = shape.hidden, shape.num_v_heads
+    def qkvz():
+        if shape.qkvz_format == "mxfp4":  # e2m1 codes uniform over the 16 codes, block exponents U{-8..-4}
+            return {"qkvz": torch.randint(0, 256, (shape.n_qkvz, H // 2), generator=g, device="cuda",
+                                          dtype=torch.uint8),
+                    "qkvz_scales": (127 + torch.randint(-8, -3, (shape.n_qkvz, H // 32), generator=g,
+                                                        device="cuda")).to(torch.uint8)}
+        return {"qkvz": bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None}
+
     copies = []
     for _ in range(ncopy):
         copies.append({
             "input_norm_w": bf16(H, std=0.1),
-            "qkvz": bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None,
+            **qkvz(),
             "ba": bf16(shape.n_ba, H, std=0.02),
             "conv_w": bf16(shape.conv_channels, shape.conv_kernel, std=0.02),
             "A_log": -2.0 * torch.rand(Hv, generator=g, device="cuda"),
@@ -310,10 +351,12 @@ def native(args):
     result = {
         "metric": METRIC, "value": round(us, 3), "unit": "µs/launch", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 math, " + shape.ssm_dtype + " state",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("mxfp4" if shape.qkvz_format == "mxfp4" else "bf16") + " weights, f32 math, " + shape.ssm_dtype + " state",
         "data": "synthetic (seeded random weights and states of the layer's shapes)",
         "config": {"workload": f"{shape.name}: H={H} Hk={shape.num_k_heads} Hv={Hv} dk=dv={shape.head_k_dim} "
-                               f"slots={shape.num_slots} {shape.ssm_dtype} state, bf16 in_proj",
+                               f"slots={shape.num_slots} {shape.ssm_dtype} state, "
+                               f"{'MXFP4' if shape.qkvz_format == 'mxfp4' else 'bf16'} in_proj_qkvz",
                    "rows": args.rows, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: weights rotated over {ncopy} copies "
                          f"({ncopy * wbytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2), fresh slots per launch",
@@ -324,7 +367,8 @@ def native(args):
         "widths": table,
         "roofline": {"bound": "hbm", "achieved": round(bytes_launch / us / 1e3, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(bytes_launch / us / 1e3 / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": bytes_launch},
+                     "traffic": measured_traffic(args.workload, args.rows), "peak_kind": peak_kind,
+                     "bytes_per_launch": bytes_launch},
         "e2e": {"value": round(e2e_us, 3), "unit": "µs/launch", "h2d_bytes_per_step": Bi,
                 "d2h_bytes_per_step": Bo, "how": "eager gdn_decode_step via the Python binding with "
                                                  "pinned-host copies in and out each step"},
