@@ -17,9 +17,15 @@
 //                       step is still running (programmatic dependent
 //                       launch), else right after issuing its x and residual
 //                       loads, so HBM streams weights while the hand-off runs
-//   thread 0 (warp 0)   TMA producer: refills each stage the MMAs release
-//   warp 1              allocates TMEM; its thread 0 issues tcgen05.mma into
-//                       one of two 64 x 256 f32 accumulators (512 columns)
+//   warp 0              TMA producer: refills each stage the MMAs release
+//                       (lane 0 issues)
+//   warp 1              allocates TMEM; issues tcgen05.mma (lane 0) into one
+//                       of two 64 x 256 f32 accumulators (512 columns)
+// Whole warps run these loops, waiting together, with lane 0 issuing (a
+// little faster end to end than a lone thread). In this kernel a 4-MMA unit
+// takes ~930 SM cycles of the issuing warp against ~510 for the same MMAs
+// issued back to back alone on an SM; the difference is issue overhead
+// between units, not tensor-core time.
 //   warps 4, 8, 12      drain an accumulator with tcgen05.ld (lane w holds
 //                       row w of the step; the warps split the columns) and
 //                       write the CTA's partial of the tile as tagged words;
@@ -46,14 +52,14 @@ constexpr uint32_t kWBytes = kTileM * kKStep * 2;       // 32 KB weight tile (B 
 constexpr uint32_t kXBytes = kMaxRows * kKStep * 2;     // 2 KB normed-input slice (A rows 0..15)
 constexpr uint32_t kXPadMin = (64 - kMaxRows) * 128;    // 6 KB an M = 64 MMA reads past the last slice
 constexpr uint32_t kWinBytes = kKStep * 2;              // input-norm weights of one k-step
-constexpr uint32_t kTmemCols = 2 * kTileM;              // two 128 x 256 f32 accumulators
+constexpr uint32_t kTmemCols = 2 * kTileM;              // two 256-column f32 accumulators
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(64, kTileM);
 static_assert(kMaxBSlots <= 32, "one owner bit per window slot");
 constexpr uint32_t kRBytes = kTileM * kKStep / 2;      // 8 KB MXFP4 code tile (256 rows x 32 bytes)
 constexpr int kMaxRStages = 4;                          // code tiles in flight per CTA (MXFP4)
 // Warps that decode MXFP4 code tiles into bf16 tiles: thread i of them owns
 // row i of the 256-row tile. (Warp 0 holds the TMA producer, warp 1 the MMA
-// issuer, warps 4 and 8 the drain.)
+// issuer, warps 4, 8 and 12 the drain.)
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
 __device__ __forceinline__ int conv_index(int warp) {
@@ -119,6 +125,13 @@ static __device__ __forceinline__ bool pipe_wait(const StepParams& p, TcShared& 
       return false;
     }
   }
+}
+
+// The same for a whole warp: every lane waits, and the warp goes on only if
+// every lane saw the phase (so its lanes never part ways).
+static __device__ __forceinline__ bool pipe_wait_warp(const StepParams& p, TcShared& ts, uint64_t* bar,
+                                                      uint32_t parity) {
+  return __all_sync(0xffffffffu, pipe_wait(p, ts, bar, parity));
 }
 
 // Wait (bounded, ignoring the abort flag) on the abort path.
@@ -397,25 +410,27 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
   }
 }
 
-// TMA producer: units `issued`.. into the rings, each into a stage that has
-// been released (a bf16 stage by the MMAs, a code stage by the decode).
-// Returns the number of units issued. (An L2 prefetch ahead of the ring was
+// TMA producer (one whole warp; lane 0 issues): units `issued`.. into the
+// rings, each into a stage that has been released (a bf16 stage by the MMAs,
+// a code stage by the decode). Returns the number of units issued. (An L2 prefetch ahead of the ring was
 // measured: the tensor form does not bring tiles in early, and per-row
 // prefetches delay the latency-bound norm hand-off more than they shorten
 // the projection.)
 template <bool FP4>
 static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
                                                    int ub, int nunits, int issued, uint64_t pol) {
+  const bool leader = (threadIdx.x & 31) == 0;
   UnitIter it(p, ub + issued);
   RingPos pos = ring_pos_at<FP4>(p, ub, issued);
   for (int n = issued; n < nunits; ++n) {
     const bool coded = unit_coded<FP4>(p, it);
     if (coded) {
-      if (!pipe_wait(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
-    } else if (!pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
+      if (!pipe_wait_warp(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
+    } else if (!pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
       return n;
     }
-    issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol);
+    if (leader) issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol);
+    __syncwarp();
     pos.advance(p, coded);
     it.next();
   }
@@ -526,9 +541,9 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
   }
 }
 
-// MMA issuer: per unit, 4 MMAs of K = 16 over the stage's 64 columns into the
-// segment's accumulator; a segment (the units of one group) starts by
-// overwriting. Commits release the stage and, at a segment's end, hand the
+// MMA issuer (one whole warp; lane 0 issues): per unit, 4 MMAs of K = 16 over
+// the stage's 64 columns into the segment's accumulator; a segment (the units
+// of one group) starts by overwriting. Commits release the stage and, at a segment's end, hand the
 // accumulator to the drain.
 template <bool FP4>
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
@@ -542,39 +557,53 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   int s = 0;
   uint32_t ph = 0;
   const uint32_t sw0 = tc::smem_u32(sW), sx0 = tc::smem_u32(sX), sxq0 = tc::smem_u32(sXq);
+  const bool leader = (threadIdx.x & 31) == 0;
+  bool landed = false;  // unit n's tile seen complete while unit n - 1 was issued
   for (int n = 0; n < nunits; ++n) {
     const bool first = !seg_open;
     if (first) {
       ++seg;
       seg_open = true;
-      if (!pipe_wait(p, ts, &ts.acc_empty[seg & 1], ((seg >> 1) & 1) ^ 1)) break;
+      if (!pipe_wait_warp(p, ts, &ts.acc_empty[seg & 1], ((seg >> 1) & 1) ^ 1)) break;
       tc::tc_fence_after();  // these MMAs come after the drain's tcgen05.ld of this accumulator
     }
     // The phase makes the stage's TMA bytes visible to the MMA (both async
     // proxy): no tcgen05 fence per unit.
-    if (!tc::mbar_try_wait(&ts.full[s], ph))
-      if (!pipe_wait(p, ts, &ts.full[s], ph)) break;
+    if (!landed &&
+        !__all_sync(0xffffffffu, tc::mbar_try_wait(&ts.full[s], ph) || pipe_wait(p, ts, &ts.full[s], ph)))
+      break;
+    // The next unit's stage, tested now: an mbarrier test takes ~200 cycles,
+    // which then pass under this unit's MMA issue instead of idling the
+    // tensor core between units.
+    int s1 = s + 1;
+    uint32_t ph1 = ph;
+    if (s1 == S) { s1 = 0; ph1 ^= 1; }
+    const bool landed1 = n + 1 < nunits && tc::mbar_test(&ts.full[s1], ph1);
     int slot = it.ks - ks0;
     if (slot < 0) slot += KS;
-    if (n == 0) tl_stamp_here(p, TL_MMA_FIRST);
+    if (n == 0 && leader) tl_stamp_here(p, TL_MMA_FIRST);
     // MXFP4 in_proj_qkvz: the quantised inputs; bf16 weights: xn itself
     const uint64_t ad = tc::sdesc_k_sw128((unit_coded<FP4>(p, it) ? sxq0 : sx0) + (uint32_t)slot * kXBytes);
     const uint64_t bd = tc::sdesc_k_sw128(sw0 + (uint32_t)s * kWBytes);
     const uint32_t d = tmem + (uint32_t)(seg & 1) * kTileM;
+    const bool seg_end = n + 1 == nunits || it.group_end();
+    if (leader) {
 #pragma unroll
-    for (int k = 0; k < kKStep / 16; ++k)
-      tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdesc, (first && k == 0) ? 0u : 1u);
-    tc::mma_commit(&ts.empty[s]);
-    if (n + 1 == nunits || it.group_end()) {
-      tc::mma_commit(&ts.acc_full[seg & 1]);
-      seg_open = false;
+      for (int k = 0; k < kKStep / 16; ++k)
+        tc::mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdesc, (first && k == 0) ? 0u : 1u);
+      tc::mma_commit(&ts.empty[s]);
+      if (seg_end) tc::mma_commit(&ts.acc_full[seg & 1]);
     }
+    landed = __all_sync(0xffffffffu, landed1);
+    if (seg_end) seg_open = false;
     it.next();
-    if (++s == S) { s = 0; ph ^= 1; }
+    s = s1;
+    ph = ph1;
   }
-  tc::mma_commit(&ts.mma_done);
+  if (leader) tc::mma_commit(&ts.mma_done);
+  __syncwarp();
   cleanup_wait(&ts.mma_done, 0);
-  tl_stamp_here(p, TL_MMA_LAST);
+  if (leader) tl_stamp_here(p, TL_MMA_LAST);
 }
 
 // Drain (warps 4, 8 and 12, all in TMEM sub-partition 0, so lane w reads row
@@ -757,9 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   if (rt0 < rt1) load_state<DK, STATE_BF16>(p, rt0, first_state);
   int issued_total = issued;
   if (nunits > 0) {
-    if (tid == 0)
+    if (warp == 0)
       issued_total = producer_loop<FP4>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
-    else if (tid == 32)
+    else if (warp == 1)
       mma_loop<FP4>(p, ts, sW, sX, sXq, ub, nunits, tmem);
     else if (warp == 4 || warp == 8 || warp == 12)
       drain_loop(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
