@@ -184,15 +184,20 @@ struct SmemTask {
 // recurrence, state stored in f32 or bf16 in place; pad rows write a zero
 // core row and no state).
 // ---------------------------------------------------------------------------
-// A thread's share of one (row, value head) state tile: NR rows of 4
-// elements (lanes sub = 0..LPR-1 of a row hold 4 consecutive elements each).
+// A thread's share of one (row, value head) state tile: NR rows, CH chunks
+// of 4 elements of each. Eight lanes share a row; lane sub holds chunks
+// sub, sub + 8, sub + 16, ... so that the eight lanes of a row read 128
+// contiguous bytes per chunk, and a row's dot products reduce in 3 shuffle
+// rounds (a warp holds 4 rows at a time).
 template <int DK>
 struct StateRegs {
-  static constexpr int LPR = DK / 4;              // lanes per state row, 4 elements each
+  static constexpr int LPR = 8;                   // lanes per state row
+  static constexpr int CH = DK / (4 * LPR);       // chunks of 4 elements per lane and row
   static constexpr int RPW = 32 / LPR;            // rows per warp per step
   static constexpr int NR = DK / (kWarps * RPW);  // rows per lane (dv == dk)
-  uint2 b[NR];   // bf16 state
-  float4 f[NR];  // f32 state
+  static_assert(NR >= 1 && CH >= 1, "state layout");
+  uint2 b[NR][CH];   // bf16 state
+  float4 f[NR][CH];  // f32 state
 };
 
 // The CTA's recurrence tasks: (row w, value head h) = task / Hv, task % Hv
@@ -207,7 +212,8 @@ __device__ __forceinline__ void task_range(const StepParams& p, int& t0, int& t1
 // a pad row).
 template <int DK, bool STATE_BF16>
 __device__ __forceinline__ void load_state(const StepParams& p, int task, StateRegs<DK>& r) {
-  constexpr int NR = StateRegs<DK>::NR, LPR = StateRegs<DK>::LPR, RPW = StateRegs<DK>::RPW;
+  constexpr int NR = StateRegs<DK>::NR, CH = StateRegs<DK>::CH, LPR = StateRegs<DK>::LPR;
+  constexpr int RPW = StateRegs<DK>::RPW;
   const int w = task / p.Hv, h = task - w * p.Hv;
   const int slot = p.idx[w];
   if (!row_is_live(p, slot)) return;
@@ -216,11 +222,14 @@ __device__ __forceinline__ void load_state(const StepParams& p, int task, StateR
 #pragma unroll
   for (int j = 0; j < NR; ++j) {
     const int v = (j * kWarps + warp) * RPW + lane / LPR;
-    const size_t off = sbase + (size_t)v * DK + (lane % LPR) * 4;
-    if (STATE_BF16)
-      r.b[j] = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.ssm_state) + off);
-    else
-      r.f[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const size_t off = sbase + (size_t)v * DK + (lane % LPR + LPR * c) * 4;
+      if (STATE_BF16)
+        r.b[j][c] = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.ssm_state) + off);
+      else
+        r.f[j][c] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.ssm_state) + off);
+    }
   }
 }
 
@@ -234,7 +243,8 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
   constexpr int LPR = StateRegs<DK>::LPR;
   constexpr int RPW = StateRegs<DK>::RPW;
   constexpr int NR = StateRegs<DK>::NR;
-  static_assert(NR >= 1 && 4 * DK <= kThreads, "task layout");
+  constexpr int CH = StateRegs<DK>::CH;
+  static_assert(4 * DK <= kThreads, "task layout");
   const int cta = blockIdx.x, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int sub = lane % LPR, rw = lane / LPR;
@@ -373,36 +383,44 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     sk = warp_sum(sk);
     const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
     const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
-    const float4 kq = *reinterpret_cast<const float4*>(&st.k[sub * 4]);
-    const float4 qq = *reinterpret_cast<const float4*>(&st.q[sub * 4]);
-    const float4 k4 = make_float4(kq.x * inv_k, kq.y * inv_k, kq.z * inv_k, kq.w * inv_k);
-    const float4 q4 = make_float4(qq.x * inv_q, qq.y * inv_q, qq.z * inv_q, qq.w * inv_q);
+    float4 k4[CH], q4[CH];  // this lane's chunks of k^ and q^
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const float4 kq = *reinterpret_cast<const float4*>(&st.k[(sub + LPR * c) * 4]);
+      const float4 qq = *reinterpret_cast<const float4*>(&st.q[(sub + LPR * c) * 4]);
+      k4[c] = make_float4(kq.x * inv_k, kq.y * inv_k, kq.z * inv_k, kq.w * inv_k);
+      q4[c] = make_float4(qq.x * inv_q, qq.y * inv_q, qq.z * inv_q, qq.w * inv_q);
+    }
     const float sp_in = st.ba[1] + dt_bias_h;
     const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
     const float g = -expf(A_log_h) * sp;
     const float eg = expf(g);
     const float beta = 1.0f / (1.0f + expf(-st.ba[0]));
 
-    float s[NR][4];
+    float4 s[NR][CH];
 #pragma unroll
-    for (int j = 0; j < NR; ++j) {
-      if (STATE_BF16) {
-        s[j][0] = bf16_lo(raw.b[j].x); s[j][1] = bf16_hi(raw.b[j].x);
-        s[j][2] = bf16_lo(raw.b[j].y); s[j][3] = bf16_hi(raw.b[j].y);
-      } else {
-        s[j][0] = raw.f[j].x; s[j][1] = raw.f[j].y; s[j][2] = raw.f[j].z; s[j][3] = raw.f[j].w;
+    for (int j = 0; j < NR; ++j)
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        if (STATE_BF16)
+          s[j][c] = make_float4(bf16_lo(raw.b[j][c].x), bf16_hi(raw.b[j][c].x), bf16_lo(raw.b[j][c].y),
+                                bf16_hi(raw.b[j][c].y));
+        else
+          s[j][c] = raw.f[j][c];
       }
-    }
     // S k over all rows of this lane at once (independent butterflies)
     float a[NR];
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
+      a[j] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) s[j][c] *= eg;
-      a[j] = s[j][0] * k4.x;
-      a[j] = fmaf(s[j][1], k4.y, a[j]);
-      a[j] = fmaf(s[j][2], k4.z, a[j]);
-      a[j] = fmaf(s[j][3], k4.w, a[j]);
+      for (int c = 0; c < CH; ++c) {
+        s[j][c].x *= eg; s[j][c].y *= eg; s[j][c].z *= eg; s[j][c].w *= eg;
+        a[j] = fmaf(s[j][c].x, k4[c].x, a[j]);
+        a[j] = fmaf(s[j][c].y, k4[c].y, a[j]);
+        a[j] = fmaf(s[j][c].z, k4[c].z, a[j]);
+        a[j] = fmaf(s[j][c].w, k4[c].w, a[j]);
+      }
     }
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1)
@@ -413,19 +431,22 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     for (int j = 0; j < NR; ++j) {
       const int v = (j * kWarps + warp) * RPW + rw;
       const float u = beta * (st.v[v] - a[j]);
-      s[j][0] = fmaf(k4.x, u, s[j][0]); s[j][1] = fmaf(k4.y, u, s[j][1]);
-      s[j][2] = fmaf(k4.z, u, s[j][2]); s[j][3] = fmaf(k4.w, u, s[j][3]);
-      ov[j] = s[j][0] * q4.x;
-      ov[j] = fmaf(s[j][1], q4.y, ov[j]);
-      ov[j] = fmaf(s[j][2], q4.z, ov[j]);
-      ov[j] = fmaf(s[j][3], q4.w, ov[j]);
-      const size_t off = sbase + (size_t)v * DK + sub * 4;
-      if (STATE_BF16) {
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ssm_state) + off) =
-            make_uint2(pack_bf16x2(s[j][0], s[j][1]), pack_bf16x2(s[j][2], s[j][3]));
-      } else {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ssm_state) + off) =
-            make_float4(s[j][0], s[j][1], s[j][2], s[j][3]);
+      ov[j] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        s[j][c].x = fmaf(k4[c].x, u, s[j][c].x); s[j][c].y = fmaf(k4[c].y, u, s[j][c].y);
+        s[j][c].z = fmaf(k4[c].z, u, s[j][c].z); s[j][c].w = fmaf(k4[c].w, u, s[j][c].w);
+        ov[j] = fmaf(s[j][c].x, q4[c].x, ov[j]);
+        ov[j] = fmaf(s[j][c].y, q4[c].y, ov[j]);
+        ov[j] = fmaf(s[j][c].z, q4[c].z, ov[j]);
+        ov[j] = fmaf(s[j][c].w, q4[c].w, ov[j]);
+        const size_t off = sbase + (size_t)v * DK + (sub + LPR * c) * 4;
+        if (STATE_BF16) {
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ssm_state) + off) =
+              make_uint2(pack_bf16x2(s[j][c].x, s[j][c].y), pack_bf16x2(s[j][c].z, s[j][c].w));
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ssm_state) + off) = s[j][c];
+        }
       }
     }
 #pragma unroll
