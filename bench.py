@@ -103,8 +103,6 @@ def run_cpu_baseline(args, steps=None, seconds=None):
 
 # ----------------------------------------------------------------- traffic
 
-ROOT = os.path.dirname(os.path.abspath(__file__))
-
 
 def kernel_source_hash() -> str:
     """sha256 (16 hex digits) of the kernel sources and the C header."""
