@@ -42,7 +42,10 @@
  *                              v(Hv*dv) | z(Hv*dv)
  *  qkvz (MXFP4)                codes [Nqkvz][H/2] uint8 (element 2i in the
  *                              low nibble, OCP E2M1) and qkvz_scales
- *                              [Nqkvz][H/32] uint8 e8m0 (2^(byte-127))
+ *                              [Nqkvz][H/32] uint8 e8m0 (2^(byte-127));
+ *                              tensor-core engine only, H a multiple of
+ *                              512, dk = 128; the normed input is then
+ *                              quantised to MXFP4 per block of 32 as well
  *  ba                          [Nba][H] bf16, rows b(Hv) | a(Hv)
  *  conv_w                      [C][K] bf16, tap K-1 multiplies the new input
  *  input_norm_w                [H] bf16 (Gemma form: x * rstd * (1 + w))
@@ -133,8 +136,9 @@ typedef struct {
 typedef struct gdn_decode gdn_decode_t;
 
 /* Device bytes the caller must provide as the workspace for this config
- * (counters, the sticky error word, norm and projection partials, the normed
- * input image, activations). 0 if the config is invalid or unsupported. */
+ * (counters, the sticky error word, the plan tables, norm and projection
+ * partials, and for the CUDA-core engine the normed input image). 0 if the
+ * config is invalid or unsupported. */
 size_t gdn_decode_workspace_bytes(const gdn_decode_config* cfg);
 
 /* Validate the config for the current device, bind the caller's workspace
@@ -162,7 +166,8 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
 /* Synchronise `stream` and read the sticky error word. Returns GDN_OK, or the
  * recorded device status; *detail (optional) receives the raw word:
  * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
- * 3 projection tile), 15..0 the CTA (deadline) or row (index error). */
+ * 3 projection tile, 4 a tensor-core pipeline stage), 15..0 the CTA
+ * (deadline) or row (index error). */
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail);
 
 /* Clear the error word, all counters and the partial buffers of the
@@ -230,11 +235,12 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
  * Set-up: the first call on a device (with that device current), and every
  * later call whose *cfg differs from the previous call's on that device,
  * first validates the config, looks up the scratch array's device address,
- * zeroes its counters and error word (they must start at zero: each launch
- * waits for counts that grow from zero) and copies the plan tables into it,
- * stream-ordered on `stream`. That first call must come before any stream
- * capture on `stream`. The other parts of the scratch need no initial value;
- * they keep whatever the last call left there.
+ * zeroes its counters, error word and partial buffers, and copies the plan
+ * tables into it, stream-ordered on `stream`. They must start at zero: a
+ * launch takes its number from a counter that grows from zero, and a partial
+ * word carries the number of the launch that wrote it, so with the counters
+ * back at zero an old word would pass for a new one. That first call must
+ * come before any stream capture on `stream`.
  *
  * Arguments, layouts and the launch are those of gdn_decode_step; `cfg` takes
  * the place of the handle. The scratch is shared by every call on a device:
@@ -249,8 +255,8 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
  * does not: use gdn_decode_create with a workspace). Device errors are sticky
  * in the scratch as for a handle: if `detail` is not NULL the call waits for
  * its launch, stores the error word in *detail (layout of gdn_decode_check),
- * returns its status, and if it is non-zero clears the word and the counters
- * so the next call runs. With detail == NULL the call does not synchronise. */
+ * returns its status, and if it is non-zero clears the word, the counters
+ * and the partial buffers so the next call runs. With detail == NULL the call does not synchronise. */
 gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32_t rows, const void* x,
                                   const void* residual, const gdn_decode_weights* w,
                                   const int32_t* state_indices, void* conv_state,
