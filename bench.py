@@ -178,6 +178,19 @@ class Clocks:
         return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's `value` (the slowest rank's time); the value
+    itself on a single process (dist None)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- GPU arm
 
 def native(args):
@@ -283,11 +296,7 @@ def native(args):
     torch.cuda.synchronize()
     # headline: exactly K timed steps
     gk = capture(args.rows, K)
-    ms = time_graph(gk)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(time_graph(gk), dist, "cuda")
     us = ms * 1e3 / K
     live = args.rows
     bytes_launch = shape.launch_bytes(args.rows, live)
@@ -396,7 +405,7 @@ def reference(args):
     d, cores = run_cpu_baseline(args, steps=args.steps)
     v = round(d["us_per_step"], 1)
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "µs/launch", "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "µs/launch", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{shape.name}", "rows": args.rows},
