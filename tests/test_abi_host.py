@@ -84,6 +84,29 @@ def test_create_and_step_argument_errors(lib):
     lib.gdn_decode_destroy(None)  # no-op
 
 
+def test_static_step_argument_errors_return_before_any_cuda_call(lib):
+    # every case fails host-side validation, so no pointer below is ever used
+    c = _cfg()
+    P = ctypes.c_void_p
+    ok, odd = P(0x10000), P(0x10001)  # placeholders: aligned / misaligned
+    w = _native.Weights()
+    for f in ("input_norm_w", "qkvz", "ba", "conv_w", "A_log", "dt_bias", "gated_norm_w"):
+        setattr(w, f, ok.value)  # each case below has exactly one defect
+    args = lambda x, idx: (1, x, None, ctypes.byref(w), idx, ok, ok, ok, ok, None, None)
+    assert lib.gdn_decode_step_static(None, *args(ok, ok)) == _native.GDN_ERR_ARG       # no config
+    assert lib.gdn_decode_step_static(ctypes.byref(c), 1, ok, None, None, ok, ok, ok, ok, ok, None,
+                                      None) == _native.GDN_ERR_ARG                     # no weights
+    assert lib.gdn_decode_step_static(ctypes.byref(c), 0, ok, None, ctypes.byref(w), ok, ok, ok, ok, ok,
+                                      None, None) == _native.GDN_ERR_ARG               # rows < 1
+    assert lib.gdn_decode_step_static(ctypes.byref(c), c.max_rows + 1, ok, None, ctypes.byref(w), ok, ok,
+                                      ok, ok, ok, None, None) == _native.GDN_ERR_ARG   # rows > max_rows
+    assert lib.gdn_decode_step_static(ctypes.byref(c), *args(None, ok)) == _native.GDN_ERR_ARG  # no x
+    assert lib.gdn_decode_step_static(ctypes.byref(c), *args(ok, None)) == _native.GDN_ERR_ARG  # no indices
+    assert lib.gdn_decode_step_static(ctypes.byref(c), *args(odd, ok)) == _native.GDN_ERR_ARG   # misaligned x
+    mx = _cfg(qkvz_format=_native.GDN_W_MXFP4)
+    assert lib.gdn_decode_step_static(ctypes.byref(mx), *args(ok, ok)) == _native.GDN_ERR_ARG  # MXFP4, no scales
+
+
 def test_product_path_never_imports_the_oracle():
     pkg = os.path.join(B.ROOT, "gated_deltanet_layer_gb300")
     for dirpath, _, files in os.walk(pkg):
