@@ -543,8 +543,8 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
 
 // MMA issuer (one whole warp; lane 0 issues): per unit, 4 MMAs of K = 16 over
 // the stage's 64 columns into the segment's accumulator; a segment (the units
-// of one group) starts by overwriting. Commits release the stage and, at a segment's end, hand the
-// accumulator to the drain.
+// of one group) starts by overwriting. Commits release the stage and, at a
+// segment's end, hand the accumulator to the drain.
 template <bool FP4>
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                 uint8_t* sX, uint8_t* sXq, int ub, int nunits, uint32_t tmem) {
