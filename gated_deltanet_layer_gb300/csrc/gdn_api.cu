@@ -98,7 +98,7 @@ gdn_status validate(const gdn_decode_config* c) {
 }
 
 // Stream-K split of the projection units over G CTAs. A unit is one 64-column
-// step (k-step) of one 128-row tile. Units are ordered by group: group g =
+// step (k-step) of one 256-row tile. Units are ordered by group: group g =
 // (k-block kb = g / T, tile t = g % T) holds the `kblock` k-steps kb*kblock ..
 // of tile t. With kblock = ksteps the order is tile-major (a CTA sweeps K of
 // one tile, then the next); the tensor-core engine of a large layer uses
