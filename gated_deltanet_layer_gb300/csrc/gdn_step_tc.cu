@@ -355,7 +355,8 @@ static __device__ __forceinline__ float exp2_int(int e) {
 // MXFP4 quantisation of one row's block of 32 normed inputs, 8 of them in
 // this thread (the block's 4 chunks are 4 consecutive lanes): the block scale
 // 2^E from the block maximum with its mantissa rounded half up to one bit,
-// E = its exponent - 2 clamped to [-127, 127]; each value |x| / 2^E rounded
+// E = its exponent - 2 clamped to [-126, 127] (a normal scale, also for an
+// all-zero block); each value |x| / 2^E rounded
 // to the e2m1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} (ties to even, saturating at
 // 6), returned dequantised (exact in bf16). The dynamic MX quantiser of
 // vLLM #60833 (review "How to make the MXFP6 weights", step 2) with E2M1's
@@ -375,7 +376,7 @@ static __device__ __forceinline__ uint4 quantize8_mxfp4(uint4 xv) {
   m = fmaxf(m, __shfl_xor_sync(mask, m, 1));
   m = fmaxf(m, __shfl_xor_sync(mask, m, 2));
   int E = (int)(((__float_as_uint(m) + (1u << 21)) >> 23) & 0xffu) - 127 - 2;
-  E = max(-127, min(127, E));
+  E = max(-126, min(127, E));
   const float inv = exp2_int(-E), scale = exp2_int(E);
   uint32_t o[4];
 #pragma unroll

@@ -42,7 +42,9 @@ Layouts (the library's documented layouts):
 
 Parity status: every function below is pinned by the CPU tests against
 closed forms, hand-worked values, brute force or library routines (see
-tests/test_oracle_pins.py). No function is "parity unpinned".
+tests/test_oracle_pins.py); the split's slices are pinned index by index
+against the documented row layout and through whole steps whose core and
+state depend on z and a alone.
 """
 from __future__ import annotations
 
@@ -194,8 +196,9 @@ def mxfp4_quantize_block(v):
     quantiser with the element type's maximum): take the block maximum |v|,
     round its f32 mantissa to 1 bit (half up: a carry moves the exponent),
     keep only the exponent E, and use 2^(E - 2) as the scale, E - 2 clamped
-    to [-127, 127]; E2M1's largest exponent is 2. An all-zero block keeps a
-    normal scale. Elements: |v| / scale rounded to the E2M1 grid, ties to
+    to [-126, 127] so that the scale is always a normal f32 (an all-zero
+    block, whose maximum has exponent field 0, gets 2^-126); E2M1's largest
+    exponent is 2. Elements: |v| / scale rounded to the E2M1 grid, ties to
     even, saturating at 6.
 
     Returns (codes [32] uint8, scale exponent int, e8m0 byte).
@@ -207,7 +210,7 @@ def mxfp4_quantize_block(v):
     # weight (2^21 in the 23-bit field); a carry moves into the exponent.
     e_field = ((bits + (1 << 21)) >> 23) & 0xFF
     exp = e_field - 127 - 2
-    exp = int(min(max(exp, -127), 127))
+    exp = int(min(max(exp, -126), 127))
     scale = math.ldexp(1.0, exp)
     mag = _e2m1_round_magnitude(np.abs(v) / scale)
     codes = _magnitude_to_code(mag)

@@ -161,9 +161,19 @@ def test_mxfp4_quantize_block_scale_rule_and_round_trip():
     v[0] = 1.7  # mantissa below 1.75: no carry; 1.7/2^-2 = 6.8 saturates at 6
     codes, exp, _ = O.mxfp4_quantize_block(v)
     assert exp == -2 and O.e2m1_value(codes[0]) == 6.0
-    # all-zero block: zero codes, a finite scale
+    # all-zero block: zero codes and the smallest normal scale, 2^-126 (the
+    # rule clamps the scale exponent to [-126, 127], so a scale is never
+    # subnormal or zero)
     codes, exp, byte = O.mxfp4_quantize_block(np.zeros(32))
-    assert np.all(codes == 0) and 0 <= byte <= 254
+    assert np.all(codes == 0) and exp == -126 and byte == 1
+    # a block far below the clamp: the scale stays 2^-126 and every element
+    # (2^-4 of that scale) rounds to the zero code
+    codes, exp, byte = O.mxfp4_quantize_block(np.full(32, 2.0**-130))
+    assert exp == -126 and np.all(codes == 0)
+    # the top of the range: a block maximum of 6 * 2^127 keeps the scale 2^127
+    v = np.zeros(32); v[3] = 1.5 * 2.0**127
+    codes, exp, byte = O.mxfp4_quantize_block(v)
+    assert exp == 127 - 2 and byte == 252 and O.e2m1_value(codes[3]) * 2.0**exp == v[3]
     # every element within the grid's reach: |v| <= 6*scale after saturation
     for _ in range(50):
         v = rng.standard_normal(32) * 10.0 ** rng.uniform(-3, 3)
@@ -378,3 +388,101 @@ def test_step_exact_write_and_frozen_state():
                 vv = y[2 * Hk * dk + h * dv: 2 * Hk * dk + (h + 1) * dv]
                 Snew = out["ssm_state"][s, h]  # f32-rounded
                 np.testing.assert_allclose(Snew @ kv, vv, atol=2e-6 + 1e-6 * np.abs(vv).max())
+
+
+# ---------------------------------------------------------------- split (q | k | v | z, b | a)
+
+def test_split_projection_follows_the_documented_row_layout():
+    """Every projection output lands where the documented layout puts it:
+    in_proj_qkvz rows are q (Hk*dk) | k (Hk*dk) | v (Hv*dv) | z (Hv*dv),
+    in_proj_ba rows are b (Hv) | a (Hv). Each value encodes its row and
+    position, and each slot of each slice is checked one by one."""
+    Hk, Hv, dk, dv, W = 2, 6, 3, 4, 2
+    nq = 2 * Hk * dk + 2 * Hv * dv
+    p = np.array([[1000.0 * w + n for n in range(nq)] for w in range(W)])
+    pba = np.array([[1000.0 * w + 500 + n for n in range(2 * Hv)] for w in range(W)])
+    q, k, v, z, b, a = O.split_projection(p, pba, Hk, Hv, dk, dv)
+    assert q.shape == k.shape == (W, Hk, dk) and v.shape == z.shape == (W, Hv, dv)
+    assert b.shape == a.shape == (W, Hv)
+    for w in range(W):
+        for h in range(Hk):
+            for d in range(dk):
+                assert q[w, h, d] == 1000 * w + h * dk + d
+                assert k[w, h, d] == 1000 * w + Hk * dk + h * dk + d
+        for h in range(Hv):
+            for d in range(dv):
+                assert v[w, h, d] == 1000 * w + 2 * Hk * dk + h * dv + d
+                assert z[w, h, d] == 1000 * w + 2 * Hk * dk + Hv * dv + h * dv + d
+            assert b[w, h] == 1000 * w + 500 + h
+            assert a[w, h] == 1000 * w + 500 + Hv + h
+
+
+def _gate_layer(shape, seed):
+    """A crafted layer whose xn is exactly 1 (x = 1, first layer, w_in = 0),
+    whose in_proj_qkvz and in_proj_ba are zero except where a test puts one
+    value per row in column 0 (so that output row n is exactly that value),
+    beta = 0 (b rows -1/16: b = -H/16, sigmoid(b) below 1e-27) and g = 0
+    (A_log = -inf), and whose conv input is a constant: conv state 1 in the
+    oldest tap, conv weight 1 there and 0 elsewhere, so every conv output is
+    silu(1) whatever the projection gives."""
+    H, Hv = shape.hidden, shape.num_v_heads
+    x, _, w, idx, conv, ssm = _np_inputs(shape, 2, seed)
+    x = np.ones_like(x)
+    w["input_norm_w"] = np.zeros(H)
+    w["qkvz"] = np.zeros_like(w["qkvz"])
+    w["ba"] = np.zeros_like(w["ba"])
+    w["ba"][:Hv] = -1.0 / 16.0
+    w["A_log"] = np.full(Hv, -np.inf)
+    w["dt_bias"] = np.zeros(Hv)
+    w["conv_w"] = np.zeros_like(w["conv_w"])
+    w["conv_w"][:, 0] = 1.0
+    conv = np.zeros_like(conv)
+    conv[:, :, 0] = 1.0
+    return x, w, idx, conv, ssm
+
+
+def test_step_core_takes_the_z_slice():
+    """Only the z rows of in_proj_qkvz are non-zero, each with its own value.
+    With beta = 0 and g = 0 the state is unchanged, so o = S q^; every state
+    row set to the same positive vector makes o a positive constant over the
+    head, whose RMSNorm is 1 (to 1e-6), so with w_g = 1 the core is
+    bf16(silu(z)) with z the value put in that z row. A z slice taken from
+    another region reads zero rows (core 0), from another head the wrong value."""
+    shape = WL.TINY
+    Hk, Hv, dk, dv = shape.num_k_heads, shape.num_v_heads, shape.head_k_dim, shape.head_v_dim
+    x, w, idx, conv, ssm = _gate_layer(shape, 150)
+    zt = np.array([[0.25 * ((h * 7 + d) % 23) - 2.5 + 0.125 * (h % 3) for d in range(dv)] for h in range(Hv)])
+    zt = O.bf16_round(zt)
+    z0 = 2 * Hk * dk + Hv * dv
+    for h in range(Hv):
+        for d in range(dv):
+            w["qkvz"][z0 + h * dv + d, 0] = zt[h, d]
+    w["gated_norm_w"] = np.ones(dv)
+    ssm = np.array(ssm)
+    ssm[:] = 0.05 + 0.01 * (np.arange(dk) % 5)  # every row of every head the same positive vector
+    out = O.gdn_step(shape, x, None, w, idx, conv, ssm)
+    want = O.bf16_round(zt * (1.0 / (1.0 + np.exp(-zt))))
+    for r in range(len(idx)):
+        got = out["core"][r].reshape(Hv, dv)
+        np.testing.assert_allclose(got, want, rtol=2.0**-8, atol=0)
+        assert np.count_nonzero(got) == np.count_nonzero(want)
+
+
+def test_step_decay_takes_the_a_slice():
+    """Only the a rows of in_proj_ba carry values (one per value head), with
+    A_log = 0 and dt_bias = 0, beta = 0: each head's state is scaled by
+    e^g with g = -softplus(a), that is by 1 / (1 + e^a). Distinct a values
+    per head make every head's factor distinct; an a slice taken from the b
+    rows (a = -H/16) would leave the state unchanged."""
+    shape = WL.TINY
+    H, Hv = shape.hidden, shape.num_v_heads
+    x, w, idx, conv, ssm = _gate_layer(shape, 160)
+    w["A_log"] = np.zeros(Hv)
+    at = O.bf16_round(np.linspace(-3.0, 2.0, Hv))
+    w["ba"][Hv:] = 0.0
+    w["ba"][Hv:, 0] = at
+    out = O.gdn_step(shape, x, None, w, idx, conv, ssm)
+    for s in idx:
+        for h in range(Hv):
+            factor = 1.0 / (1.0 + math.exp(at[h]))
+            np.testing.assert_allclose(out["ssm_state"][s, h], ssm[s, h] * factor, rtol=2.0**-23, atol=1e-30)
