@@ -7,8 +7,15 @@ of rows. Launches are replayed from a CUDA graph; every launch reads another
 copy of the layer weights (the copies together exceed L2) and another set of
 state slots, so each launch streams its weights and state from HBM.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--rows R] [--workload shard]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--rows R] [--workload full]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+The headline is the full unsharded layer (H=8192, 16 key / 64 value heads,
+dk=dv=128, 512 slots of f32 state) at 16 rows: the largest configuration of
+the method that runs on one GPU. The same line carries per-width tables of
+every workload (the shard, the full layer, the shard with a bf16 state in
+its first-layer variant with a quarter of the rows padding, and the dense
+MXFP4 layer over a rotated 48-layer stack).
 
 Prints one JSON line (rank 0).
 """
@@ -36,14 +43,20 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="shard")
+    ap.add_argument("--workload", default="full")
     ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
-    ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width table")
+    ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width tables")
+    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4",
+                    help="workloads of the per-width tables ('' for none)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--engine", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
+
+
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal
 
 
 def peaks():
@@ -53,6 +66,17 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+# Per-width table recipe of each workload: widths, the pad fraction, the
+# first-layer variant, the least number of weight copies the launches rotate
+# over (the dense MXFP4 layer rotates a 48-layer stack).
+TABLES = {
+    "shard": {"widths": [1, 2, 4, 8, 16]},
+    "full": {"widths": [1, 2, 4, 8, 16]},
+    "shard_bf16": {"widths": [1, 3, 8, 9, 16], "pad": 0.25, "first_layer": True},
+    "dense_mxfp4": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
+}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -193,9 +217,97 @@ def max_over_ranks(value: float, dist, device) -> float:
 
 # ----------------------------------------------------------------- GPU arm
 
+class Rig:
+    """One workload on the device: weight copies the launches rotate over
+    (together larger than 3x L2, and at least `min_copies`), the conv and SSM
+    state of every slot, and a handle."""
+
+    def __init__(self, shape, g, l2, engine, min_copies=4):
+        import torch
+        from gated_deltanet_layer_gb300 import GdnDecode
+        self.shape, self.g = shape, g
+        wbytes = shape.weight_bytes()
+        self.ncopy = max(min_copies, int((3 * l2 + wbytes - 1) // wbytes) + 1)
+        self.wbytes = wbytes
+        H, Hv = shape.hidden, shape.num_v_heads
+
+        def qkvz():
+            if shape.qkvz_format == "mxfp4":  # e2m1 codes uniform over the 16 codes, block exponents U{-8..-4}
+                return {"qkvz": torch.randint(0, 256, (shape.n_qkvz, H // 2), generator=g, device="cuda",
+                                              dtype=torch.uint8),
+                        "qkvz_scales": (127 + torch.randint(-8, -3, (shape.n_qkvz, H // 32), generator=g,
+                                                            device="cuda")).to(torch.uint8)}
+            return {"qkvz": self.bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None}
+
+        self.copies = []
+        for _ in range(self.ncopy):
+            self.copies.append({
+                "input_norm_w": self.bf16(H, std=0.1),
+                **qkvz(),
+                "ba": self.bf16(shape.n_ba, H, std=0.02),
+                "conv_w": self.bf16(shape.conv_channels, shape.conv_kernel, std=0.02),
+                "A_log": -2.0 * torch.rand(Hv, generator=g, device="cuda"),
+                "dt_bias": self.bf16(Hv, std=0.5),
+                "gated_norm_w": self.bf16(shape.head_v_dim, std=0.1),
+            })
+        sdt = torch.bfloat16 if shape.ssm_dtype == "bf16" else torch.float32
+        self.conv = self.bf16(shape.num_slots, shape.conv_channels, shape.conv_kernel - 1, std=1.0)
+        self.ssm = (torch.randn(shape.num_slots, Hv, shape.head_v_dim, shape.head_k_dim, generator=g,
+                                device="cuda") * 0.1).to(sdt)
+        self.layer = GdnDecode(shape, engine=engine)
+        self.wstructs = [self.layer.weights_struct(c) for c in self.copies]
+
+    def bf16(self, *s, std):
+        import torch
+        return (torch.randn(*s, generator=self.g, device="cuda") * std).to(torch.bfloat16)
+
+    def batch(self, rows, n, pad=0.0, first_layer=False):
+        """n distinct step inputs of `rows` rows with fresh random slots each;
+        round(pad * rows) of the rows are pad rows (index 0)."""
+        import torch
+        sh = self.shape
+        npad = int(round(pad * rows))
+        out = []
+        for _ in range(n):
+            perm = torch.randperm(sh.num_slots - 1, generator=self.g, device="cuda")[:rows] + 1
+            if npad:
+                perm[torch.randperm(rows, generator=self.g, device="cuda")[:npad]] = 0
+            out.append((self.bf16(rows, sh.hidden, std=1.0), None if first_layer else self.bf16(rows, sh.hidden, std=1.0),
+                        perm.to(torch.int32).contiguous(),
+                        torch.empty(rows, sh.num_v_heads * sh.head_v_dim, dtype=torch.bfloat16, device="cuda"),
+                        torch.empty(rows, sh.hidden, dtype=torch.bfloat16, device="cuda")))
+        return out
+
+    def capture(self, rows, n, pad=0.0, first_layer=False):
+        """A CUDA graph of n launches, each on the next weight copy."""
+        import torch
+        batch = self.batch(rows, min(n, 64), pad, first_layer)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            # one eager launch first (lazy set-up outside the capture)
+            x, r, i, c, ro = batch[0]
+            self.layer.step(x, r, self.copies[0], i, self.conv, self.ssm, c, ro, weights_struct=self.wstructs[0])
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(graph, stream=s):
+                for k in range(n):
+                    x, r, i, c, ro = batch[k % len(batch)]
+                    self.layer.step(x, r, self.copies[k % self.ncopy], i, self.conv, self.ssm, c, ro,
+                                    weights_struct=self.wstructs[k % self.ncopy])
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return graph
+
+    def check(self):
+        st, detail = self.layer.check()
+        if st != 0:
+            raise RuntimeError(f"device error word 0x{detail:08x} ({self.shape.name})")
+
+
 def native(args):
     import torch
-    from gated_deltanet_layer_gb300 import GdnDecode, workloads as WL
+    from gated_deltanet_layer_gb300 import workloads as WL
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -212,68 +324,6 @@ def native(args):
     g = torch.Generator(device="cuda")
     g.manual_seed(1234 + rank)
 
-    # Weight copies: together at least 3x L2, so no launch finds its weights in L2.
-    wbytes = shape.weight_bytes()
-    ncopy = max(4, int((3 * l2 + wbytes - 1) // wbytes) + 1)
-
-    def bf16(*s, std):
-        return (torch.randn(*s, generator=g, device="cuda") * std).to(torch.bfloat16)
-
-    H, Hv = shape.hidden, shape.num_v_heads
-    def qkvz():
-        if shape.qkvz_format == "mxfp4":  # e2m1 codes uniform over the 16 codes, block exponents U{-8..-4}
-            return {"qkvz": torch.randint(0, 256, (shape.n_qkvz, H // 2), generator=g, device="cuda",
-                                          dtype=torch.uint8),
-                    "qkvz_scales": (127 + torch.randint(-8, -3, (shape.n_qkvz, H // 32), generator=g,
-                                                        device="cuda")).to(torch.uint8)}
-        return {"qkvz": bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None}
-
-    copies = []
-    for _ in range(ncopy):
-        copies.append({
-            "input_norm_w": bf16(H, std=0.1),
-            **qkvz(),
-            "ba": bf16(shape.n_ba, H, std=0.02),
-            "conv_w": bf16(shape.conv_channels, shape.conv_kernel, std=0.02),
-            "A_log": -2.0 * torch.rand(Hv, generator=g, device="cuda"),
-            "dt_bias": bf16(Hv, std=0.5),
-            "gated_norm_w": bf16(shape.head_v_dim, std=0.1),
-        })
-    sdt = torch.bfloat16 if shape.ssm_dtype == "bf16" else torch.float32
-    conv = bf16(shape.num_slots, shape.conv_channels, shape.conv_kernel - 1, std=1.0)
-    ssm = (torch.randn(shape.num_slots, Hv, shape.head_v_dim, shape.head_k_dim, generator=g,
-                       device="cuda") * 0.1).to(sdt)
-    layer = GdnDecode(shape, engine=args.engine)
-    wstructs = [layer.weights_struct(c) for c in copies]
-
-    def make_batch(rows, n):
-        """n distinct step inputs of `rows` rows with fresh random slots each."""
-        out = []
-        for _ in range(n):
-            perm = torch.randperm(shape.num_slots - 1, generator=g, device="cuda")[:rows] + 1
-            out.append((bf16(rows, H, std=1.0), bf16(rows, H, std=1.0), perm.to(torch.int32).contiguous(),
-                        torch.empty(rows, Hv * shape.head_v_dim, dtype=torch.bfloat16, device="cuda"),
-                        torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")))
-        return out
-
-    def capture(rows, n):
-        batch = make_batch(rows, min(n, 64))
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            # one eager launch per input set first (lazy init outside capture)
-            x, r, i, c, ro = batch[0]
-            layer.step(x, r, copies[0], i, conv, ssm, c, ro, weights_struct=wstructs[0])
-            torch.cuda.current_stream().synchronize()
-            with torch.cuda.graph(graph, stream=s):
-                for k in range(n):
-                    x, r, i, c, ro = batch[k % len(batch)]
-                    layer.step(x, r, copies[k % ncopy], i, conv, ssm, c, ro, weights_struct=wstructs[k % ncopy])
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        return graph
-
     def time_graph(graph):
         st = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -288,81 +338,112 @@ def native(args):
             dist.barrier()
         return e0.elapsed_time(e1)  # ms
 
+    def row_of(sh, u, rows, live, first_layer):
+        b = sh.launch_bytes(rows, live, first_layer=first_layer)
+        gbs = b / u / 1e3
+        return {"us": round(u, 3), "GBps": round(gbs, 1), "frac_of_" + peak_kind: round(gbs / peak, 4),
+                "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": b, "live_rows": live}
+
+    def width_table(rig, widths, pad=0.0, first_layer=False):
+        """µs per launch of a graph of 100 launches, median of replays over
+        ~0.3 s (so the clock sampler sees the GPU under load)."""
+        out = {}
+        for wdt in widths:
+            gg = rig.capture(wdt, 100, pad, first_layer)
+            times = []
+            t_end = time.time() + 0.3
+            while time.time() < t_end or len(times) < 5:
+                times.append(time_graph(gg) * 10.0)  # µs per launch
+            times.sort()
+            live = wdt - int(round(pad * wdt))
+            out[str(wdt)] = row_of(rig.shape, times[len(times) // 2], wdt, live, first_layer)
+            del gg
+        rig.check()
+        return out
+
     K, Wm = args.steps, args.warmup
     clocks = Clocks(local)
+    rig = Rig(shape, g, l2, args.engine)
     # warm-up: W untimed steps
-    gw = capture(args.rows, max(3, Wm))
+    gw = rig.capture(args.rows, max(3, Wm))
     gw.replay()
     torch.cuda.synchronize()
     # headline: exactly K timed steps
-    gk = capture(args.rows, K)
+    gk = rig.capture(args.rows, K)
     ms = max_over_ranks(time_graph(gk), dist, "cuda")
     us = ms * 1e3 / K
-    live = args.rows
-    bytes_launch = shape.launch_bytes(args.rows, live)
-    st, detail = layer.check()
-    if st != 0:
-        raise RuntimeError(f"device error word 0x{detail:08x}")
+    bytes_launch = shape.launch_bytes(args.rows, args.rows)
+    rig.check()
+    del gw, gk
 
-    # per-width table (outside the headline timed region); each graph replayed
-    # for ~0.3 s so the clock sampler sees the GPU under load
-    table = {}
-    for wdt in [int(v) for v in args.widths.split(",") if v]:
-        gg = capture(wdt, 100)
-        times = []
-        t_end = time.time() + 0.3
-        while time.time() < t_end or len(times) < 5:
-            times.append(time_graph(gg) * 10.0)  # µs per launch
-        times.sort()
-        u = times[len(times) // 2]
-        b = shape.launch_bytes(wdt, wdt)
-        table[str(wdt)] = {"us": round(u, 3), "GBps": round(b / u / 1e3, 1),
-                           "frac_of_" + peak_kind: round(b / u / 1e3 / peak, 4), "bytes": b}
+    e2e = None
+    if not args.no_e2e:
+        # end to end through the public API with host buffers: per step, copy this
+        # step's inputs from pinned host memory, launch, read the outputs back
+        H, Hv = shape.hidden, shape.num_v_heads
+        Bi = args.rows * H * 2 * 2 + args.rows * 4
+        Bo = args.rows * Hv * shape.head_v_dim * 2 + args.rows * H * 2
+        hx = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+        hr = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+        hi = torch.randperm(shape.num_slots - 1)[:args.rows].add(1).to(torch.int32).pin_memory()
+        hx.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
+        hr.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
+        hc = torch.empty(args.rows, Hv * shape.head_v_dim, dtype=torch.bfloat16).pin_memory()
+        ho = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
+        dx, dr, di = (torch.empty_like(hx, device="cuda"), torch.empty_like(hr, device="cuda"),
+                      torch.empty_like(hi, device="cuda"))
+        dc, do = torch.empty_like(hc, device="cuda"), torch.empty_like(ho, device="cuda")
+
+        def e2e_step(k):
+            dx.copy_(hx, non_blocking=True)
+            dr.copy_(hr, non_blocking=True)
+            di.copy_(hi, non_blocking=True)
+            rig.layer.step(dx, dr, rig.copies[k % rig.ncopy], di, rig.conv, rig.ssm, dc, do,
+                           weights_struct=rig.wstructs[k % rig.ncopy])
+            hc.copy_(dc, non_blocking=True)
+            ho.copy_(do, non_blocking=True)
+
+        for k in range(max(3, Wm)):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        st0 = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st0)
+        for k in range(K):
+            e2e_step(k)
+        e1.record(st0)
+        torch.cuda.synchronize()
+        rig.check()
+        e2e = {"value": round(e0.elapsed_time(e1) * 1e3 / K, 3), "unit": "µs/launch", "h2d_bytes_per_step": Bi,
+               "d2h_bytes_per_step": Bo, "how": "eager gdn_decode_step via the Python binding with "
+                                                "pinned-host copies in and out each step"}
+    n_ctas, engine = rig.layer.launch_info(args.rows)
+    ncopy, wbytes = rig.ncopy, rig.wbytes
+
+    # per-width tables, one workload at a time (outside the headline timed region)
+    tables = {}
+    widths = [int(v) for v in args.widths.split(",") if v]
+    for name in [t for t in args.tables.split(",") if t]:
+        rec = TABLES[name]
+        if name != args.workload or rig is None:
+            rig = None
+            torch.cuda.empty_cache()
+            rig = Rig(WL.SHAPES[name], g, l2, args.engine, rec.get("min_copies", 4))
+        ws = rec["widths"] if name != args.workload else sorted(set(rec["widths"]) | set(widths))
+        tables[name] = {"copies": rig.ncopy, "first_layer": rec.get("first_layer", False),
+                        "pad_fraction": rec.get("pad", 0.0),
+                        "widths": width_table(rig, ws, rec.get("pad", 0.0), rec.get("first_layer", False))}
+        rig = None
     clk = clocks.stop()
 
-    # end to end through the public API with host buffers: per step, copy this
-    # step's inputs from pinned host memory, launch, read the outputs back
-    Bi = args.rows * H * 2 * 2 + args.rows * 4
-    Bo = args.rows * Hv * shape.head_v_dim * 2 + args.rows * H * 2
-    hx = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
-    hr = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
-    hi = torch.randperm(shape.num_slots - 1)[:args.rows].add(1).to(torch.int32).pin_memory()
-    hx.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
-    hr.copy_(torch.randn(args.rows, H).to(torch.bfloat16))
-    hc = torch.empty(args.rows, Hv * shape.head_v_dim, dtype=torch.bfloat16).pin_memory()
-    ho = torch.empty(args.rows, H, dtype=torch.bfloat16).pin_memory()
-    dx, dr, di = torch.empty_like(hx, device="cuda"), torch.empty_like(hr, device="cuda"), torch.empty_like(hi, device="cuda")
-    dc, do = torch.empty_like(hc, device="cuda"), torch.empty_like(ho, device="cuda")
-
-    def e2e_step(k):
-        dx.copy_(hx, non_blocking=True)
-        dr.copy_(hr, non_blocking=True)
-        di.copy_(hi, non_blocking=True)
-        layer.step(dx, dr, copies[k % ncopy], di, conv, ssm, dc, do, weights_struct=wstructs[k % ncopy])
-        hc.copy_(dc, non_blocking=True)
-        ho.copy_(do, non_blocking=True)
-
-    for k in range(max(3, Wm)):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    st0 = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st0)
-    for k in range(K):
-        e2e_step(k)
-    e1.record(st0)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1e3 / K
-
-    n_ctas, engine = layer.launch_info(args.rows)
     result = {
         "metric": METRIC, "value": round(us, 3), "unit": "µs/launch", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("mxfp4" if shape.qkvz_format == "mxfp4" else "bf16") + " weights, f32 math, " + shape.ssm_dtype + " state",
         "data": "synthetic (seeded random weights and states of the layer's shapes)",
-        "config": {"workload": f"{shape.name}: H={H} Hk={shape.num_k_heads} Hv={Hv} dk=dv={shape.head_k_dim} "
-                               f"slots={shape.num_slots} {shape.ssm_dtype} state, "
+        "config": {"workload": f"{shape.name}: H={shape.hidden} Hk={shape.num_k_heads} Hv={shape.num_v_heads} "
+                               f"dk=dv={shape.head_k_dim} slots={shape.num_slots} {shape.ssm_dtype} state, "
                                f"{'MXFP4' if shape.qkvz_format == 'mxfp4' else 'bf16'} in_proj_qkvz",
                    "rows": args.rows, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: weights rotated over {ncopy} copies "
@@ -371,14 +452,13 @@ def native(args):
                    "grid": n_ctas, "engine": engine,
                    "launch": "persistent grid, one CTA per SM; programmatic dependent launch between steps"},
         "achieved_GBps": round(bytes_launch / us / 1e3, 1),
-        "widths": table,
+        "frac_of_nominal_8TBps": round(bytes_launch / us / 1e3 / NOMINAL_HBM_GBS, 4),
+        "widths": tables,
         "roofline": {"bound": "hbm", "achieved": round(bytes_launch / us / 1e3, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(bytes_launch / us / 1e3 / peak, 4),
                      "traffic": measured_traffic(args.workload, args.rows), "peak_kind": peak_kind,
                      "bytes_per_launch": bytes_launch},
-        "e2e": {"value": round(e2e_us, 3), "unit": "µs/launch", "h2d_bytes_per_step": Bi,
-                "d2h_bytes_per_step": Bo, "how": "eager gdn_decode_step via the Python binding with "
-                                                 "pinned-host copies in and out each step"},
+        "e2e": e2e,
         "gpu_launches": K,
         "clocks": clk,
         "context": PAGES_NOTE,

@@ -108,17 +108,15 @@ class GdnDecode:
 
     def timeline(self, stream=None):
         """Phase stamps of the last step (handle made with GDN_DEBUG_TIMELINE):
-        (per-CTA [G][48] ns, per-tile [T][2] ns) as nested lists."""
+        per-CTA [G][48] nanosecond stamps as nested lists."""
         L = _native.lib()
-        cap_c, cap_t = 256 * 48, 4096 * 2
-        cs, ts = (ctypes.c_uint64 * cap_c)(), (ctypes.c_uint64 * cap_t)()
-        g, t = ctypes.c_int32(), ctypes.c_int32()
-        st = L.gdn_decode_debug_timeline(self._h, _stream_ptr(stream), cs, cap_c, ts, cap_t,
-                                         ctypes.byref(g), ctypes.byref(t))
+        cap_c = 256 * 48
+        cs = (ctypes.c_uint64 * cap_c)()
+        g = ctypes.c_int32()
+        st = L.gdn_decode_debug_timeline(self._h, _stream_ptr(stream), cs, cap_c, ctypes.byref(g))
         if st != GDN_OK:
             raise GdnError("gdn_decode_debug_timeline", st)
-        return ([list(cs[i * 48:(i + 1) * 48]) for i in range(g.value)],
-                [list(ts[i * 2:(i + 1) * 2]) for i in range(t.value)])
+        return [list(cs[i * 48:(i + 1) * 48]) for i in range(g.value)]
 
     def check(self, stream=None):
         """(status, detail word) of the sticky device error word; synchronises."""

@@ -18,8 +18,10 @@ GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05 = 0, 1, 2
 GDN_DEBUG_SKIP_NORM_PUBLISH = 0x1
 GDN_DEBUG_TIMELINE = 0x2
 GDN_LAUNCH_COOPERATIVE = 0x1
+GDN_LAUNCH_NO_EARLY_WEIGHTS = 0x2
 
-# Every symbol the header declares.
+# Every symbol the headers declare (include/gdn_decode.h and the diagnostics
+# in include/gdn_decode_diag.h).
 EXPORTS = (
     "gdn_decode_workspace_bytes", "gdn_decode_create", "gdn_decode_step", "gdn_decode_check",
     "gdn_decode_reset", "gdn_decode_destroy", "gdn_status_string", "gdn_decode_launch_info",
@@ -86,7 +88,7 @@ def lib() -> ctypes.CDLL:
     L.gdn_decode_plan.argtypes = [cfgp, i32, i32p, i32p, u8p, u16p, u8p, u8p, i32, i32p, i32p, i32p]
     L.gdn_decode_plan.restype = ctypes.c_int
     u64p = ctypes.POINTER(ctypes.c_uint64)
-    L.gdn_decode_debug_timeline.argtypes = [vp, vp, u64p, i32, u64p, i32, i32p, i32p]
+    L.gdn_decode_debug_timeline.argtypes = [vp, vp, u64p, i32, i32p]
     L.gdn_decode_debug_timeline.restype = ctypes.c_int
     L.gdn_decode_step_static.argtypes = [cfgp, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp,
                                          u32p]

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "gdn_decode.h"
+#include "gdn_decode_diag.h"
 #include "gdn_kernels.h"
 
 using namespace gdn;
@@ -38,6 +39,14 @@ struct Plan {
   size_t smem;
 };
 
+// Weight tile maps, re-encoded only when the weight pointers change.
+struct MapCache {
+  const void* qkvz_ptr = nullptr;
+  const void* ba_ptr = nullptr;
+  CUtensorMap qkvz;
+  CUtensorMap ba;
+};
+
 // Shared memory a CTA may use on sm_100-class GPUs (opt-in limit per block).
 constexpr size_t kSmemOptin = 232448;
 
@@ -52,11 +61,7 @@ struct gdn_decode {
   Layout lay;
   Plan plan;
   bool pdl;  // launch with programmatic stream serialisation
-  // TMA maps of the last weights a step used
-  const void* map_qkvz_ptr;
-  const void* map_ba_ptr;
-  CUtensorMap map_qkvz;
-  CUtensorMap map_ba;
+  MapCache maps;  // TMA maps of the last weights a step used
 };
 
 namespace {
@@ -79,7 +84,7 @@ gdn_status validate(const gdn_decode_config* c) {
   if (c->engine < GDN_ENGINE_AUTO || c->engine > GDN_ENGINE_TCGEN05) return GDN_ERR_ARG;
   if (!(c->norm_eps >= 0.f) || !(c->gated_norm_eps >= 0.f) || !(c->l2_eps >= 0.f)) return GDN_ERR_ARG;
   if (c->num_ctas < 0 || c->num_ctas > kMaxCtas) return GDN_ERR_ARG;
-  if (c->launch_flags & ~GDN_LAUNCH_COOPERATIVE) return GDN_ERR_ARG;
+  if (c->launch_flags & ~(GDN_LAUNCH_COOPERATIVE | GDN_LAUNCH_NO_EARLY_WEIGHTS)) return GDN_ERR_ARG;
   // Shapes this build runs.
   if (c->conv_kernel != 4) return GDN_ERR_UNSUPPORTED;
   if (c->head_k_dim != c->head_v_dim) return GDN_ERR_UNSUPPORTED;
@@ -349,6 +354,149 @@ bool encode_maps(const gdn_decode_config& c, const gdn_decode_weights* w, CUtens
   return okq && encode_weight_map(mba, w->ba, n_ba(c), c.hidden);
 }
 
+
+// The tensors of one step call.
+struct StepArgs {
+  int32_t rows;
+  const void* x;
+  const void* residual;
+  const gdn_decode_weights* w;
+  const int32_t* idx;
+  void* conv_state;
+  void* ssm_state;
+  void* core_out;
+  void* residual_out;
+};
+
+// Host-side checks of a step's arguments (before any launch): rows in range,
+// non-null and aligned pointers, no output overlapping an input, the
+// scratch or the other output, conv and SSM state apart.
+gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const void* scratch,
+                           size_t scratch_bytes) {
+  const gdn_decode_weights* w = a.w;
+  if (!w) return GDN_ERR_ARG;
+  if (a.rows < 1 || a.rows > c.max_rows) return GDN_ERR_ARG;
+  if (!a.x || !a.idx || !a.conv_state || !a.ssm_state || !a.core_out || !a.residual_out) return GDN_ERR_ARG;
+  if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
+    return GDN_ERR_ARG;
+  if (c.qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
+  const void* a16[] = {a.x, a.residual, a.core_out, a.residual_out, a.conv_state, a.ssm_state, w->input_norm_w,
+                       w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
+  for (const void* q : a16)
+    if (q && !aligned(q, 16)) return GDN_ERR_ARG;
+  if (!aligned(a.idx, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
+  const size_t H = (size_t)c.hidden;
+  const size_t xb = (size_t)a.rows * H * 2;
+  const size_t coreb = (size_t)a.rows * c.num_v_heads * c.head_v_dim * 2;
+  const size_t sdt = c.ssm_dtype == GDN_STATE_BF16 ? 2 : 4;
+  const size_t ssmb = (size_t)c.num_slots * c.num_v_heads * c.head_v_dim * c.head_k_dim * sdt;
+  const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
+  struct Rg { const void* p; size_t n; };
+  const Rg ins[] = {{a.x, xb}, {a.residual, a.residual ? xb : 0}, {a.idx, (size_t)a.rows * 4},
+                    {a.conv_state, convb}, {a.ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
+                    {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
+                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
+                    {scratch, scratch_bytes}};
+  const Rg outs[] = {{a.core_out, coreb}, {a.residual_out, xb}};
+  for (const Rg& o : outs)
+    for (const Rg& i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return GDN_ERR_ARG;
+  if (overlaps(a.core_out, coreb, a.residual_out, xb)) return GDN_ERR_ARG;
+  if (overlaps(a.conv_state, convb, a.ssm_state, ssmb)) return GDN_ERR_ARG;
+  return GDN_OK;
+}
+
+// The launch parameters of a step on scratch `base` (a workspace or the
+// static scratch) laid out as `lay`.
+void fill_params(const gdn_decode_config& c, const Plan& pl, const Layout& lay, char* base, const StepArgs& a,
+                 StepParams* p) {
+  memset(p, 0, sizeof(*p));
+  p->H = c.hidden; p->Hk = c.num_k_heads; p->Hv = c.num_v_heads;
+  p->dk = c.head_k_dim; p->dv = c.head_v_dim; p->C = n_conv(c);
+  p->Nqkvz = n_qkvz(c); p->Nba = n_ba(c); p->num_slots = c.num_slots; p->rows = a.rows;
+  p->group = c.num_v_heads / c.num_k_heads;
+  set_plan_params(pl, p);
+  p->norm_eps = c.norm_eps; p->gnorm_eps = c.gated_norm_eps; p->l2_eps = c.l2_eps; p->q_scale = c.q_scale;
+  p->deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
+  p->debug_flags = c.debug_flags;
+  p->early_weights = (c.launch_flags & GDN_LAUNCH_NO_EARLY_WEIGHTS) ? 0 : 1;
+  p->x = (const __nv_bfloat16*)a.x;
+  p->res = (const __nv_bfloat16*)a.residual;
+  p->res_out = (__nv_bfloat16*)a.residual_out;
+  p->core_out = (__nv_bfloat16*)a.core_out;
+  p->idx = a.idx;
+  p->conv_state = (__nv_bfloat16*)a.conv_state;
+  p->ssm_state = a.ssm_state;
+  const gdn_decode_weights* w = a.w;
+  p->w_in = (const __nv_bfloat16*)w->input_norm_w;
+  p->w_qkvz = (const __nv_bfloat16*)w->qkvz;
+  p->w_qkvz_scales = w->qkvz_scales;
+  p->fp4 = c.qkvz_format == GDN_W_MXFP4;
+  p->w_ba = (const __nv_bfloat16*)w->ba;
+  p->conv_w = (const __nv_bfloat16*)w->conv_w;
+  p->A_log = w->A_log;
+  p->dt_bias = (const __nv_bfloat16*)w->dt_bias;
+  p->gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
+  p->ctr = (WsCounters*)(base + lay.ctr);
+  p->norm_part = (unsigned long long*)(base + lay.norm_part);
+  p->xn = (__nv_bfloat16*)(base + lay.xn);
+  p->proj_part = (unsigned long long*)(base + lay.proj_part);
+  p->plan = (const PlanDev*)(base + lay.plan);
+}
+
+bool weight_maps(const gdn_decode_config& c, const gdn_decode_weights* w, MapCache* m, StepParams* p) {
+  if (m->qkvz_ptr != w->qkvz || m->ba_ptr != w->ba) {
+    if (!encode_maps(c, w, &m->qkvz, &m->ba)) {
+      m->qkvz_ptr = m->ba_ptr = nullptr;
+      return false;
+    }
+    m->qkvz_ptr = w->qkvz;
+    m->ba_ptr = w->ba;
+  }
+  p->tm_qkvz = m->qkvz;
+  p->tm_ba = m->ba;
+  return true;
+}
+
+// One launch of the step kernel. Programmatic stream serialisation (while
+// *pdl): the launch may start while the previous kernel in the stream
+// finishes; the kernel reads only the weights it streams and the plan
+// before its griddepcontrol.wait, or nothing with
+// GDN_LAUNCH_NO_EARLY_WEIGHTS. Cooperative (on request): every CTA resident
+// at once, guaranteed by the runtime. If the runtime refuses programmatic
+// serialisation, *pdl is cleared and the launch goes without it.
+gdn_status launch_step(const gdn_decode_config& c, const Plan& pl, bool* pdl, const StepParams& p, bool has_res,
+                       cudaStream_t s) {
+  const void* kern = pick_kernel(c, pl.engine, has_res);
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(pl.G);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = kernel_smem(pl);
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (c.launch_flags & GDN_LAUNCH_COOPERATIVE) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
+  if (*pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  lc.attrs = attr;
+  lc.numAttrs = na;
+  void* args[] = {const_cast<StepParams*>(&p)};
+  cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
+  if (e != cudaSuccess && *pdl) {
+    (void)cudaGetLastError();
+    *pdl = false;
+    lc.numAttrs = na - 1;
+    e = cudaLaunchKernelExC(&lc, kern, args);
+  }
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -388,7 +536,6 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
   gdn_decode* h = new (std::nothrow) gdn_decode;
   if (!h) return GDN_ERR_ARG;
   h->cfg = *cfg;
-  h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
   h->pdl = true;
   if (h->cfg.deadline_us == 0) h->cfg.deadline_us = 200000;
   int G;
@@ -451,118 +598,14 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
                            const gdn_decode_weights* w, const int32_t* state_indices,
                            void* conv_state, void* ssm_state, void* core_out, void* residual_out,
                            void* stream) {
-  if (!h || !w) return GDN_ERR_ARG;
-  const gdn_decode_config& c = h->cfg;
-  if (rows < 1 || rows > c.max_rows) return GDN_ERR_ARG;
-  if (!x || !state_indices || !conv_state || !ssm_state || !core_out || !residual_out) return GDN_ERR_ARG;
-  if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
-    return GDN_ERR_ARG;
-  if (c.qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
-  const void* a16[] = {x, residual, core_out, residual_out, conv_state, ssm_state, w->input_norm_w,
-                       w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
-  for (const void* p : a16)
-    if (p && !aligned(p, 16)) return GDN_ERR_ARG;
-  if (!aligned(state_indices, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
-  const size_t H = (size_t)c.hidden;
-  const size_t xb = (size_t)rows * H * 2;
-  const size_t coreb = (size_t)rows * c.num_v_heads * c.head_v_dim * 2;
-  const size_t sdt = c.ssm_dtype == GDN_STATE_BF16 ? 2 : 4;
-  const size_t ssmb = (size_t)c.num_slots * c.num_v_heads * c.head_v_dim * c.head_k_dim * sdt;
-  const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
-  struct Rg { const void* p; size_t n; };
-  const Rg ins[] = {{x, xb}, {residual, residual ? xb : 0}, {state_indices, (size_t)rows * 4},
-                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
-                    {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
-                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
-                    {h->ws, h->lay.total}};
-  const Rg outs[] = {{core_out, coreb}, {residual_out, xb}};
-  for (const Rg& o : outs)
-    for (const Rg& i : ins)
-      if (overlaps(o.p, o.n, i.p, i.n)) return GDN_ERR_ARG;
-  if (overlaps(core_out, coreb, residual_out, xb)) return GDN_ERR_ARG;
-  if (overlaps(conv_state, convb, ssm_state, ssmb)) return GDN_ERR_ARG;
-
-  const Plan& pl = h->plan;
-  StepParams* p = new (std::nothrow) StepParams;
-  if (!p) return GDN_ERR_ARG;
-  memset(p, 0, sizeof(*p));
-  p->H = c.hidden; p->Hk = c.num_k_heads; p->Hv = c.num_v_heads;
-  p->dk = c.head_k_dim; p->dv = c.head_v_dim; p->C = n_conv(c);
-  p->Nqkvz = n_qkvz(c); p->Nba = n_ba(c); p->num_slots = c.num_slots; p->rows = rows;
-  p->group = c.num_v_heads / c.num_k_heads;
-  set_plan_params(pl, p);
-  p->norm_eps = c.norm_eps; p->gnorm_eps = c.gated_norm_eps; p->l2_eps = c.l2_eps; p->q_scale = c.q_scale;
-  p->deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
-  p->debug_flags = c.debug_flags;
-  p->x = (const __nv_bfloat16*)x;
-  p->res = (const __nv_bfloat16*)residual;
-  p->res_out = (__nv_bfloat16*)residual_out;
-  p->core_out = (__nv_bfloat16*)core_out;
-  p->idx = state_indices;
-  p->conv_state = (__nv_bfloat16*)conv_state;
-  p->ssm_state = ssm_state;
-  p->w_in = (const __nv_bfloat16*)w->input_norm_w;
-  p->w_qkvz = (const __nv_bfloat16*)w->qkvz;
-  p->w_qkvz_scales = w->qkvz_scales;
-  p->fp4 = c.qkvz_format == GDN_W_MXFP4;
-  p->w_ba = (const __nv_bfloat16*)w->ba;
-  p->conv_w = (const __nv_bfloat16*)w->conv_w;
-  p->A_log = w->A_log;
-  p->dt_bias = (const __nv_bfloat16*)w->dt_bias;
-  p->gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
-  char* base = (char*)h->ws;
-  p->ctr = (WsCounters*)(base + h->lay.ctr);
-  p->norm_part = (unsigned long long*)(base + h->lay.norm_part);
-  p->xn = (__nv_bfloat16*)(base + h->lay.xn);
-  p->proj_part = (unsigned long long*)(base + h->lay.proj_part);
-  p->plan = (const PlanDev*)(base + h->lay.plan);
-  // weight tile maps (cached for the last weights seen)
-  if (h->map_qkvz_ptr != w->qkvz || h->map_ba_ptr != w->ba) {
-    if (!encode_maps(c, w, &h->map_qkvz, &h->map_ba)) {
-      h->map_qkvz_ptr = h->map_ba_ptr = nullptr;
-      delete p;
-      return GDN_ERR_CUDA;
-    }
-    h->map_qkvz_ptr = w->qkvz;
-    h->map_ba_ptr = w->ba;
-  }
-  p->tm_qkvz = h->map_qkvz;
-  p->tm_ba = h->map_ba;
-
-  const void* kern = pick_kernel(c, pl.engine, residual != nullptr);
-  cudaLaunchConfig_t lc;
-  memset(&lc, 0, sizeof(lc));
-  lc.gridDim = dim3(pl.G);
-  lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = kernel_smem(pl);
-  lc.stream = (cudaStream_t)stream;
-  // Programmatic stream serialisation: the launch may start while the
-  // previous launch in the stream finishes; the kernel reads nothing but the
-  // weights before its griddepcontrol.wait. Cooperative (on request): every
-  // CTA resident at once, guaranteed by the runtime.
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (c.launch_flags & GDN_LAUNCH_COOPERATIVE) {
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na++].val.cooperative = 1;
-  }
-  if (h->pdl) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na++].val.programmaticStreamSerializationAllowed = 1;
-  }
-  lc.attrs = attr;
-  lc.numAttrs = na;
-  void* args[] = {p};
-  cudaError_t e = cudaLaunchKernelExC(&lc, kern, args);
-  if (e != cudaSuccess && h->pdl) {
-    // the runtime refused programmatic serialisation here: launch without it
-    (void)cudaGetLastError();
-    h->pdl = false;
-    lc.numAttrs = na - 1;
-    e = cudaLaunchKernelExC(&lc, kern, args);
-  }
-  delete p;
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  if (!h) return GDN_ERR_ARG;
+  const StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
+  gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
+  if (st != GDN_OK) return st;
+  StepParams p;  // on the stack: the step allocates nothing
+  fill_params(h->cfg, h->plan, h->lay, (char*)h->ws, a, &p);
+  if (!weight_maps(h->cfg, w, &h->maps, &p)) return GDN_ERR_CUDA;
+  return launch_step(h->cfg, h->plan, &h->pdl, p, residual != nullptr, (cudaStream_t)stream);
 }
 
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail) {
@@ -596,22 +639,18 @@ gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows, int32_t* 
   return GDN_OK;
 }
 
-gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
-                                     int32_t cta_cap, uint64_t* tile_stamps, int32_t tile_cap,
-                                     int32_t* num_ctas, int32_t* num_tiles) {
-  if (!h || !cta_stamps || !tile_stamps || !num_ctas || !num_tiles) return GDN_ERR_ARG;
-  const int G = h->plan.G, T = h->plan.num_tiles;
-  if (cta_cap < G * kTlSlots || tile_cap < T * 2) return GDN_ERR_ARG;
+gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps, int32_t cta_cap,
+                                     int32_t* num_ctas) {
+  if (!h || !cta_stamps || !num_ctas) return GDN_ERR_ARG;
+  const int G = h->plan.G;
+  if (cta_cap < G * kTlSlots) return GDN_ERR_ARG;
   const char* base = (const char*)h->ws + h->lay.ctr;
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemcpyAsync(cta_stamps, base + offsetof(WsCounters, tl_cta), sizeof(uint64_t) * G * kTlSlots,
                       cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(tile_stamps, base + offsetof(WsCounters, tl_tile), sizeof(uint64_t) * T * 2,
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return GDN_ERR_CUDA;
   *num_ctas = G;
-  *num_tiles = T;
   return GDN_OK;
 }
 
@@ -665,29 +704,58 @@ namespace {
 
 constexpr int kStaticMaxDevices = 32;
 
+// The unique id of the CUDA context current on this thread (0 if none), from
+// the driver, looked up once. Ids are never reused within a process, so a
+// set-up keyed on one cannot outlive its context (cudaDeviceReset, or
+// another context made current).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (CtxGetCurrentFn)f;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (CtxGetIdFn)f;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 struct StaticDevice {
-  bool ready;                // set up for `cfg`
+  bool ready;                // set up for `cfg` in context `ctx_id`
+  unsigned long long ctx_id; // the context the scratch address belongs to
   gdn_decode_config cfg;     // the caller's config the scratch is set up for
   gdn_decode_config run;     // the same with defaults filled in
-  void* scratch;             // this device's address of g_static_scratch
+  void* scratch;             // this context's device address of g_static_scratch
   Layout lay;
   Plan plan;
   PlanDev staging;           // host image of the plan tables
-  const void* map_qkvz_ptr;  // weights the cached tile maps describe
-  const void* map_ba_ptr;
-  CUtensorMap map_qkvz;
-  CUtensorMap map_ba;
+  bool pdl;                  // launch with programmatic stream serialisation
+  MapCache maps;             // weights the cached tile maps describe
 };
 StaticDevice g_static[kStaticMaxDevices];
 
-// Set the current device's scratch up for `cfg` unless it already is:
-// validate, plan, zero the counters and the error word and copy the plan
-// tables in, ordered on `stream`.
+// Set the current device's scratch up for `cfg` unless it already is in the
+// current context: validate, plan, look up the scratch address, zero the
+// counters, the error word and the partials, and copy the plan tables in,
+// ordered on `stream`.
 gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stream, StaticDevice** out) {
   if (dev < 0 || dev >= kStaticMaxDevices) return GDN_ERR_UNSUPPORTED;
   StaticDevice& d = g_static[dev];
   *out = &d;
-  if (d.ready && memcmp(&d.cfg, cfg, sizeof(*cfg)) == 0) return GDN_OK;
+  const unsigned long long ctx = current_context_id();
+  if (d.ready && ctx != 0 && ctx == d.ctx_id && memcmp(&d.cfg, cfg, sizeof(*cfg)) == 0) return GDN_OK;
   d.ready = false;
   gdn_status st = validate(cfg);
   if (st != GDN_OK) return st;
@@ -711,11 +779,12 @@ gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stre
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess || per_sm < 1)
       return GDN_ERR_UNSUPPORTED;
   }
-  if (!d.scratch) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return GDN_ERR_CUDA;
-    d.scratch = ptr;
-  }
+  // the address of this context's copy of the array (the runtime has made a
+  // context current by now)
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return GDN_ERR_CUDA;
+  d.scratch = ptr;
+  d.ctx_id = current_context_id();
   PlanDev& pd = d.staging;
   memset(&pd, 0, sizeof(pd));
   memcpy(pd.unit_begin, d.plan.unit_begin, sizeof(int) * (d.plan.G + 1));
@@ -729,9 +798,10 @@ gdn_status static_setup(int dev, const gdn_decode_config* cfg, cudaStream_t stre
   if (!clear_launch_state(base, d.lay, stream) ||
       cudaMemcpyAsync(base + d.lay.plan, &pd, sizeof(PlanDev), cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return GDN_ERR_CUDA;
-  d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
+  d.maps = MapCache();
+  d.pdl = true;
   d.cfg = *cfg;
-  d.ready = true;
+  d.ready = d.ctx_id != 0;
   return GDN_OK;
 }
 
@@ -744,110 +814,25 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
                                              uint32_t* detail) {
   if (!cfg || !w) return GDN_ERR_ARG;
   if (rows < 1 || rows > cfg->max_rows || cfg->max_rows > kMaxRows) return GDN_ERR_ARG;
-  if (!x || !state_indices || !conv_state || !ssm_state || !core_out || !residual_out) return GDN_ERR_ARG;
-  if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
-    return GDN_ERR_ARG;
-  if (cfg->qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
-  const void* a16[] = {x, residual, core_out, residual_out, conv_state, ssm_state, w->input_norm_w,
-                       w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
-  for (const void* p : a16)
-    if (p && !aligned(p, 16)) return GDN_ERR_ARG;
-  if (!aligned(state_indices, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
+  // argument errors come back before any CUDA call
+  const StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
+  gdn_status st = check_step_args(*cfg, a, nullptr, 0);
+  if (st != GDN_OK) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   const cudaStream_t s = (cudaStream_t)stream;
   StaticDevice* dp = nullptr;
-  gdn_status st = static_setup(dev, cfg, s, &dp);
+  st = static_setup(dev, cfg, s, &dp);
   if (st != GDN_OK) return st;
   StaticDevice& d = *dp;
-  const gdn_decode_config& c = d.run;
-  const size_t H = (size_t)c.hidden;
-  const size_t xb = (size_t)rows * H * 2;
-  const size_t coreb = (size_t)rows * c.num_v_heads * c.head_v_dim * 2;
-  const size_t sdt = c.ssm_dtype == GDN_STATE_BF16 ? 2 : 4;
-  const size_t ssmb = (size_t)c.num_slots * c.num_v_heads * c.head_v_dim * c.head_k_dim * sdt;
-  const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
-  struct Rg { const void* p; size_t n; };
-  const Rg ins[] = {{x, xb}, {residual, residual ? xb : 0}, {state_indices, (size_t)rows * 4},
-                    {conv_state, convb}, {ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
-                    {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
-                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
-                    {d.scratch, d.lay.total}};
-  const Rg outs[] = {{core_out, coreb}, {residual_out, xb}};
-  for (const Rg& o : outs)
-    for (const Rg& i : ins)
-      if (overlaps(o.p, o.n, i.p, i.n)) return GDN_ERR_ARG;
-  if (overlaps(core_out, coreb, residual_out, xb)) return GDN_ERR_ARG;
-  if (overlaps(conv_state, convb, ssm_state, ssmb)) return GDN_ERR_ARG;
-
-  const Plan& pl = d.plan;
+  st = check_step_args(d.run, a, d.scratch, d.lay.total);  // now also against the scratch
+  if (st != GDN_OK) return st;
   StepParams p;
-  memset(&p, 0, sizeof(p));
-  p.H = c.hidden; p.Hk = c.num_k_heads; p.Hv = c.num_v_heads;
-  p.dk = c.head_k_dim; p.dv = c.head_v_dim; p.C = n_conv(c);
-  p.Nqkvz = n_qkvz(c); p.Nba = n_ba(c); p.num_slots = c.num_slots; p.rows = rows;
-  p.group = c.num_v_heads / c.num_k_heads;
-  set_plan_params(pl, &p);
-  p.norm_eps = c.norm_eps; p.gnorm_eps = c.gated_norm_eps; p.l2_eps = c.l2_eps; p.q_scale = c.q_scale;
-  p.deadline_ns = (unsigned long long)c.deadline_us * 1000ull;
-  p.debug_flags = c.debug_flags;
-  p.x = (const __nv_bfloat16*)x;
-  p.res = (const __nv_bfloat16*)residual;
-  p.res_out = (__nv_bfloat16*)residual_out;
-  p.core_out = (__nv_bfloat16*)core_out;
-  p.idx = state_indices;
-  p.conv_state = (__nv_bfloat16*)conv_state;
-  p.ssm_state = ssm_state;
-  p.w_in = (const __nv_bfloat16*)w->input_norm_w;
-  p.w_qkvz = (const __nv_bfloat16*)w->qkvz;
-  p.w_qkvz_scales = w->qkvz_scales;
-  p.fp4 = c.qkvz_format == GDN_W_MXFP4;
-  p.w_ba = (const __nv_bfloat16*)w->ba;
-  p.conv_w = (const __nv_bfloat16*)w->conv_w;
-  p.A_log = w->A_log;
-  p.dt_bias = (const __nv_bfloat16*)w->dt_bias;
-  p.gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
   char* base = (char*)d.scratch;
-  p.ctr = (WsCounters*)(base + d.lay.ctr);
-  p.norm_part = (unsigned long long*)(base + d.lay.norm_part);
-  p.xn = (__nv_bfloat16*)(base + d.lay.xn);
-  p.proj_part = (unsigned long long*)(base + d.lay.proj_part);
-  p.plan = (const PlanDev*)(base + d.lay.plan);
-  if (d.map_qkvz_ptr != w->qkvz || d.map_ba_ptr != w->ba) {
-    if (!encode_maps(c, w, &d.map_qkvz, &d.map_ba)) {
-      d.map_qkvz_ptr = d.map_ba_ptr = nullptr;
-      return GDN_ERR_CUDA;
-    }
-    d.map_qkvz_ptr = w->qkvz;
-    d.map_ba_ptr = w->ba;
-  }
-  p.tm_qkvz = d.map_qkvz;
-  p.tm_ba = d.map_ba;
-
-  cudaLaunchConfig_t lc;
-  memset(&lc, 0, sizeof(lc));
-  lc.gridDim = dim3(pl.G);
-  lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = kernel_smem(pl);
-  lc.stream = s;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (c.launch_flags & GDN_LAUNCH_COOPERATIVE) {
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na++].val.cooperative = 1;
-  }
-  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[na++].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = na;
-  void* args[] = {&p};
-  const void* kern = pick_kernel(c, pl.engine, residual != nullptr);
-  if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
-    (void)cudaGetLastError();  // without programmatic serialisation
-    lc.numAttrs = na - 1;
-    if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) return GDN_ERR_CUDA;
-  }
-  if (!detail) return GDN_OK;
+  fill_params(d.run, d.plan, d.lay, base, a, &p);
+  if (!weight_maps(d.run, w, &d.maps, &p)) return GDN_ERR_CUDA;
+  st = launch_step(d.run, d.plan, &d.pdl, p, residual != nullptr, s);
+  if (st != GDN_OK || !detail) return st;
 
   uint32_t word = 0;
   const char* err = base + d.lay.ctr + offsetof(WsCounters, error);

@@ -49,9 +49,8 @@ struct WsCounters {
   // that makes the count a multiple of G is the group's last reader
   unsigned int conv_group[kMaxRows][kMaxKHeads];
   // Debug timeline (kDebugTimeline): %globaltimer stamps per CTA at phase
-  // boundaries (tl_tile is no longer written and reads as zeros).
+  // boundaries.
   unsigned long long tl_cta[kMaxCtas][kTlSlots];
-  unsigned long long tl_tile[kMaxTiles][2];
 };
 
 // Timeline stamp points of a CTA.
@@ -78,6 +77,7 @@ struct StepParams {
   float norm_eps, gnorm_eps, l2_eps, q_scale;
   unsigned long long deadline_ns;
   int debug_flags;
+  int early_weights;   // stream the weights (and read the plan) before griddepcontrol.wait
   // step tensors
   const __nv_bfloat16* x;
   const __nv_bfloat16* res;   // nullptr: first layer

@@ -704,6 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   uint8_t* sPad = sX + (size_t)(p.fp4 ? 2 : 1) * p.xslots * kXBytes;  // read past the windows; scratch
   uint8_t* sWin = sPad + p.xpad;
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
+  // Without early weight reads nothing is read before the previous kernel in
+  // the stream is done (the caller's kernel just before may write weights).
+  if (!p.early_weights) griddep_wait();
   const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
 
   if (tid == 0) {
@@ -738,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const int first = min(issued, kFirstTiles);
   if (tid == 32) start_weight_stream<FP4>(p, ts, sW, sR, ub, 0, first);
   const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
-  griddep_wait();  // from here on the previous step's writes are visible
+  griddep_wait();  // from here on the previous kernel's writes are visible (a no-op if already waited)
   griddep_launch_dependents();
   if (tid == 0) {
     sm.flag = (ld_relaxed_u32(&p.ctr->error) == 0);

@@ -83,22 +83,32 @@ typedef enum {
   GDN_ENGINE_TCGEN05 = 2     /* tcgen05.mma, TMEM accumulators, TMA-fed operands */
 } gdn_engine;
 
-/* Test hooks (debug_flags). Never set in production. */
-#define GDN_DEBUG_SKIP_NORM_PUBLISH 0x1 /* CTA 0 never publishes its norm partials,
-                                           so every CTA's first wait runs out */
-#define GDN_DEBUG_TIMELINE 0x2          /* record %globaltimer stamps of each CTA's
-                                           phases (read with gdn_decode_debug_timeline) */
-
-/* Launch options (launch_flags). By default a step is an ordinary launch
- * with programmatic stream serialisation: a step's CTAs start as soon as
- * SMs free up at the end of the previous step in the stream, and stream the
- * step's weights before the previous step's results are needed. The step's
- * CTAs wait on one another, so all of them must be resident at once; create
- * checks that one CTA per SM fits. If other work holds SMs while a step runs,
- * its bounded waits run out and it reports GDN_ERR_DEADLINE (it cannot hang).
- * GDN_LAUNCH_COOPERATIVE makes the runtime guarantee co-residency instead
- * (cooperative launch), at the cost of that overlap. */
+/* Launch options (launch_flags).
+ *
+ * By default a step is an ordinary launch with programmatic stream
+ * serialisation: its CTAs start as soon as SMs free up at the end of the
+ * kernel before it in the stream, and they begin streaming the step's
+ * weights (in_proj_qkvz, in_proj_ba and the input-norm weight) and reading
+ * the handle's plan tables BEFORE that kernel has finished. Only those
+ * reads come early; x, residual, state_indices, the states and every other
+ * weight are read after the previous kernel's writes are visible. So by
+ * default the caller must not have the kernel launched just before the
+ * step, in the same stream, write those weights (a weight load, update or
+ * quantisation kernel, a copy_ into the weight tensor): the step could read
+ * the old values. A copy engine operation, an event wait or any
+ * non-kernel operation in between restores the ordering, and so does
+ * GDN_LAUNCH_NO_EARLY_WEIGHTS, which makes the step read nothing before the
+ * previous kernel is done (it keeps the overlapped launch otherwise; it costs
+ * the overlap of the first weight tiles with that kernel's tail).
+ *
+ * The step's CTAs wait on one another, so all of them must be resident at
+ * once; create checks that one CTA per SM fits. If other work holds SMs
+ * while a step runs, its bounded waits run out and it reports
+ * GDN_ERR_DEADLINE (it cannot hang). GDN_LAUNCH_COOPERATIVE makes the
+ * runtime guarantee co-residency instead (cooperative launch), at the cost
+ * of the overlap between consecutive steps. */
 #define GDN_LAUNCH_COOPERATIVE 0x1
+#define GDN_LAUNCH_NO_EARLY_WEIGHTS 0x2
 
 typedef struct {
   int32_t hidden;
@@ -118,7 +128,7 @@ typedef struct {
   float q_scale;           /* multiplies the L2-normalised q */
   uint32_t deadline_us;    /* bound of every cross-CTA wait; 0 = 200000 */
   int32_t num_ctas;        /* persistent grid size; 0 = one CTA per SM */
-  int32_t debug_flags;     /* GDN_DEBUG_*; 0 in production */
+  int32_t debug_flags;     /* test hooks (gdn_decode_diag.h); 0 in production */
   int32_t launch_flags;    /* GDN_LAUNCH_*; 0 = overlapped launches */
 } gdn_decode_config;
 
@@ -138,21 +148,35 @@ typedef struct gdn_decode gdn_decode_t;
 /* Device bytes the caller must provide as the workspace for this config
  * (counters, the sticky error word, the plan tables, norm and projection
  * partials, and for the CUDA-core engine the normed input image). 0 if the
- * config is invalid or unsupported. */
+ * config is invalid or unsupported. The workspace holds what the pages'
+ * runtime helpers keep per launch key: the scratch of the cross-CTA
+ * hand-offs and the health word (vLLM #60833, Details, "Shared helpers":
+ * launch ABI and health words, a tagged mailbox with bounded waits). */
 size_t gdn_decode_workspace_bytes(const gdn_decode_config* cfg);
 
 /* Validate the config for the current device, bind the caller's workspace
  * (device memory of at least gdn_decode_workspace_bytes(cfg) bytes, 256-byte
  * aligned; it stays owned by the caller and must outlive the handle) and zero
- * it asynchronously on `stream`. The handle holds host state only.
- * Returns GDN_ERR_ARG / GDN_ERR_UNSUPPORTED / GDN_ERR_CUDA on failure. */
+ * it asynchronously on `stream`. The handle holds host state only: the
+ * shapes, the stream-K plan of the projection units (written once into the
+ * workspace) and the weight tile maps. It stands for one build key of the
+ * pages' launch (one persistent launch per GDN layer front with its layer
+ * shape, state dtype and first-layer variant; sgl-amd-mono #89,
+ * Modifications, gdn.py and spec.py rows; vLLM #60833, Details,
+ * "Launches"). Returns GDN_ERR_ARG / GDN_ERR_UNSUPPORTED / GDN_ERR_CUDA on
+ * failure; a config outside the shapes this build runs is refused up front
+ * with GDN_ERR_UNSUPPORTED, as the pages refuse configurations at start-up
+ * (sgl-amd-mono #89, "Refusals"). */
 gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace,
                              size_t workspace_bytes, void* stream,
                              gdn_decode_t** out);
 
-/* Run one decode step of `rows` rows (1..max_rows) as one launch on `stream`.
- * Asynchronous and stream-ordered; allocates nothing; may be captured in a
- * CUDA graph. residual == NULL selects the first-layer variant (r = x).
+/* Run one decode step of `rows` rows (1..max_rows) as one launch on `stream`
+ * (the step list at the top of this header). Asynchronous and
+ * stream-ordered; allocates no memory on the host or the device; may be
+ * captured in a CUDA graph. residual == NULL selects the first-layer variant
+ * (r = x). See "Launch options" for the weights it reads before the previous
+ * kernel in the stream has finished.
  * Reads x, residual, weights, state_indices; writes residual_out and core_out
  * and updates the rows' conv_state and ssm_state slots in place. Outputs must
  * not overlap any input. state_indices must be distinct among non-pad rows.
@@ -166,12 +190,20 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
 /* Synchronise `stream` and read the sticky error word. Returns GDN_OK, or the
  * recorded device status; *detail (optional) receives the raw word:
  * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
- * 3 projection tile, 4 a tensor-core pipeline stage), 15..0 the CTA
- * (deadline) or row (index error). */
+ * 3 projection tile, 4 a tensor-core pipeline stage, 5 a recurrence state
+ * tile), 15..0 the CTA (deadline) or row (index error). This is the host
+ * side of the pages' failure design: every wait in the launch is bounded, a
+ * CTA that gives up records which wait in a sticky failed word, and the host
+ * reads that word after the step without a fallback path (vLLM #60833,
+ * Details, "Limitations / follow-ups"; sgl-amd-mono #89, Kernel checks,
+ * "fault at the first wait"). */
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail);
 
 /* Clear the error word, all counters and the partial buffers of the
- * workspace on `stream` (the plan stays). */
+ * workspace on `stream` (the plan stays). Until then every step on the
+ * handle returns at once on the device, as a launch does once the pages'
+ * sticky failed word is set (vLLM #60833, Details, "Limitations /
+ * follow-ups"). */
 gdn_status gdn_decode_reset(gdn_decode_t* h, void* stream);
 
 /* Free the host handle. The workspace stays the caller's. */
@@ -183,38 +215,6 @@ const char* gdn_status_string(gdn_status s);
  * (diagnostics for tests and benchmarks). */
 gdn_status gdn_decode_launch_info(const gdn_decode_t* h, int32_t rows,
                                   int32_t* num_ctas, int32_t* engine);
-
-/* Diagnostics: synchronise `stream` and copy the phase timeline the last
- * step recorded (handle created with GDN_DEBUG_TIMELINE). cta_stamps receives
- * num_ctas x 48 uint64 nanosecond stamps: 0 start (after the previous step),
- * 1 norm partials out, 2 norm sums in (rstd known), 3 normed input out
- * (CUDA-core engine), 4 projection start, 5 projection end, 6 the first
- * recurrence task's projection partials in, 7 end, 8 that task's inputs
- * done, 9 first MMA, 10 last MMA done, 11 first weight tiles issued,
- * 12 x and residual staged, 13 that task's state written; 32+n the n-th
- * weight tile issued (n < 16, tensor-core engine); other slots unused.
- * tile_stamps receives num_tiles x 2 zeros (kept for the layout of this
- * call). Capacities are in elements; *num_ctas and *num_tiles receive the
- * sizes. */
-gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,
-                                     int32_t cta_cap, uint64_t* tile_stamps, int32_t tile_cap,
-                                     int32_t* num_ctas, int32_t* num_tiles);
-
-/* Host-only diagnostics of the stream-K split of the projection work units
- * (no device call) for a grid of num_ctas CTAs. A unit is one 64-column step
- * (k-step) of one 256-row projection tile (tiles: in_proj_qkvz rows first,
- * then in_proj_ba rows); units are ordered by group g = (k-block g / T,
- * tile g % T) of `kblock` k-steps. Fills *engine (the engine the config runs
- * with), unit_begin[num_ctas+1] (CTA c takes units [unit_begin[c],
- * unit_begin[c+1])), seg_slot[num_ctas][16] (partial slot of the i-th group
- * CTA c touches), ks_first[num_ctas] and nb_slots[num_ctas] (CTA c keeps the
- * normed input of k-steps ks_first[c] + j mod ksteps, j < nb_slots[c]),
- * tile_count[*num_tiles] (partials per tile; capacity tile_cap), *ksteps and
- * *kblock. Errors as for gdn_decode_create. */
-gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* engine,
-                           int32_t* unit_begin, uint8_t* seg_slot, uint16_t* ks_first, uint8_t* nb_slots,
-                           uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
-                           int32_t* kblock);
 
 /* Largest scratch gdn_decode_step_static can use, in bytes (8 MiB). */
 #define GDN_STATIC_SCRATCH_BYTES (8u << 20)
@@ -232,15 +232,18 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
  * GPU that loads the library's device code until the process exits. The call
  * allocates nothing on the host or the device, through no API or library.
  *
- * Set-up: the first call on a device (with that device current), and every
- * later call whose *cfg differs from the previous call's on that device,
- * first validates the config, looks up the scratch array's device address,
- * zeroes its counters, error word and partial buffers, and copies the plan
- * tables into it, stream-ordered on `stream`. They must start at zero: a
- * launch takes its number from a counter that grows from zero, and a partial
- * word carries the number of the launch that wrote it, so with the counters
- * back at zero an old word would pass for a new one. That first call must
- * come before any stream capture on `stream`.
+ * Set-up: the first call on a device (with that device current), every
+ * later call whose *cfg differs from the previous call's on that device, and
+ * the first call in a new CUDA context on the device (after cudaDeviceReset,
+ * or with another context current: the library keys its set-up on the
+ * context's unique id, so it never reuses an address of a context that is
+ * gone) first validates the config, looks up the scratch array's device
+ * address, zeroes its counters, error word and partial buffers, and copies
+ * the plan tables into it, stream-ordered on `stream`. They must start at
+ * zero: a launch takes its number from a counter that grows from zero, and a
+ * partial word carries the number of the launch that wrote it, so with the
+ * counters back at zero an old word would pass for a new one. A call that
+ * does the set-up must come before any stream capture on `stream`.
  *
  * Arguments, layouts and the launch are those of gdn_decode_step; `cfg` takes
  * the place of the handle. The scratch is shared by every call on a device:
@@ -256,7 +259,12 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
  * in the scratch as for a handle: if `detail` is not NULL the call waits for
  * its launch, stores the error word in *detail (layout of gdn_decode_check),
  * returns its status, and if it is non-zero clears the word, the counters
- * and the partial buffers so the next call runs. With detail == NULL the call does not synchronise. */
+ * and the partial buffers so the next call runs. With detail == NULL the
+ * call does not synchronise and nothing reads the word: once a device error
+ * is set, that call and every later one return at once on the device
+ * without writing their outputs or states, until a call with detail != NULL
+ * reads and clears it. A caller that passes NULL for speed should pass
+ * detail on some calls (every N-th step, say) to find such an error. */
 gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32_t rows, const void* x,
                                   const void* residual, const gdn_decode_weights* w,
                                   const int32_t* state_indices, void* conv_state,

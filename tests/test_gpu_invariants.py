@@ -69,15 +69,17 @@ def test_batch_invariance():
 
 
 def test_graph_replay_matches_eager():
-    """Widths 8, 1, 3, 8, 2, 5 captured in one CUDA graph on one state, replayed;
-    every output bit-equal to the same sequence run eagerly."""
+    """Widths 8, 1, 3, 8, 2, 5 captured in one CUDA graph on one state, replayed
+    200 times (the replay count of sgl-amd-mono #89, Kernel checks); every
+    output and the final states bit-equal to the same sequence run eagerly
+    200 times."""
     shape = WL.SHARD
     widths = [8, 1, 3, 8, 2, 5]
     base = Case(shape, 8, 6300)
     steps = [WL.make_step(shape, w, 6400 + i) for i, w in enumerate(widths)]
     dw = {k: (v.cuda() if v is not None else None) for k, v in base.w.items()}
     xs = [(s["x"].cuda(), s["residual"].cuda(), s["state_indices"].cuda()) for s in steps]
-    reps = 20
+    reps = 200
 
     def run(graph):
         conv = base.st["conv_state"].cuda()
@@ -178,3 +180,30 @@ def test_host_argument_errors():
         layer.step(case.dx, case.dres, case.dw, case.didx, case.dconv, case.dssm,
                    core_out=case.dssm.view(torch.bfloat16).view(-1)[:4 * 512].view(4, 512))
     assert layer.check()[0] == 0  # nothing was launched
+
+
+def test_no_early_weights_sees_weights_written_by_the_kernel_just_before():
+    """With GDN_LAUNCH_NO_EARLY_WEIGHTS the step reads nothing before the
+    kernel launched just before it in the stream has finished. Torch kernels
+    (dtype-converting copies, so they run as kernels rather than copy-engine
+    transfers) overwrite in_proj_qkvz, in_proj_ba and the input-norm weight
+    right before each step; every step matches the oracle on the new weights."""
+    shape = WL.SHARD
+    case = Case(shape, 4, 6800).to_device()
+    layer = GdnDecode(shape, launch_flags=_native.GDN_LAUNCH_NO_EARLY_WEIGHTS)
+    fresh = WL.make_weights(shape, 6801)
+    src = {k: fresh[k].float().cuda() for k in ("qkvz", "ba", "input_norm_w")}
+    # a first step on the old weights (tile maps encoded, module warm)
+    case.run_gpu(layer)
+    conv0, ssm0 = case.st["conv_state"].cuda(), case.st["ssm_state"].cuda()
+    case.dconv.copy_(conv0)
+    case.dssm.copy_(ssm0)
+    torch.cuda.synchronize()
+    for k, t in src.items():
+        case.dw[k].copy_(t)  # f32 -> bf16: a kernel, launched just before the step
+    core, res = layer.step(case.dx, case.dres, case.dw, case.didx, case.dconv, case.dssm)
+    torch.cuda.synchronize()
+    assert layer.check()[0] == 0
+    for k in src:
+        case.w[k] = fresh[k]
+    compare(case, case.run_oracle(), core, res)

@@ -1,11 +1,12 @@
 """CUDA path (through the C ABI) against the CPU oracle, element by element,
 on seeded synthetic layers of every workload shape: widths 1..16, pad rows,
 the first-layer variant and the bf16 state."""
+import numpy as np
 import pytest
 import torch
 
 from gated_deltanet_layer_gb300 import GdnDecode, workloads as WL
-from gdn_harness import Case, compare
+from gdn_harness import Case, compare, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -73,12 +74,47 @@ def test_full_layer(rows, engine):
 
 
 # Stress case: conv weights ~N(0, 0.5) (25x the recipe's) make the v path and
-# the state update matter. A projection output that rounds to the other
-# neighbouring bf16 value than the oracle's (one ulp, up to 2^-5 for |p| in
-# [4, 8)) then moves v by |w3| * ulp ~ 0.5 * 0.03 and the state by
-# |k_i| * beta * dv ~ 0.09 * 0.015 ~ 1.4e-3, past the 1e-3 bar of the
-# recipe's inputs; this case uses 5e-3 for the f32 state.
+# the state update matter. A projection output that the kernel's f32 sum
+# rounds to the other bf16 neighbour than the oracle's exact sum (one ulp, up
+# to 2^-5 for |p| in [4, 8)) then moves v by |w3| * ulp ~ 0.5 * 0.03 and the
+# state by |k_i| * beta * that ~ 1.4e-3, past the 1e-3 bar of the recipe's
+# inputs. The test shows that this is the only source of the excess: with
+# the kernel's own q, k, v projection values (read back from the new conv
+# taps, each within one bf16 ulp of the oracle's) fed through the oracle's
+# conv, norms, gates and delta rule, the kernel's f32 state is within the
+# 1e-3 bar; end to end it is within 5e-3.
 STRESS_STATE_TOL = 5e-3
+
+
+def _state_given_kernel_projections(case, gconv):
+    """The oracle's f32 state after the step when its q, k, v projection
+    outputs are replaced by the kernel's (the new conv taps hold them as
+    bf16), b, a and z staying the oracle's. Also checks that each of the
+    kernel's values is within one bf16 ulp of the oracle's."""
+    from oracle import gdn_oracle as O
+    from gdn_harness import bf16_ulp
+    sh = case.shape
+    Hk, Hv, dk, dv, C = sh.num_k_heads, sh.num_v_heads, sh.head_k_dim, sh.head_v_dim, sh.conv_channels
+    ref = case.run_oracle()
+    w = {k: f64(v) for k, v in case.w.items()}
+    conv0, ssm0 = f64(case.st["conv_state"]), f64(case.st["ssm_state"])
+    out = ssm0.copy()
+    _, _, _, _, b, a = O.split_projection(ref["p_qkvz"], ref["p_ba"], Hk, Hv, dk, dv)
+    for r, s in enumerate(case.step["state_indices"].numpy()):
+        if not 0 < s < sh.num_slots:
+            continue
+        u = gconv[s][:, -1]
+        assert np.all(np.abs(u - ref["p_qkvz"][r, :C]) <= bf16_ulp(ref["p_qkvz"][r, :C]))
+        y, _ = O.conv_update(conv0[s], w["conv_w"], u)
+        qn = O.l2norm(y[:Hk * dk].reshape(Hk, dk), sh.l2_eps) * sh.scale_q
+        kn = O.l2norm(y[Hk * dk:2 * Hk * dk].reshape(Hk, dk), sh.l2_eps)
+        yv = y[2 * Hk * dk:].reshape(Hv, dv)
+        g, beta = O.gates(a[r], b[r], w["A_log"], w["dt_bias"])
+        for h in range(Hv):
+            kh = h // (Hv // Hk)
+            S, _ = O.delta_rule(ssm0[s, h], kn[kh], yv[h], qn[kh], g[h], beta[h])
+            out[s, h] = O.f32_round(S)
+    return out
 
 
 def _run_stress(shape, rows, seed, engine, **kw):
@@ -87,6 +123,8 @@ def _run_stress(shape, rows, seed, engine, **kw):
     core, res_out = case.run_gpu(layer)
     assert layer.check()[0] == 0
     compare(case, case.run_oracle(), core, res_out, state_tol=STRESS_STATE_TOL)
+    cond = _state_given_kernel_projections(case, f64(case.dconv))
+    assert float(np.max(np.abs(f64(case.dssm) - cond))) <= 1e-3
 
 
 @pytest.mark.parametrize("engine", ENGINES)

@@ -8,14 +8,17 @@ array inside the library instead of a caller workspace, with no handle.
 
 Each case runs two steps in a row on each path from the same starting state,
 so the second step reads the state the first one wrote and runs on counters
-the first one advanced. The bar is the step's own parity tolerance. This file
-is named to be collected last: the static scratch lives as long as the
-process, and the cases must pass both alone and after every other GPU test."""
+the first one advanced. Both paths launch the same kernel with the same plan
+and a fixed reduction order, so every output must be bit-identical; the
+first step is also compared with the CPU oracle at the step's tolerances.
+This file is named to be collected last: the static scratch lives as long as
+the process, and the cases must pass both alone and after every other GPU
+test."""
 import pytest
 import torch
 
 from gated_deltanet_layer_gb300 import GdnDecode, GdnError, _native, step_static, workloads as WL
-from gdn_harness import CORE_MAX_ABS, STATE_BF16_MAX_ABS, STATE_F32_MAX_ABS, Case
+from gdn_harness import Case, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +27,10 @@ pytestmark = pytest.mark.gpu
 def _built():
     import __graft_entry__ as g
     g.build()
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
 
 
 def _two_steps_each(shape, rows, seed, **kw):
@@ -35,9 +42,15 @@ def _two_steps_each(shape, rows, seed, **kw):
     layer = GdnDecode(shape)
     conv_a, ssm_a = case.dconv.clone(), case.dssm.clone()
     ref = []
-    for x, r, i in steps:
+    for k, (x, r, i) in enumerate(steps):
         core, res_out = layer.step(x, r, case.dw, i, conv_a, ssm_a)
         ref.append((core.clone(), res_out.clone()))
+        if k == 0:
+            # the handle path's first step against the oracle
+            torch.cuda.synchronize()
+            case.dconv, case.dssm, saved = conv_a.clone(), ssm_a.clone(), (case.dconv, case.dssm)
+            compare(case, case.run_oracle(), core, res_out)
+            case.dconv, case.dssm = saved
     assert layer.check()[0] == 0
 
     conv_b, ssm_b = case.dconv.clone(), case.dssm.clone()
@@ -45,25 +58,32 @@ def _two_steps_each(shape, rows, seed, **kw):
     res_b = torch.empty(rows, shape.hidden, dtype=torch.bfloat16, device="cuda")
     ws = GdnDecode.weights_struct(case.dw)
     got = [(torch.empty_like(core_b), torch.empty_like(res_b)) for _ in steps]
-    free0 = None
+    torch.cuda.synchronize()
+    reserved0 = torch.cuda.memory_reserved()
+    free_before = torch.cuda.mem_get_info()[0]
     for k, (x, r, i) in enumerate(steps):
         if k == 1:
             torch.cuda.synchronize()
-            free0 = torch.cuda.mem_get_info()[0]
+            free_second = torch.cuda.mem_get_info()[0]
         st, detail = step_static(shape, x, r, ws, i, conv_b, ssm_b, core_b, res_b, check=True)
         assert st == _native.GDN_OK, f"device error 0x{detail:08x}"
         got[k][0].copy_(core_b)
         got[k][1].copy_(res_b)
     torch.cuda.synchronize()
-    # the second call found its set-up done: no device memory changed hands
-    assert torch.cuda.mem_get_info()[0] == free0
+    # nothing went through torch's allocator on either call
+    assert torch.cuda.memory_reserved() == reserved0
+    # the second call found its set-up done: no device memory changed hands.
+    # The first call may load the library's module that holds the scratch
+    # array (lazy module loading), which the driver does, not the call: a
+    # loose bound of the array's size plus a few MiB of code and tables.
+    assert torch.cuda.mem_get_info()[0] == free_second
+    assert free_before - free_second <= _native.GDN_STATIC_SCRATCH_BYTES + (16 << 20)
 
-    state_tol = STATE_BF16_MAX_ABS if shape.ssm_dtype == "bf16" else STATE_F32_MAX_ABS
     for (ca, ra), (cb, rb) in zip(ref, got):
-        assert torch.equal(ra, rb)  # residual_out: bit-exact
-        assert (ca.float() - cb.float()).abs().max().item() <= CORE_MAX_ABS
-    assert (ssm_a.float() - ssm_b.float()).abs().max().item() <= state_tol
-    assert (conv_a.float() - conv_b.float()).abs().max().item() <= CORE_MAX_ABS
+        assert torch.equal(_bits(ra), _bits(rb))
+        assert torch.equal(_bits(ca), _bits(cb))
+    assert torch.equal(_bits(ssm_a), _bits(ssm_b))
+    assert torch.equal(_bits(conv_a), _bits(conv_b))
 
 
 @pytest.mark.parametrize("rows", [1, 16])
