@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--workload", default="full")
     ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
     ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width tables")
-    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4",
+    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,shard_wide",
                     help="workloads of the per-width tables ('' for none)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--engine", default="auto")
@@ -76,6 +76,8 @@ TABLES = {
     "full": {"widths": [1, 2, 4, 8, 16]},
     "shard_bf16": {"widths": [1, 3, 8, 9, 16], "pad": 0.25, "first_layer": True},
     "dense_mxfp4": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
+    # steps wider than one launch (one launch per 16-row tile)
+    "shard_wide": {"shape": "shard", "max_rows": 64, "widths": [16, 24, 32, 48, 64]},
 }
 
 
@@ -342,7 +344,8 @@ def native(args):
         b = sh.launch_bytes(rows, live, first_layer=first_layer)
         gbs = b / u / 1e3
         return {"us": round(u, 3), "GBps": round(gbs, 1), "frac_of_" + peak_kind: round(gbs / peak, 4),
-                "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": b, "live_rows": live}
+                "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": b, "live_rows": live,
+                "launches": -(-rows // 16)}
 
     def width_table(rig, widths, pad=0.0, first_layer=False):
         """µs per launch of a graph of 100 launches, median of replays over
@@ -428,7 +431,8 @@ def native(args):
         if name != args.workload or rig is None:
             rig = None
             torch.cuda.empty_cache()
-            rig = Rig(WL.SHAPES[name], g, l2, args.engine, rec.get("min_copies", 4))
+            tshape = WL.SHAPES[rec.get("shape", name)].with_(max_rows=rec.get("max_rows", 16))
+            rig = Rig(tshape, g, l2, args.engine, rec.get("min_copies", 4))
         ws = rec["widths"] if name != args.workload else sorted(set(rec["widths"]) | set(widths))
         tables[name] = {"copies": rig.ncopy, "first_layer": rec.get("first_layer", False),
                         "pad_fraction": rec.get("pad", 0.0),

@@ -77,7 +77,7 @@ int n_conv(const gdn_decode_config& c) {
 gdn_status validate(const gdn_decode_config* c) {
   if (!c) return GDN_ERR_ARG;
   if (c->hidden <= 0 || c->num_k_heads <= 0 || c->num_v_heads <= 0 || c->head_k_dim <= 0 ||
-      c->head_v_dim <= 0 || c->num_slots <= 0 || c->max_rows < 1 || c->max_rows > kMaxRows)
+      c->head_v_dim <= 0 || c->num_slots <= 0 || c->max_rows < 1 || c->max_rows > GDN_MAX_ROWS)
     return GDN_ERR_ARG;
   if (c->ssm_dtype != GDN_STATE_F32 && c->ssm_dtype != GDN_STATE_BF16) return GDN_ERR_ARG;
   if (c->qkvz_format != GDN_W_BF16 && c->qkvz_format != GDN_W_MXFP4) return GDN_ERR_ARG;
@@ -497,6 +497,30 @@ gdn_status launch_step(const gdn_decode_config& c, const Plan& pl, bool* pdl, co
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// The launches of one step: rows in tiles of at most kMaxRows, one launch
+// per tile in row order, each a whole step over its rows (rows are
+// independent: distinct state slots). A step of up to kMaxRows rows is one
+// launch; wider steps stream the weights once per tile.
+gdn_status launch_row_tiles(const gdn_decode_config& c, const Plan& pl, const Layout& lay, char* base,
+                            const StepArgs& a, MapCache* maps, bool* pdl, cudaStream_t s) {
+  const size_t xrow = (size_t)c.hidden * 2, crow = (size_t)c.num_v_heads * c.head_v_dim * 2;
+  for (int r0 = 0; r0 < a.rows; r0 += kMaxRows) {
+    StepArgs t = a;
+    t.rows = std::min(kMaxRows, a.rows - r0);
+    t.x = (const char*)a.x + r0 * xrow;
+    t.residual = a.residual ? (const char*)a.residual + r0 * xrow : nullptr;
+    t.idx = a.idx + r0;
+    t.core_out = (char*)a.core_out + r0 * crow;
+    t.residual_out = (char*)a.residual_out + r0 * xrow;
+    StepParams p;  // on the stack: the step allocates nothing
+    fill_params(c, pl, lay, base, t, &p);
+    if (!weight_maps(c, a.w, maps, &p)) return GDN_ERR_CUDA;
+    const gdn_status st = launch_step(c, pl, pdl, p, a.residual != nullptr, s);
+    if (st != GDN_OK) return st;
+  }
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -602,10 +626,7 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   const StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
   gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
   if (st != GDN_OK) return st;
-  StepParams p;  // on the stack: the step allocates nothing
-  fill_params(h->cfg, h->plan, h->lay, (char*)h->ws, a, &p);
-  if (!weight_maps(h->cfg, w, &h->maps, &p)) return GDN_ERR_CUDA;
-  return launch_step(h->cfg, h->plan, &h->pdl, p, residual != nullptr, (cudaStream_t)stream);
+  return launch_row_tiles(h->cfg, h->plan, h->lay, (char*)h->ws, a, &h->maps, &h->pdl, (cudaStream_t)stream);
 }
 
 gdn_status gdn_decode_check(gdn_decode_t* h, void* stream, uint32_t* detail) {
@@ -813,7 +834,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
                                              void* core_out, void* residual_out, void* stream,
                                              uint32_t* detail) {
   if (!cfg || !w) return GDN_ERR_ARG;
-  if (rows < 1 || rows > cfg->max_rows || cfg->max_rows > kMaxRows) return GDN_ERR_ARG;
+  if (rows < 1 || rows > cfg->max_rows || cfg->max_rows > GDN_MAX_ROWS) return GDN_ERR_ARG;
   // argument errors come back before any CUDA call
   const StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
   gdn_status st = check_step_args(*cfg, a, nullptr, 0);
@@ -827,11 +848,8 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_decode_config* cfg, int32
   StaticDevice& d = *dp;
   st = check_step_args(d.run, a, d.scratch, d.lay.total);  // now also against the scratch
   if (st != GDN_OK) return st;
-  StepParams p;
   char* base = (char*)d.scratch;
-  fill_params(d.run, d.plan, d.lay, base, a, &p);
-  if (!weight_maps(d.run, w, &d.maps, &p)) return GDN_ERR_CUDA;
-  st = launch_step(d.run, d.plan, &d.pdl, p, residual != nullptr, s);
+  st = launch_row_tiles(d.run, d.plan, d.lay, base, a, &d.maps, &d.pdl, s);
   if (st != GDN_OK || !detail) return st;
 
   uint32_t word = 0;

@@ -11,7 +11,7 @@ namespace gdn {
 
 constexpr int kThreads = 512;              // one persistent CTA per SM
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRows = 16;               // rows of one decode step
+constexpr int kMaxRows = 16;               // rows of one launch (wider steps run as several launches)
 constexpr int kTileM = 256;                // projection rows per tile (one MMA's N)
 constexpr int kTileShift = 8;              // log2(kTileM)
 constexpr int kKStep = 64;                 // projection columns per work unit

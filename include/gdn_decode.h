@@ -73,6 +73,14 @@ typedef enum {
   GDN_ERR_FAILED = 6        /* device: the sticky error word holds an unknown code */
 } gdn_status;
 
+/* Rows of one step: up to GDN_ROWS_PER_LAUNCH run as one launch (the row
+ * cap of the pages' launch: vLLM #60833, Details, "Steps"; sgl-amd-mono #89,
+ * Modifications); wider steps, up to GDN_MAX_ROWS, run as one launch per
+ * tile of GDN_ROWS_PER_LAUNCH rows, in row order, each streaming the
+ * weights again. */
+#define GDN_ROWS_PER_LAUNCH 16
+#define GDN_MAX_ROWS 64
+
 typedef enum { GDN_STATE_F32 = 0, GDN_STATE_BF16 = 1 } gdn_state_dtype;
 typedef enum { GDN_W_BF16 = 0, GDN_W_MXFP4 = 1 } gdn_weight_format;
 
@@ -118,7 +126,7 @@ typedef struct {
   int32_t head_v_dim;
   int32_t conv_kernel;     /* must be 4 */
   int32_t num_slots;
-  int32_t max_rows;        /* 1..16 */
+  int32_t max_rows;        /* 1..GDN_MAX_ROWS */
   int32_t ssm_dtype;       /* gdn_state_dtype */
   int32_t qkvz_format;     /* gdn_weight_format */
   int32_t engine;          /* gdn_engine */
@@ -171,8 +179,9 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace,
                              size_t workspace_bytes, void* stream,
                              gdn_decode_t** out);
 
-/* Run one decode step of `rows` rows (1..max_rows) as one launch on `stream`
- * (the step list at the top of this header). Asynchronous and
+/* Run one decode step of `rows` rows (1..max_rows) on `stream` (the step
+ * list at the top of this header): one launch for up to GDN_ROWS_PER_LAUNCH
+ * rows, else one launch per tile of that many rows. Asynchronous and
  * stream-ordered; allocates no memory on the host or the device; may be
  * captured in a CUDA graph. residual == NULL selects the first-layer variant
  * (r = x). See "Launch options" for the weights it reads before the previous

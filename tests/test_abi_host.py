@@ -56,7 +56,7 @@ def _cfg(**kw):
 
 
 @pytest.mark.parametrize("field,value", [
-    ("max_rows", 0), ("max_rows", 17), ("hidden", 0), ("num_slots", 0), ("ssm_dtype", 7),
+    ("max_rows", 0), ("max_rows", 65), ("hidden", 0), ("num_slots", 0), ("ssm_dtype", 7),
     ("engine", 9), ("num_ctas", -1), ("norm_eps", float("nan")), ("launch_flags", 4), ("launch_flags", -1),
 ])
 def test_invalid_config_has_no_workspace(lib, field, value):

@@ -178,3 +178,37 @@ def test_mxfp4_needs_the_tensor_core_engine():
     with pytest.raises(GdnError) as e:
         GdnDecode(WL.DENSE_MXFP4, engine="cuda_core")
     assert e.value.code == _native.GDN_ERR_UNSUPPORTED
+
+
+# Steps wider than one launch's 16 rows run as one launch per tile of 16
+# rows (the pages' row cap per launch); every row is checked against the
+# oracle, pad rows included.
+WIDE_TINY = WL.TINY.with_(num_slots=80, max_rows=64)
+
+
+@pytest.mark.parametrize("rows", [17, 32, 40, 64])
+def test_wide_steps(rows):
+    _run(WIDE_TINY, rows, 9000 + rows, "auto", pad_rows=rows // 5)
+
+
+def test_wide_step_shard_first_layer_bf16_state():
+    _run(WL.SHARD_BF16.with_(max_rows=64), 48, 9100, "auto", first_layer=True, pad_rows=12)
+
+
+def test_wide_step_rows_match_16_row_steps():
+    """Each 16-row tile of a 40-row step is bit-identical to a 16-row (or
+    8-row) step of the same rows on the same state."""
+    shape = WL.SHARD.with_(max_rows=64)
+    wide = Case(shape, 40, 9200).to_device()
+    cw, rw = wide.run_gpu(GdnDecode(shape))
+    for r0 in (0, 16, 32):
+        n = min(16, 40 - r0)
+        stp = {"x": wide.step["x"][r0:r0 + n].clone(), "residual": wide.step["residual"][r0:r0 + n].clone(),
+               "state_indices": wide.step["state_indices"][r0:r0 + n].clone()}
+        part = Case(shape, n, 0, weights=wide.w, state=wide.st, step=stp).to_device()
+        cp, rp = part.run_gpu(GdnDecode(shape))
+        assert torch.equal(cp.view(torch.int16), cw[r0:r0 + n].view(torch.int16))
+        assert torch.equal(rp.view(torch.int16), rw[r0:r0 + n].view(torch.int16))
+        for s in stp["state_indices"].tolist():
+            assert torch.equal(part.dssm[s].view(torch.int32), wide.dssm[s].view(torch.int32))
+            assert torch.equal(part.dconv[s].view(torch.int16), wide.dconv[s].view(torch.int16))
