@@ -445,15 +445,41 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
 // K-major layout the MMA reads, then release the code stage and hand the bf16
 // stage to the MMA. A row's scales for 8 k-steps are one aligned 16-byte
 // load, issued a block ahead.
-static __device__ __forceinline__ float e8m0_scale(uint32_t e) {
-  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);  // 2^(e - 127); e = 0: 2^-127
+// 2^(e - 127) of an e8m0 byte as bf16x2 (both halves): bf16 exponent field
+// e; e = 0 is 2^-127, the bf16 subnormal 0x0040.
+static __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
+  const uint32_t h = e == 0 ? 0x0040u : (e << 7);
+  return h | (h << 16);
 }
-// Value of a 4-bit e2m1 code (sign bit 3, exponent bits 2..1 with bias 1,
-// mantissa bit 0; exponent 0: 0 or 0.5), built from its f32 bits.
-static __device__ __forceinline__ float e2m1_value(uint32_t c) {
-  const uint32_t m = c & 7u;
-  const uint32_t mag = m < 2u ? (m ? 0x3f000000u : 0u) : ((126u + (m >> 1)) << 23) | ((m & 1u) << 22);
-  return __uint_as_float(mag | ((c & 8u) << 28));
+static __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// bf16x2 product, round to nearest even (exact here: a power of two times a
+// value with a 2-bit significand).
+static __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Eight e2m1 codes (one 32-bit word, element i in nibble i: sign bit 3,
+// exponent bits 2..1 with bias 1, mantissa bit 0) to their bf16 values as
+// four bf16x2 words, element 2j in the low half of word j. The magnitudes
+// {0, .5, 1, 1.5, 2, 3, 4, 6} have the bf16 patterns 0x0000, 0x3F00, 0x3F80,
+// 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0: their high and low bytes are two
+// 8-entry byte tables, looked up four codes at a time with PRMT (the code's
+// low 3 bits select a byte); the sign bits are shifted into bit 15 / 31.
+static __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&o)[4]) {
+  constexpr uint32_t kHiLo = 0x3F3F3F00u, kHiHi = 0x40404040u;  // high bytes of magnitudes 0..3, 4..7
+  constexpr uint32_t kLoLo = 0xC0800000u, kLoHi = 0xC0804000u;  // low bytes
+  const uint32_t m = w & 0x77777777u, m2 = m >> 16;
+  const uint32_t h0 = prmt(kHiLo, kHiHi, m), l0 = prmt(kLoLo, kLoHi, m);
+  const uint32_t h1 = prmt(kHiLo, kHiHi, m2), l1 = prmt(kLoLo, kLoHi, m2);
+  o[0] = prmt(l0, h0, 0x5140u) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
+  o[1] = prmt(l0, h0, 0x7362u) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+  o[2] = prmt(l1, h1, 0x5140u) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
+  o[3] = prmt(l1, h1, 0x7362u) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
 }
 // All-threads-of-a-named-barrier AND of a predicate (every thread gets it).
 static __device__ __forceinline__ bool bar_and(bool v) {
@@ -516,18 +542,15 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
       const int kk = it.ks & 7;  // k-step within the block: scale bytes 2kk, 2kk + 1
       const uint32_t sw4 = (kk >> 1) == 0 ? cur.x : (kk >> 1) == 1 ? cur.y : (kk >> 1) == 2 ? cur.z : cur.w;
       const uint32_t sword = sw4 >> ((kk & 1) * 16);
-      const float sc[2] = {e8m0_scale(sword & 0xffu), e8m0_scale((sword >> 8) & 0xffu)};
+      const uint32_t sc[2] = {e8m0_bf16x2(sword & 0xffu), e8m0_bf16x2((sword >> 8) & 0xffu)};
       uint8_t* dst = sW + (size_t)pos.s * kWBytes + ci * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {  // 8 columns per 16-byte chunk, from one 32-bit word of codes
-        const uint32_t wv = words[c];
-        const float scale = sc[c >> 2];
         uint32_t o[4];
+        e2m1x8_to_bf16(words[c], o);
+        const uint32_t scale = sc[c >> 2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = (wv >> (8 * e)) & 0xfu, hi = (wv >> (8 * e + 4)) & 0xfu;
-          o[e] = pack_bf16x2(e2m1_value(lo) * scale, e2m1_value(hi) * scale);  // exact in bf16
-        }
+        for (int e = 0; e < 4; ++e) o[e] = mul_bf16x2(o[e], scale);  // exact in bf16
         *reinterpret_cast<uint4*>(dst + ((c ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       tc::fence_proxy_async_smem();  // the generic-proxy writes, visible to the MMA
