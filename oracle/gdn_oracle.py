@@ -14,7 +14,7 @@ Launches; SGLang #43558 "Qwen3.8-27B dense mono decode", Modifications, K1):
   1. residual add                       r  = x + residual     (first layer: r = x)
   2. Gemma RMSNorm                      xn = r * rstd * (1 + w_in),
                                         rstd = 1 / sqrt(mean(r^2) + eps)
-  3. in_proj_qkvz, in_proj_ba           p  = W xn   (bf16 or MXFP4 weights)
+  3. in_proj_qkvz, in_proj_ba           p  = W xn   (bf16, MXFP4 or MXFP6 weights)
   4. split                              p -> q | k | v | z   and  b | a
   5. causal depthwise conv1d + SiLU     over the q, k, v channels, state update
   6. L2 norm of q and k per key head    (q also times q_scale)
@@ -56,7 +56,8 @@ __all__ = [
     "bf16_round", "f32_round", "silu", "softplus", "sigmoid",
     "residual_add", "gemma_rmsnorm", "project_bf16", "e2m1_value",
     "mxfp4_unpack_codes", "mxfp4_quantize_block", "mxfp4_quantize_row",
-    "project_mxfp4", "split_projection", "conv_update", "l2norm",
+    "project_mxfp4", "e2m3_value", "mxfp6_quantize_block", "mxfp6_quantize_matrix",
+    "mxfp6_pack", "mxfp6_unpack", "project_mxfp6", "split_projection", "conv_update", "l2norm",
     "gates", "delta_rule", "gated_rmsnorm", "gdn_step",
 ]
 
@@ -254,6 +255,117 @@ def project_mxfp4(xn, w_packed, w_scales):
 
 
 # --------------------------------------------------------------------------
+# MXFP6 E2M3 weights with bf16 activations (W6A16): vLLM #60833, review
+# comment "How to make the MXFP6 weights". Step 2 there rounds each bf16
+# weight, one block of 32 along K at a time, to its E2M3 value times a
+# power-of-two block scale; step 3 packs the codes (sign at bit 5, then two
+# exponent and three mantissa bits) 32 to 24 bytes, code i at bits 6i to
+# 6i + 5 in little-endian order, with one e8m0 byte per block. The
+# activations stay bf16; decoded weights are exact in bf16.
+# --------------------------------------------------------------------------
+
+def e2m3_value(code):
+    """Value of a 6-bit E2M3 code: sign bit 5, exponent bits 4..3 with bias
+    1, mantissa bits 2..0; exponent field 0 is subnormal (m / 8)."""
+    code = np.asarray(code, dtype=np.int64)
+    s = np.where((code >> 5) & 1, -1.0, 1.0)
+    e = (code >> 3) & 3
+    m = code & 7
+    mag = np.where(e == 0, m / 8.0, np.ldexp(1.0 + m / 8.0, e - 1))
+    return s * mag
+
+
+def _e2m3_round_magnitude(a):
+    """Round non-negative magnitudes to the E2M3 grid (steps of 1/8 below 2,
+    1/4 in [2, 4), 1/2 from 4), ties to even, saturating at 7.5."""
+    a = np.asarray(a, dtype=np.float64)
+    step = np.where(a < 2.0, 0.125, np.where(a < 4.0, 0.25, 0.5))
+    return np.minimum(np.rint(a / step) * step, 7.5)
+
+
+def _e2m3_code(q):
+    """Code of a non-negative E2M3 grid value q."""
+    q = np.asarray(q, dtype=np.float64)
+    sub = q < 1.0
+    e = np.where(sub, 0, np.floor(np.log2(np.where(sub, 1.0, q))).astype(np.int64) + 1)
+    m = np.where(sub, np.rint(q * 8.0), np.rint((q / np.ldexp(1.0, e - 1) - 1.0) * 8.0))
+    return (e << 3 | m.astype(np.int64)).astype(np.int64)
+
+
+def mxfp6_quantize_block(v):
+    """One block of 32 values to E2M3 codes and a block scale.
+
+    Scale: the block maximum |v| as f32, its mantissa rounded at the third
+    bit (2^19 added to its bits: a carry moves the exponent), exponent E kept;
+    the scale is 2^(E - 2), E - 2 clamped to [-126, 127] so an all-zero
+    block keeps a normal scale. Elements: |v| / scale rounded to the E2M3
+    grid, ties to even, saturating at 7.5.
+
+    Returns (codes [32] uint8, scale exponent int, e8m0 byte)."""
+    v = np.asarray(v, dtype=np.float64)
+    amax = np.float32(np.max(np.abs(v)))
+    bits = int(amax.view(np.uint32))
+    e_field = ((bits + (1 << 19)) >> 23) & 0xFF
+    exp = int(min(max(e_field - 127 - 2, -126), 127))
+    mag = _e2m3_round_magnitude(np.abs(v) / math.ldexp(1.0, exp))
+    codes = _e2m3_code(mag)
+    codes = np.where(np.signbit(v) & (mag > 0), codes | 32, codes).astype(np.uint8)
+    return codes, exp, exp + 127
+
+
+def mxfp6_quantize_matrix(W):
+    """[N, K] weights (K a multiple of 32) to E2M3 codes [N, K] and e8m0
+    scale bytes [N, K/32], block by block along K."""
+    W = np.asarray(W, dtype=np.float64)
+    N, K = W.shape
+    codes = np.empty((N, K), dtype=np.uint8)
+    scales = np.empty((N, K // 32), dtype=np.uint8)
+    for n in range(N):
+        for b in range(K // 32):
+            c, _, byte = mxfp6_quantize_block(W[n, 32 * b:32 * b + 32])
+            codes[n, 32 * b:32 * b + 32] = c
+            scales[n, b] = byte
+    return codes, scales
+
+
+def mxfp6_pack(codes):
+    """[..., K] 6-bit codes to [..., 3K/4] bytes: each block of 32 codes
+    is a 192-bit little-endian number with code i at bits 6i..6i+5."""
+    codes = np.asarray(codes, dtype=np.uint64)
+    lead, K = codes.shape[:-1], codes.shape[-1]
+    blocks = codes.reshape(-1, K // 32, 32)
+    out = np.zeros(blocks.shape[:2] + (24,), dtype=np.uint8)
+    for i in range(32):
+        for bit in range(6):
+            pos = 6 * i + bit
+            out[..., pos // 8] |= (((blocks[..., i] >> np.uint64(bit)) & np.uint64(1)) << np.uint64(pos % 8)).astype(np.uint8)
+    return out.reshape(lead + (K // 32 * 24,))
+
+
+def mxfp6_unpack(packed):
+    """Inverse of mxfp6_pack: [..., 3K/4] bytes to [..., K] codes."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    lead, nb = packed.shape[:-1], packed.shape[-1]
+    groups = packed.reshape(-1, nb // 24, 24)
+    codes = np.zeros(groups.shape[:2] + (32,), dtype=np.uint8)
+    for i in range(32):
+        for bit in range(6):
+            pos = 6 * i + bit
+            codes[..., i] |= ((groups[..., pos // 8] >> (pos % 8)) & 1).astype(np.uint8) << bit
+    return codes.reshape(lead + (nb // 24 * 32,))
+
+
+def project_mxfp6(xn, w_packed, w_scales):
+    """W6A16 projection: p[w, n] = bf16(sum_h e2m3(W[n, h]) 2^(s[n, h/32] - 127)
+    xn[w, h]) with bf16 activations, the sum taken in float64 and rounded once."""
+    xn = np.asarray(xn, dtype=np.float64)
+    wv = e2m3_value(mxfp6_unpack(w_packed))  # [N, K]
+    ws = np.ldexp(1.0, np.asarray(w_scales, dtype=np.int64) - 127)
+    W = wv * np.repeat(ws, 32, axis=1)
+    return bf16_round(xn @ W.T)
+
+
+# --------------------------------------------------------------------------
 # Step 4: split of the projection outputs (sgl-amd-mono #89, "Kernels before
 # and after": the split of the projection output is its own stock kernel)
 # --------------------------------------------------------------------------
@@ -380,6 +492,8 @@ def gdn_step(shape, x, residual, weights, state_indices, conv_state, ssm_state):
     xn = gemma_rmsnorm(r, weights["input_norm_w"], shape.norm_eps)
     if shape.qkvz_format == "mxfp4":
         p_qkvz = project_mxfp4(xn, weights["qkvz"], weights["qkvz_scales"])
+    elif shape.qkvz_format == "mxfp6":
+        p_qkvz = project_mxfp6(xn, weights["qkvz"], weights["qkvz_scales"])
     else:
         p_qkvz = project_bf16(xn, weights["qkvz"])
     p_ba = project_bf16(xn, weights["ba"])

@@ -486,3 +486,104 @@ def test_step_decay_takes_the_a_slice():
         for h in range(Hv):
             factor = 1.0 / (1.0 + math.exp(at[h]))
             np.testing.assert_allclose(out["ssm_state"][s, h], ssm[s, h] * factor, rtol=2.0**-23, atol=1e-30)
+
+
+# ---------------------------------------------------------------- MXFP6 E2M3 (W6A16)
+
+def test_e2m3_table(golden):
+    for code, value in golden("e2m3_codes.txt"):
+        v = float(O.e2m3_value(int(code)))
+        assert v == value and math.copysign(1.0, v) == math.copysign(1.0, value), (code, v, value)
+
+
+def _nearest_e2m3_brute(a):
+    """Nearest E2M3 magnitude by search over the 32 codes' values; a tie
+    goes to the even code; above 7.5: 7.5."""
+    grid = [float(O.e2m3_value(c)) for c in range(32)]
+    if a >= 7.5:
+        return 7.5
+    best = None
+    for code, g in enumerate(grid):
+        d = abs(a - g)
+        if best is None or d < best[0] or (d == best[0] and code % 2 == 0):
+            best = (d, code, g)
+    return best[2]
+
+
+def test_mxfp6_element_rounding_brute_force():
+    rng = np.random.default_rng(15)
+    mags = np.concatenate([rng.uniform(0, 9, 4000), np.arange(0, 8.01, 0.0625)])
+    for a in mags:
+        assert float(O._e2m3_round_magnitude(a)) == _nearest_e2m3_brute(float(a)), a
+
+
+def test_mxfp6_quantize_block_scale_rule():
+    """The block-scale rule of the MXFP6 review comment (step 2): the block
+    maximum rounded at its third mantissa bit, scale 2^(E - 2) clamped to
+    [-126, 127], values rounded to the grid, nothing above 7.5 x scale."""
+    rng = np.random.default_rng(16)
+    grid = np.array([float(O.e2m3_value(c)) for c in range(32)])
+    for k in (-7, -1, 0, 2):
+        # values on the grid with the block maximum 7.5 * 2^k: they quantise to themselves
+        v = rng.choice(grid, 32) * rng.choice([-1.0, 1.0], 32) * 2.0**k
+        v[9] = 7.5 * 2.0**k
+        codes, exp, byte = O.mxfp6_quantize_block(v)
+        assert exp == k and byte == k + 127
+        np.testing.assert_array_equal(O.e2m3_value(codes) * 2.0**exp, v)
+    # 1.9375 = 1.1111b: rounding at the third mantissa bit carries, E = 1,
+    # scale 2^-1; 1.9375 / 0.5 = 3.875 lies halfway between 3.75 and 4.0 on
+    # the quarter grid and goes to the even code (4.0, code 24): value 2.0
+    v = np.zeros(32); v[0] = 1.9375
+    codes, exp, _ = O.mxfp6_quantize_block(v)
+    assert exp == -1 and codes[0] == 24 and float(O.e2m3_value(codes[0])) * 2.0**exp == 2.0
+    # 1.875 = 1.111b: no carry, E = 0, scale 2^-2, 1.875 / 0.25 = 7.5 exactly (code 31)
+    v[0] = 1.875
+    codes, exp, _ = O.mxfp6_quantize_block(v)
+    assert exp == -2 and codes[0] == 31
+    # all-zero block: zero codes, scale 2^-126
+    codes, exp, byte = O.mxfp6_quantize_block(np.zeros(32))
+    assert np.all(codes == 0) and exp == -126 and byte == 1
+    for _ in range(50):
+        v = rng.standard_normal(32) * 10.0 ** rng.uniform(-3, 3)
+        codes, exp, _ = O.mxfp6_quantize_block(v)
+        deq = O.e2m3_value(codes) * 2.0**exp
+        assert np.all(np.abs(deq) <= 7.5 * 2.0**exp)
+        assert np.all(np.sign(deq) * np.sign(v) >= 0)
+        # every element within half a grid step (of its binade) of its value
+        assert np.all(np.abs(deq - v) <= 0.25 * 2.0**exp + 1e-300)
+
+
+def test_mxfp6_packing_bit_positions():
+    """32 codes in 24 bytes, code i at bits 6i..6i+5 of the little-endian
+    group (review comment step 3); bytes worked by hand."""
+    codes = np.zeros(32, dtype=np.uint8)
+    codes[0] = 0x01           # bits 0..5   -> byte 0 = 0x01
+    codes[1] = 0x01           # bits 6..11  -> byte 0 bit 6 (0x40)
+    codes[2] = 0x3F           # bits 12..17 -> byte 1 bits 4..7 (0xF0), byte 2 bits 0..1 (0x03)
+    codes[3] = 0x20           # bits 18..23 -> bit 23: byte 2 bit 7 (0x80)
+    codes[31] = 0x3F          # bits 186..191 -> byte 23 bits 2..7 (0xFC)
+    packed = O.mxfp6_pack(codes[None, :])[0]
+    want = np.zeros(24, dtype=np.uint8)
+    want[0], want[1], want[2], want[23] = 0x41, 0xF0, 0x83, 0xFC
+    np.testing.assert_array_equal(packed, want)
+    rng = np.random.default_rng(17)
+    c = rng.integers(0, 64, size=(5, 96)).astype(np.uint8)
+    np.testing.assert_array_equal(O.mxfp6_unpack(O.mxfp6_pack(c)), c)
+
+
+def test_project_mxfp6_brute_force():
+    """W6A16: bf16 activations times decoded E2M3 weights, the exact
+    rational sum rounded once to bf16."""
+    rng = np.random.default_rng(18)
+    N, K = 3, 64
+    codes = rng.integers(0, 64, size=(N, K)).astype(np.uint8)
+    scales = (127 + rng.integers(-8, -3, size=(N, K // 32))).astype(np.uint8)
+    packed = O.mxfp6_pack(codes)
+    xn = _torch_bf16(rng.standard_normal((2, K)))
+    got = O.project_mxfp6(xn, packed, scales)
+    table = {c: Fraction(float(O.e2m3_value(c))) for c in range(64)}
+    for w in range(2):
+        for n in range(N):
+            total = sum(table[int(codes[n, h])] * Fraction(2) ** (int(scales[n, h // 32]) - 127) * Fraction(float(xn[w, h]))
+                        for h in range(K))
+            assert got[w, n] == O.bf16_round(float(total))
