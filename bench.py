@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--workload", default="full")
     ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
     ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width tables")
-    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,shard_wide",
+    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,dense_mxfp6,shard_wide",
                     help="workloads of the per-width tables ('' for none)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--engine", default="auto")
@@ -76,6 +76,7 @@ TABLES = {
     "full": {"widths": [1, 2, 4, 8, 16]},
     "shard_bf16": {"widths": [1, 3, 8, 9, 16], "pad": 0.25, "first_layer": True},
     "dense_mxfp4": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
+    "dense_mxfp6": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
     # steps wider than one launch (one launch per 16-row tile)
     "shard_wide": {"shape": "shard", "max_rows": 64, "widths": [16, 24, 32, 48, 64]},
 }
@@ -234,10 +235,12 @@ class Rig:
         H, Hv = shape.hidden, shape.num_v_heads
 
         def qkvz():
-            if shape.qkvz_format == "mxfp4":  # e2m1 codes uniform over the 16 codes, block exponents U{-8..-4}
-                return {"qkvz": torch.randint(0, 256, (shape.n_qkvz, H // 2), generator=g, device="cuda",
+            if shape.qkvz_format in ("mxfp4", "mxfp6"):
+                # codes uniform; block exponents U{-8..-4} (MXFP4) or U{-10..-6} (MXFP6)
+                nbytes, elo = (H // 2, -8) if shape.qkvz_format == "mxfp4" else (H * 3 // 4, -10)
+                return {"qkvz": torch.randint(0, 256, (shape.n_qkvz, nbytes), generator=g, device="cuda",
                                               dtype=torch.uint8),
-                        "qkvz_scales": (127 + torch.randint(-8, -3, (shape.n_qkvz, H // 32), generator=g,
+                        "qkvz_scales": (127 + torch.randint(elo, elo + 5, (shape.n_qkvz, H // 32), generator=g,
                                                             device="cuda")).to(torch.uint8)}
             return {"qkvz": self.bf16(shape.n_qkvz, H, std=0.02), "qkvz_scales": None}
 
@@ -444,11 +447,11 @@ def native(args):
         "metric": METRIC, "value": round(us, 3), "unit": "µs/launch", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("mxfp4" if shape.qkvz_format == "mxfp4" else "bf16") + " weights, f32 math, " + shape.ssm_dtype + " state",
+        "dtype": shape.qkvz_format + " weights, f32 math, " + shape.ssm_dtype + " state",
         "data": "synthetic (seeded random weights and states of the layer's shapes)",
         "config": {"workload": f"{shape.name}: H={shape.hidden} Hk={shape.num_k_heads} Hv={shape.num_v_heads} "
                                f"dk=dv={shape.head_k_dim} slots={shape.num_slots} {shape.ssm_dtype} state, "
-                               f"{'MXFP4' if shape.qkvz_format == 'mxfp4' else 'bf16'} in_proj_qkvz",
+                               f"{shape.qkvz_format} in_proj_qkvz",
                    "rows": args.rows, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: weights rotated over {ncopy} copies "
                          f"({ncopy * wbytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2), fresh slots per launch",

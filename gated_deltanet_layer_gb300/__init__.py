@@ -11,7 +11,9 @@ import ctypes
 
 from . import _native
 from ._native import (GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05, GDN_OK,
-                      GDN_STATE_BF16, GDN_STATE_F32, GDN_W_BF16, GDN_W_MXFP4, GdnError)
+                      GDN_STATE_BF16, GDN_STATE_F32, GDN_W_BF16, GDN_W_MXFP4, GDN_W_MXFP6, GdnError)
+
+_FORMATS = {"bf16": GDN_W_BF16, "mxfp4": GDN_W_MXFP4, "mxfp6": GDN_W_MXFP6}
 
 __all__ = ["GdnDecode", "GdnError", "ENGINES", "step_static"]
 
@@ -39,7 +41,7 @@ def make_config(shape, *, engine: str = "auto", deadline_us: int = 0, num_ctas: 
         head_k_dim=shape.head_k_dim, head_v_dim=shape.head_v_dim, conv_kernel=shape.conv_kernel,
         num_slots=shape.num_slots, max_rows=max_rows or shape.max_rows,
         ssm_dtype=GDN_STATE_BF16 if shape.ssm_dtype == "bf16" else GDN_STATE_F32,
-        qkvz_format=GDN_W_MXFP4 if shape.qkvz_format == "mxfp4" else GDN_W_BF16,
+        qkvz_format=_FORMATS[shape.qkvz_format],
         engine=ENGINES[engine], norm_eps=shape.norm_eps, gated_norm_eps=shape.gated_norm_eps,
         l2_eps=shape.l2_eps, q_scale=q_scale, deadline_us=deadline_us, num_ctas=num_ctas,
         debug_flags=debug_flags, launch_flags=launch_flags)

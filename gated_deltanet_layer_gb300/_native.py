@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(HERE, "libgdn_decode.so")
 
 GDN_OK, GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEADLINE, GDN_ERR_INDEX, GDN_ERR_FAILED = range(7)
 GDN_STATE_F32, GDN_STATE_BF16 = 0, 1
-GDN_W_BF16, GDN_W_MXFP4 = 0, 1
+GDN_W_BF16, GDN_W_MXFP4, GDN_W_MXFP6 = 0, 1, 2
 GDN_ENGINE_AUTO, GDN_ENGINE_CUDA_CORE, GDN_ENGINE_TCGEN05 = 0, 1, 2
 GDN_DEBUG_SKIP_NORM_PUBLISH = 0x1
 GDN_DEBUG_TIMELINE = 0x2

@@ -80,7 +80,8 @@ gdn_status validate(const gdn_decode_config* c) {
       c->head_v_dim <= 0 || c->num_slots <= 0 || c->max_rows < 1 || c->max_rows > GDN_MAX_ROWS)
     return GDN_ERR_ARG;
   if (c->ssm_dtype != GDN_STATE_F32 && c->ssm_dtype != GDN_STATE_BF16) return GDN_ERR_ARG;
-  if (c->qkvz_format != GDN_W_BF16 && c->qkvz_format != GDN_W_MXFP4) return GDN_ERR_ARG;
+  if (c->qkvz_format != GDN_W_BF16 && c->qkvz_format != GDN_W_MXFP4 && c->qkvz_format != GDN_W_MXFP6)
+    return GDN_ERR_ARG;
   if (c->engine < GDN_ENGINE_AUTO || c->engine > GDN_ENGINE_TCGEN05) return GDN_ERR_ARG;
   if (!(c->norm_eps >= 0.f) || !(c->gated_norm_eps >= 0.f) || !(c->l2_eps >= 0.f)) return GDN_ERR_ARG;
   if (c->num_ctas < 0 || c->num_ctas > kMaxCtas) return GDN_ERR_ARG;
@@ -95,8 +96,8 @@ gdn_status validate(const gdn_decode_config* c) {
   if ((c->num_k_heads * c->head_k_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if ((c->num_v_heads * c->head_v_dim) % kTileM != 0) return GDN_ERR_UNSUPPORTED;
   if (c->hidden % kKStep != 0 || c->hidden > (1 << 20)) return GDN_ERR_UNSUPPORTED;
-  // MXFP4: a row's e8m0 scales for 8 k-steps are one aligned 16-byte load
-  if (c->qkvz_format == GDN_W_MXFP4 && (c->hidden % 512 != 0 || c->head_k_dim != 128)) return GDN_ERR_UNSUPPORTED;
+  // MXFP4 / MXFP6: a row's e8m0 scales for 8 k-steps are one aligned 16-byte load
+  if (c->qkvz_format != GDN_W_BF16 && (c->hidden % 512 != 0 || c->head_k_dim != 128)) return GDN_ERR_UNSUPPORTED;
   const int tiles = n_qkvz(*c) / kTileM + (n_ba(*c) + kTileM - 1) / kTileM;
   if (tiles > kMaxTiles) return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
@@ -202,19 +203,19 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
   pl->max_contrib = maxc;
   if (engine == GDN_ENGINE_TCGEN05) {
     // the ring takes what the window (two windows with MXFP4 weights: xn and
-    // its quantised copy) and the raw ring leave: 2..6 tiles of 32 KB
-    const bool fp4 = c.qkvz_format == GDN_W_MXFP4;
+    // its quantised copy) and the code ring leave: 2..6 tiles of 32 KB
+    const int fmt = c.qkvz_format;
     int xs = 1;
     for (int cta = 0; cta < G; ++cta) xs = std::max(xs, (int)pl->nb_slots[cta]);
     pl->xslots = xs;
     pl->xpad = tensor_core_xpad(xs);
     const size_t avail = kSmemOptin - tensor_core_static_smem() - 1024;
     const size_t wtile = (size_t)kTileM * kKStep * 2;
-    pl->rstages = fp4 ? tensor_core_max_rstages() : 0;
-    const size_t fixed = tensor_core_smem_bytes(0, pl->rstages, xs, fp4);
+    pl->rstages = fmt != GDN_W_BF16 ? tensor_core_max_rstages() : 0;
+    const size_t fixed = tensor_core_smem_bytes(0, pl->rstages, xs, fmt);
     if (fixed + 2 * wtile > avail) return GDN_ERR_UNSUPPORTED;
     pl->stages = (int)std::min<size_t>((avail - fixed) / wtile, (size_t)tensor_core_max_stages());
-    pl->smem = tensor_core_smem_bytes(pl->stages, pl->rstages, xs, fp4);
+    pl->smem = tensor_core_smem_bytes(pl->stages, pl->rstages, xs, fmt);
   } else {
     pl->stages = pl->rstages = pl->xslots = 0;
     pl->xpad = 0;
@@ -256,7 +257,7 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
   const bool b16 = c.ssm_dtype == GDN_STATE_BF16;
-  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format == GDN_W_MXFP4)
+  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format)
                                       : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
@@ -280,9 +281,9 @@ void set_plan_params(const Plan& pl, StepParams* p) {
 
 // The engine a config runs with and its plan: the requested engine, or for
 // GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA
-// cores. MXFP4 weights run on the tensor-core engine only.
+// cores. MXFP4 and MXFP6 weights run on the tensor-core engine only.
 gdn_status resolve_plan(const gdn_decode_config& c, int G, Plan* pl) {
-  if (c.qkvz_format == GDN_W_MXFP4) {
+  if (c.qkvz_format != GDN_W_BF16) {
     if (c.engine == GDN_ENGINE_CUDA_CORE) return GDN_ERR_UNSUPPORTED;
     return make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
   }
@@ -326,14 +327,15 @@ bool encode_weight_map(CUtensorMap* m, const void* base, int rows, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile map of MXFP4 codes [rows][H/2] uint8: box 32 bytes (64 codes) x 256
-// rows, no swizzle (the decoding warps read each row's 32 bytes).
-bool encode_code_map(CUtensorMap* m, const void* base, int rows, int H) {
+// Tile map of codes [rows][H * bits / 8] uint8 (MXFP4 4 bits, MXFP6 6 bits a
+// code): box of one k-step's codes (32 or 48 bytes) x 256 rows, no swizzle
+// (the decoding warps read each row's bytes).
+bool encode_code_map(CUtensorMap* m, const void* base, int rows, int H, int bits) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)H / 2, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)H / 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kKStep / 2, (cuuint32_t)kTileM};
+  const cuuint64_t dims[2] = {(cuuint64_t)H * bits / 8, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * bits / 8};
+  const cuuint32_t box[2] = {(cuuint32_t)kKStep * bits / 8, (cuuint32_t)kTileM};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -343,14 +345,15 @@ bool encode_code_map(CUtensorMap* m, const void* base, int rows, int H) {
 // Bytes of in_proj_qkvz as the config stores it.
 size_t qkvz_bytes(const gdn_decode_config& c) {
   const size_t n = (size_t)n_qkvz(c), H = (size_t)c.hidden;
-  return c.qkvz_format == GDN_W_MXFP4 ? n * H / 2 : n * H * 2;
+  return c.qkvz_format == GDN_W_MXFP4 ? n * H / 2 : c.qkvz_format == GDN_W_MXFP6 ? n * H * 3 / 4 : n * H * 2;
 }
 
-// The weight tile maps of a step: in_proj_qkvz (bf16, or MXFP4 codes) and
-// in_proj_ba (bf16).
+// The weight tile maps of a step: in_proj_qkvz (bf16, or MXFP4 / MXFP6
+// codes) and in_proj_ba (bf16).
 bool encode_maps(const gdn_decode_config& c, const gdn_decode_weights* w, CUtensorMap* mq, CUtensorMap* mba) {
-  const bool okq = c.qkvz_format == GDN_W_MXFP4 ? encode_code_map(mq, w->qkvz, n_qkvz(c), c.hidden)
-                                                : encode_weight_map(mq, w->qkvz, n_qkvz(c), c.hidden);
+  const bool okq = c.qkvz_format == GDN_W_BF16
+                       ? encode_weight_map(mq, w->qkvz, n_qkvz(c), c.hidden)
+                       : encode_code_map(mq, w->qkvz, n_qkvz(c), c.hidden, c.qkvz_format == GDN_W_MXFP4 ? 4 : 6);
   return okq && encode_weight_map(mba, w->ba, n_ba(c), c.hidden);
 }
 
@@ -379,7 +382,7 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
   if (!a.x || !a.idx || !a.conv_state || !a.ssm_state || !a.core_out || !a.residual_out) return GDN_ERR_ARG;
   if (!w->input_norm_w || !w->qkvz || !w->ba || !w->conv_w || !w->A_log || !w->dt_bias || !w->gated_norm_w)
     return GDN_ERR_ARG;
-  if (c.qkvz_format == GDN_W_MXFP4 && !w->qkvz_scales) return GDN_ERR_ARG;
+  if (c.qkvz_format != GDN_W_BF16 && !w->qkvz_scales) return GDN_ERR_ARG;
   const void* a16[] = {a.x, a.residual, a.core_out, a.residual_out, a.conv_state, a.ssm_state, w->input_norm_w,
                        w->qkvz, w->ba, w->conv_w, w->gated_norm_w};
   for (const void* q : a16)
@@ -395,7 +398,7 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
   const Rg ins[] = {{a.x, xb}, {a.residual, a.residual ? xb : 0}, {a.idx, (size_t)a.rows * 4},
                     {a.conv_state, convb}, {a.ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
                     {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
-                    {w->qkvz_scales, c.qkvz_format == GDN_W_MXFP4 ? (size_t)n_qkvz(c) * H / 32 : 0},
+                    {w->qkvz_scales, c.qkvz_format != GDN_W_BF16 ? (size_t)n_qkvz(c) * H / 32 : 0},
                     {scratch, scratch_bytes}};
   const Rg outs[] = {{a.core_out, coreb}, {a.residual_out, xb}};
   for (const Rg& o : outs)
@@ -431,7 +434,7 @@ void fill_params(const gdn_decode_config& c, const Plan& pl, const Layout& lay, 
   p->w_in = (const __nv_bfloat16*)w->input_norm_w;
   p->w_qkvz = (const __nv_bfloat16*)w->qkvz;
   p->w_qkvz_scales = w->qkvz_scales;
-  p->fp4 = c.qkvz_format == GDN_W_MXFP4;
+  p->fmt = c.qkvz_format;
   p->w_ba = (const __nv_bfloat16*)w->ba;
   p->conv_w = (const __nv_bfloat16*)w->conv_w;
   p->A_log = w->A_log;

@@ -28,6 +28,9 @@ constexpr uint32_t kStatusDeadline = 4;
 constexpr uint32_t kStatusIndex = 5;
 constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3;
 
+// in_proj_qkvz weight formats (the values of gdn_weight_format).
+constexpr int kFmtBf16 = 0, kFmtMxfp4 = 1, kFmtMxfp6 = 2;
+
 constexpr int kDebugSkipNormPublish = 0x1;
 constexpr int kDebugTimeline = 0x2;
 constexpr int kTlSlots = 48;  // timeline stamps per CTA: 16 phase points, then 16 + 16 per-unit stamps
@@ -69,9 +72,9 @@ struct StepParams {
   int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
   int max_contrib;     // most CTAs contributing to one tile
   int num_ctas;
-  int fp4;             // in_proj_qkvz is MXFP4 (codes + e8m0 scales; tensor-core engine)
+  int fmt;             // in_proj_qkvz format: kFmtBf16, kFmtMxfp4 or kFmtMxfp6 (codes + e8m0 scales)
   int stages;          // bf16 weight tiles in flight per CTA (tensor-core engine)
-  int rstages;         // MXFP4 code tiles in flight per CTA
+  int rstages;         // MXFP4 / MXFP6 code tiles in flight per CTA
   int xslots;          // normed-input k-steps a CTA keeps in shared memory
   unsigned int xpad;   // bytes past the window an MMA may read (and norm-sum scratch)
   float norm_eps, gnorm_eps, l2_eps, q_scale;

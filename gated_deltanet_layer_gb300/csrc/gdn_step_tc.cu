@@ -30,8 +30,8 @@
 //                       row w of the step; the warps split the columns) and
 //                       write the CTA's partial of the tile as tagged words;
 //                       the recurrence tasks reduce the partials they need
-//   warps 2, 3, 5-7,    (MXFP4 in_proj_qkvz) decode each code tile into a
-//   9-11                bf16 tile for the MMA
+//   warps 2, 3, 5-7,    (MXFP4 or MXFP6 in_proj_qkvz) decode each code tile
+//   9-11                into a bf16 tile for the MMA
 // The A operand (xn of the CTA's k-steps, 16 rows, rows past the step's row
 // count zero) is built per launch in shared memory: r = x + residual is
 // staged while the norm hand-off is in flight and normalised in place once
@@ -55,9 +55,14 @@ constexpr uint32_t kWinBytes = kKStep * 2;              // input-norm weights of
 constexpr uint32_t kTmemCols = 2 * kTileM;              // two 256-column f32 accumulators
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(64, kTileM);
 static_assert(kMaxBSlots <= 32, "one owner bit per window slot");
-constexpr uint32_t kRBytes = kTileM * kKStep / 2;      // 8 KB MXFP4 code tile (256 rows x 32 bytes)
-constexpr int kMaxRStages = 4;                          // code tiles in flight per CTA (MXFP4)
-// Warps that decode MXFP4 code tiles into bf16 tiles: thread i of them owns
+// Bytes of one row of a unit's code tile (64 codes: MXFP4 32, MXFP6 48) and
+// of the tile (256 rows).
+template <int FMT>
+__host__ __device__ constexpr uint32_t code_row_bytes() { return FMT == kFmtMxfp6 ? 48u : 32u; }
+template <int FMT>
+__host__ __device__ constexpr uint32_t code_tile_bytes() { return kTileM * code_row_bytes<FMT>(); }
+constexpr int kMaxRStages = 4;                          // code tiles in flight per CTA (MXFP4, MXFP6)
+// Warps that decode MXFP4 / MXFP6 code tiles into bf16 tiles: thread i of them owns
 // row i of the 256-row tile. (Warp 0 holds the TMA producer, warp 1 the MMA
 // issuer, warps 4, 8 and 12 the drain.)
 constexpr int kConvWarps = 8;
@@ -71,10 +76,10 @@ constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on
 }  // namespace
 
 struct TcShared {
-  uint64_t full[kMaxStages];   // bf16 weight tile ready (TMA complete_tx, or the MXFP4 decode done)
+  uint64_t full[kMaxStages];   // bf16 weight tile ready (TMA complete_tx, or the code tile's decode done)
   uint64_t empty[kMaxStages];  // MMAs of the stage done (tcgen05.commit)
-  uint64_t rfull[kMaxRStages];   // MXFP4 code tile landed (TMA complete_tx)
-  uint64_t rempty[kMaxRStages];  // MXFP4 code tile decoded
+  uint64_t rfull[kMaxRStages];   // code tile landed (TMA complete_tx)
+  uint64_t rempty[kMaxRStages];  // code tile decoded
   uint64_t acc_full[2];     // accumulator ready for the drain
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
@@ -150,11 +155,11 @@ __device__ __forceinline__ const CUtensorMap* weight_map(const StepParams& p, in
   return &p.tm_ba;
 }
 
-// A unit whose weights are MXFP4 codes (decoded to bf16 in shared memory
-// before the MMA); the others are bf16 tiles the MMA reads as loaded.
-template <bool FP4>
+// A unit whose weights are MXFP4 or MXFP6 codes (decoded to bf16 in shared
+// memory before the MMA); the others are bf16 tiles the MMA reads as loaded.
+template <int FMT>
 __device__ __forceinline__ bool unit_coded(const StepParams& p, const UnitIter& it) {
-  return FP4 && it.t < p.tiles_qkvz;
+  return FMT != kFmtBf16 && it.t < p.tiles_qkvz;
 }
 
 // Ring positions along a CTA's units: every unit takes the next bf16 stage
@@ -168,16 +173,17 @@ struct RingPos {
   }
 };
 
-// Unit n's weights: MXFP4 codes into code stage pos.r, else a bf16 tile into
+// Unit n's weights: codes into code stage pos.r, else a bf16 tile into
 // stage pos.s (the caller has made sure the stage is free).
-template <bool FP4>
+template <int FMT>
 __device__ __forceinline__ void issue_unit(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
                                            const UnitIter& it, int n, const RingPos& pos, uint64_t pol) {
   int row0;
   const CUtensorMap* m = weight_map(p, it.t, row0);
-  if (unit_coded<FP4>(p, it)) {
-    tc::mbar_arrive_expect_tx(&ts.rfull[pos.r], kRBytes);
-    tc::tma_load_2d(sR + (size_t)pos.r * kRBytes, m, it.ks * (kKStep / 2), row0, &ts.rfull[pos.r], pol);
+  if (unit_coded<FMT>(p, it)) {
+    tc::mbar_arrive_expect_tx(&ts.rfull[pos.r], code_tile_bytes<FMT>());
+    tc::tma_load_2d(sR + (size_t)pos.r * code_tile_bytes<FMT>(), m, it.ks * (int)code_row_bytes<FMT>(), row0,
+                    &ts.rfull[pos.r], pol);
   } else {
     tc::mbar_arrive_expect_tx(&ts.full[pos.s], kWBytes);
     tc::tma_load_2d(sW + (size_t)pos.s * kWBytes, m, it.ks * kKStep, row0, &ts.full[pos.s], pol);
@@ -186,22 +192,22 @@ __device__ __forceinline__ void issue_unit(const StepParams& p, TcShared& ts, ui
 }
 
 // Ring positions after the CTA's first n units.
-template <bool FP4>
+template <int FMT>
 __device__ __forceinline__ RingPos ring_pos_at(const StepParams& p, int ub, int n) {
   RingPos pos;
   UnitIter it(p, ub);
-  for (int j = 0; j < n; ++j, it.next()) pos.advance(p, unit_coded<FP4>(p, it));
+  for (int j = 0; j < n; ++j, it.next()) pos.advance(p, unit_coded<FMT>(p, it));
   return pos;
 }
 
 // The CTA's leading units that fit the rings before any stage is reused (at
 // most `cap`): the ones issued without waiting.
-template <bool FP4>
+template <int FMT>
 __device__ __forceinline__ int prefill_units(const StepParams& p, int ub, int nunits, int cap) {
   UnitIter it(p, ub);
   int coded = 0, n = 0;
   for (; n < min(nunits, cap); ++n, it.next()) {
-    if (unit_coded<FP4>(p, it)) {
+    if (unit_coded<FMT>(p, it)) {
       if (coded == p.rstages) break;
       ++coded;
     } else if (n >= p.stages) {
@@ -213,16 +219,16 @@ __device__ __forceinline__ int prefill_units(const StepParams& p, int ub, int nu
 
 // Units [from, to) of the CTA's weight stream, all within the prefill (one
 // thread, no waits).
-template <bool FP4>
+template <int FMT>
 static __device__ __forceinline__ void start_weight_stream(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                            uint8_t* sR, int ub, int from, int to) {
   if (from >= to) return;
   const uint64_t pol0 = tc::policy_evict_first();
-  RingPos pos = ring_pos_at<FP4>(p, ub, from);
+  RingPos pos = ring_pos_at<FMT>(p, ub, from);
   UnitIter it(p, ub + from);
   for (int n = from; n < to; ++n, it.next()) {
-    issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol0);
-    pos.advance(p, unit_coded<FP4>(p, it));
+    issue_unit<FMT>(p, ts, sW, sR, it, n, pos, pol0);
+    pos.advance(p, unit_coded<FMT>(p, it));
   }
   if (from == 0) tl_stamp_here(p, TL_ISSUED);
 }
@@ -396,7 +402,7 @@ static __device__ __forceinline__ uint4 quantize8_mxfp4(uint4 xv) {
 
 // xn = bf16(r * rstd * (1 + w)) in place; with MXFP4 weights also its
 // quantised copy in the second window sXq (same layout).
-template <bool FP4>
+template <int FMT>
 static __device__ __forceinline__ void finish_normed_slices(const StepParams& p, const SmemPhases& sm,
                                                             uint8_t* sX, uint8_t* sXq, const uint8_t* sWin) {
   const int cta = blockIdx.x, W = p.rows;
@@ -407,7 +413,7 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
     uint4* d = reinterpret_cast<uint4*>(sX + off);
     const uint4 xv = normed8(*d, reinterpret_cast<const uint4*>(sWin + (size_t)j * kWinBytes)[c], sm.rstd[w]);
     *d = xv;
-    if (FP4) *reinterpret_cast<uint4*>(sXq + off) = quantize8_mxfp4(xv);
+    if (FMT == kFmtMxfp4) *reinterpret_cast<uint4*>(sXq + off) = quantize8_mxfp4(xv);
   }
 }
 
@@ -417,20 +423,20 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
 // measured: the tensor form does not bring tiles in early, and per-row
 // prefetches delay the latency-bound norm hand-off more than they shorten
 // the projection.)
-template <bool FP4>
+template <int FMT>
 static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShared& ts, uint8_t* sW, uint8_t* sR,
                                                    int ub, int nunits, int issued, uint64_t pol) {
   const bool leader = (threadIdx.x & 31) == 0;
   UnitIter it(p, ub + issued);
-  RingPos pos = ring_pos_at<FP4>(p, ub, issued);
+  RingPos pos = ring_pos_at<FMT>(p, ub, issued);
   for (int n = issued; n < nunits; ++n) {
-    const bool coded = unit_coded<FP4>(p, it);
+    const bool coded = unit_coded<FMT>(p, it);
     if (coded) {
       if (!pipe_wait_warp(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
     } else if (!pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
       return n;
     }
-    if (leader) issue_unit<FP4>(p, ts, sW, sR, it, n, pos, pol);
+    if (leader) issue_unit<FMT>(p, ts, sW, sR, it, n, pos, pol);
     __syncwarp();
     pos.advance(p, coded);
     it.next();
@@ -438,13 +444,13 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
   return nunits;
 }
 
-// MXFP4 decode (kConvThreads threads, thread i owns row i of the tile): per
+// Code decode (kConvThreads threads, thread i owns row i of the tile): per
 // coded unit, wait for its code tile and for its bf16 stage to be free, turn
-// each row's 64 e2m1 codes and their two e8m0 block scales into bf16
-// (code value x 2^(scale - 127), exact in bf16) in the 128-byte swizzled
-// K-major layout the MMA reads, then release the code stage and hand the bf16
-// stage to the MMA. A row's scales for 8 k-steps are one aligned 16-byte
-// load, issued a block ahead.
+// each row's 64 codes (MXFP4 e2m1 or MXFP6 e2m3) and their two e8m0 block
+// scales into bf16 (code value x 2^(scale - 127), exact in bf16) in the
+// 128-byte swizzled K-major layout the MMA reads, then release the code
+// stage and hand the bf16 stage to the MMA. A row's scales for 8 k-steps are
+// one aligned 16-byte load, issued a block ahead.
 // 2^(e - 127) of an e8m0 byte as bf16x2 (both halves): bf16 exponent field
 // e; e = 0 is 2^-127, the bf16 subnormal 0x0040.
 static __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
@@ -481,6 +487,44 @@ static __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&o)[
   o[2] = prmt(l1, h1, 0x5140u) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
   o[3] = prmt(l1, h1, 0x7362u) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
 }
+// Two e2m3 codes (6 bits: sign bit 5, exponent bits 4..3 with bias 1,
+// mantissa bits 2..0) to a bf16x2 word, c0 in the low half. With exponent
+// field e >= 1 the value (1 + m/8) 2^(e-1) has the bf16 pattern
+// 0x3F00 + ((code & 31) << 4); with e = 0 it is m/8, whose eight bf16
+// patterns (0, 0x3E00, 0x3E80, 0x3EC0, 0x3F00, 0x3F20, 0x3F40, 0x3F60) are
+// looked up bytewise with PRMT; the sign goes to bit 15 / 31.
+static __device__ __forceinline__ uint32_t e2m3x2_to_bf16(uint32_t c0, uint32_t c1) {
+  uint32_t v = (((c0 & 31u) << 4) | ((c1 & 31u) << 20)) + 0x3F003F00u;
+  const uint32_t sel = (c0 & 7u) | ((c1 & 7u) << 4);
+  const uint32_t hi = prmt(0x3E3E3E00u, 0x3F3F3F3Fu, sel), lo = prmt(0xC0800000u, 0x60402000u, sel);
+  const uint32_t sub = prmt(lo, hi, 0x5140u);
+  const uint32_t mask = ((c0 & 24u) ? 0u : 0xFFFFu) | ((c1 & 24u) ? 0u : 0xFFFF0000u);
+  v = (v & ~mask) | (sub & mask);
+  return v | ((c0 & 32u) << 10) | ((c1 & 32u) << 26);
+}
+
+// One row's 64 MXFP6 codes (48 bytes: two 24-byte groups of 32 codes, code i
+// of a group at bits 6i..6i+5 little-endian, so code j of the row starts at
+// bit 6j) to eight 16-byte chunks of bf16 (chunk c: columns 8c..8c+7),
+// scaled by the groups' e8m0 scales.
+static __device__ __forceinline__ void decode_row_mxfp6(const uint8_t* src, const uint32_t (&sc)[2], uint8_t* dst,
+                                                        int swz) {
+  const uint4 q0 = reinterpret_cast<const uint4*>(src)[0], q1 = reinterpret_cast<const uint4*>(src)[1],
+              q2 = reinterpret_cast<const uint4*>(src)[2];
+  const uint32_t w[12] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // chunk c: codes 8c..8c+7, bits 48c..48c+47 of the row
+    const int k = (3 * c) >> 1, off = (c & 1) * 16;
+    const unsigned long long bits = (((unsigned long long)w[k + 1] << 32) | w[k]) >> off;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = mul_bf16x2(e2m3x2_to_bf16((uint32_t)(bits >> (12 * e)) & 63u, (uint32_t)(bits >> (12 * e + 6)) & 63u),
+                        sc[c >> 2]);
+    *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // All-threads-of-a-named-barrier AND of a predicate (every thread gets it).
 static __device__ __forceinline__ bool bar_and(bool v) {
   uint32_t r;
@@ -496,6 +540,7 @@ static __device__ __forceinline__ uint4 scale_block(const StepParams& p, const U
   const int grow = (it.t * kTileM) + row;  // coded units are in_proj_qkvz rows
   return ld_stream_v4(p.w_qkvz_scales + (size_t)grow * (p.H / 32) + (it.ks >> 3) * 16);
 }
+template <int FMT>
 static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                    const uint8_t* sR, int ub, int nunits, int ci) {
   UnitIter it(p, ub);
@@ -507,7 +552,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
   {
     UnitIter f(p, ub);
     for (int n = 0; n < nunits; ++n, f.next())
-      if (unit_coded<true>(p, f)) {
+      if (unit_coded<FMT>(p, f)) {
         nxt = scale_block(p, f, ci);
         nxt_t = f.t;
         nxt_k = f.ks >> 3;
@@ -515,7 +560,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
       }
   }
   for (int n = 0; n < nunits; ++n) {
-    const bool coded = unit_coded<true>(p, it);
+    const bool coded = unit_coded<FMT>(p, it);
     if (coded) {
       if (it.t != blk_t || (it.ks >> 3) != blk_k) {
         // this unit starts a new scale block: take the prefetched one, prefetch the next
@@ -525,7 +570,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
         UnitIter f = it;
         for (int j = n + 1; j < nunits; ++j) {
           f.next();
-          if (unit_coded<true>(p, f) && (f.t != blk_t || (f.ks >> 3) != blk_k)) {
+          if (unit_coded<FMT>(p, f) && (f.t != blk_t || (f.ks >> 3) != blk_k)) {
             nxt = scale_block(p, f, ci);
             nxt_t = f.t;
             nxt_k = f.ks >> 3;
@@ -536,22 +581,26 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
       bool ok = pipe_wait(p, ts, &ts.rfull[pos.r], pos.rph);
       ok = ok && pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1);
       if (!bar_and(ok)) return;  // the same decision in every decoding thread (bounded waits)
-      const uint4* src = reinterpret_cast<const uint4*>(sR + (size_t)pos.r * kRBytes + ci * 32);
-      const uint4 c0 = src[0], c1 = src[1];
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint8_t* row = sR + (size_t)pos.r * code_tile_bytes<FMT>() + ci * code_row_bytes<FMT>();
       const int kk = it.ks & 7;  // k-step within the block: scale bytes 2kk, 2kk + 1
       const uint32_t sw4 = (kk >> 1) == 0 ? cur.x : (kk >> 1) == 1 ? cur.y : (kk >> 1) == 2 ? cur.z : cur.w;
       const uint32_t sword = sw4 >> ((kk & 1) * 16);
       const uint32_t sc[2] = {e8m0_bf16x2(sword & 0xffu), e8m0_bf16x2((sword >> 8) & 0xffu)};
       uint8_t* dst = sW + (size_t)pos.s * kWBytes + ci * 128;
+      if (FMT == kFmtMxfp6) {
+        decode_row_mxfp6(row, sc, dst, ci & 7);
+      } else {
+        const uint4 c0 = reinterpret_cast<const uint4*>(row)[0], c1 = reinterpret_cast<const uint4*>(row)[1];
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 8 columns per 16-byte chunk, from one 32-bit word of codes
-        uint32_t o[4];
-        e2m1x8_to_bf16(words[c], o);
-        const uint32_t scale = sc[c >> 2];
+        for (int c = 0; c < 8; ++c) {  // 8 columns per 16-byte chunk, from one 32-bit word of codes
+          uint32_t o[4];
+          e2m1x8_to_bf16(words[c], o);
+          const uint32_t scale = sc[c >> 2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = mul_bf16x2(o[e], scale);  // exact in bf16
-        *reinterpret_cast<uint4*>(dst + ((c ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int e = 0; e < 4; ++e) o[e] = mul_bf16x2(o[e], scale);  // exact in bf16
+          *reinterpret_cast<uint4*>(dst + ((c ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
       tc::fence_proxy_async_smem();  // the generic-proxy writes, visible to the MMA
       asm volatile("barrier.sync 2, %0;" ::"n"(kConvThreads) : "memory");
@@ -569,7 +618,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
 // the stage's 64 columns into the segment's accumulator; a segment (the units
 // of one group) starts by overwriting. Commits release the stage and, at a
 // segment's end, hand the accumulator to the drain.
-template <bool FP4>
+template <int FMT>
 static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
                                                 uint8_t* sX, uint8_t* sXq, int ub, int nunits, uint32_t tmem) {
   // Stage and phase advance incrementally: a division per unit by the
@@ -606,8 +655,9 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
     int slot = it.ks - ks0;
     if (slot < 0) slot += KS;
     if (n == 0 && leader) tl_stamp_here(p, TL_MMA_FIRST);
-    // MXFP4 in_proj_qkvz: the quantised inputs; bf16 weights: xn itself
-    const uint64_t ad = tc::sdesc_k_sw128((unit_coded<FP4>(p, it) ? sxq0 : sx0) + (uint32_t)slot * kXBytes);
+    // MXFP4 in_proj_qkvz: the quantised inputs (W4A4); bf16 or MXFP6 weights: xn itself
+    const uint64_t ad = tc::sdesc_k_sw128(((FMT == kFmtMxfp4 && unit_coded<FMT>(p, it)) ? sxq0 : sx0) +
+                                          (uint32_t)slot * kXBytes);
     const uint64_t bd = tc::sdesc_k_sw128(sw0 + (uint32_t)s * kWBytes);
     const uint32_t d = tmem + (uint32_t)(seg & 1) * kTileM;
     const bool seg_end = n + 1 == nunits || it.group_end();
@@ -675,19 +725,19 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
 
 // On an exit that skips the projection: wait (bounded) for the TMA loads of
 // the CTA's first n units, all within the prefill (first use of each stage).
-template <bool FP4>
+template <int FMT>
 static __device__ void land_prefill(const StepParams& p, TcShared& ts, int ub, int n) {
   RingPos pos;
   UnitIter it(p, ub);
   for (int j = 0; j < n; ++j, it.next()) {
-    const bool coded = unit_coded<FP4>(p, it);
+    const bool coded = unit_coded<FMT>(p, it);
     cleanup_wait(coded ? &ts.rfull[pos.r] : &ts.full[pos.s], 0);
     pos.advance(p, coded);
   }
 }
 // On an aborted projection: wait (bounded) for the last TMA load issued into
 // each stage of either ring (units [0, issued)).
-template <bool FP4>
+template <int FMT>
 static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, int issued) {
   int last_s[kMaxStages], last_r[kMaxRStages];
   uint32_t ph_s[kMaxStages], ph_r[kMaxRStages];
@@ -696,7 +746,7 @@ static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, in
   RingPos pos;
   UnitIter it(p, ub);
   for (int j = 0; j < issued; ++j, it.next()) {
-    const bool coded = unit_coded<FP4>(p, it);
+    const bool coded = unit_coded<FMT>(p, it);
     if (coded) {
       last_r[pos.r] = j;
       ph_r[pos.r] = pos.rph;
@@ -712,19 +762,20 @@ static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, in
     if (last_r[i] >= 0) cleanup_wait(&ts.rfull[i], ph_r[i]);
 }
 
-// FP4: the instantiation for MXFP4 in_proj_qkvz (it alone carries the
-// decoding warps' code; p.fp4 equals FP4).
-template <bool HAS_RES, bool STATE_BF16, int DK, bool FP4>
+// FMT: the in_proj_qkvz weight format (kFmtBf16, kFmtMxfp4, kFmtMxfp6; the
+// coded formats alone carry the decoding warps' code; p.fmt equals FMT).
+template <bool HAS_RES, bool STATE_BF16, int DK, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemPhases sm;
   __shared__ SmemTask st;
   __shared__ TcShared ts;
   uint8_t* sW = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-  uint8_t* sR = sW + (size_t)p.stages * kWBytes;                      // MXFP4 code ring
-  uint8_t* sX = sR + (size_t)p.rstages * kRBytes;                     // normed-input window
-  uint8_t* sXq = sX + (size_t)p.xslots * kXBytes;                     // its MXFP4-quantised copy
-  uint8_t* sPad = sX + (size_t)(p.fp4 ? 2 : 1) * p.xslots * kXBytes;  // read past the windows; scratch
+  constexpr int kWindows = FMT == kFmtMxfp4 ? 2 : 1;                         // xn (and its MXFP4 copy)
+  uint8_t* sR = sW + (size_t)p.stages * kWBytes;                             // code ring
+  uint8_t* sX = sR + (size_t)p.rstages * code_tile_bytes<FMT>();             // normed-input window
+  uint8_t* sXq = sX + (size_t)p.xslots * kXBytes;                            // its MXFP4-quantised copy
+  uint8_t* sPad = sX + (size_t)kWindows * p.xslots * kXBytes;                // read past the windows; scratch
   uint8_t* sWin = sPad + p.xpad;
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
   // Without early weight reads nothing is read before the previous kernel in
@@ -760,9 +811,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // kFirstTiles go out now: the x and residual loads that start the norm
   // hand-off would otherwise queue behind a whole ring's worth of weights in
   // HBM. The rest of the ring follows once the norm partials are out.
-  const int issued = prefill_units<FP4>(p, ub, nunits, kMaxStages + kMaxRStages);
+  const int issued = prefill_units<FMT>(p, ub, nunits, kMaxStages + kMaxRStages);
   const int first = min(issued, kFirstTiles);
-  if (tid == 32) start_weight_stream<FP4>(p, ts, sW, sR, ub, 0, first);
+  if (tid == 32) start_weight_stream<FMT>(p, ts, sW, sR, ub, 0, first);
   const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
   griddep_wait();  // from here on the previous kernel's writes are visible (a no-op if already waited)
   griddep_launch_dependents();
@@ -774,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   __syncthreads();
   if (!sm.flag) {  // sticky error: every later launch returns at once
-    if (tid == 32) land_prefill<FP4>(p, ts, ub, first);  // once the weight tiles in flight have landed
+    if (tid == 32) land_prefill<FMT>(p, ts, ub, first);  // once the weight tiles in flight have landed
     return;
   }
   tl_stamp(p, TL_START);
@@ -788,17 +839,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tl_stamp(p, TL_R_STAGED);
   const int L = sm.L;
   publish_norm_partials(p, sq, L);
-  if (tid == 32) start_weight_stream<FP4>(p, ts, sW, sR, ub, first, issued);
+  if (tid == 32) start_weight_stream<FMT>(p, ts, sW, sR, ub, first, issued);
   write_residual_out(p, sX);
   if (!phase_wait_rstd(p, sm, L)) {
-    if (tid == 32) land_prefill<FP4>(p, ts, ub, issued);  // let the weight tiles in flight land
+    if (tid == 32) land_prefill<FMT>(p, ts, ub, issued);  // let the weight tiles in flight land
     if (warp == 1) {
       tc::tc_fence_after();
       tc::tmem_dealloc(ts.tmem_base, kTmemCols);
     }
     return;
   }
-  finish_normed_slices<FP4>(p, sm, sX, sXq, sWin);
+  finish_normed_slices<FMT>(p, sm, sX, sXq, sWin);
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -814,18 +865,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   int issued_total = issued;
   if (nunits > 0) {
     if (warp == 0)
-      issued_total = producer_loop<FP4>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
+      issued_total = producer_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
     else if (warp == 1)
-      mma_loop<FP4>(p, ts, sW, sX, sXq, ub, nunits, tmem);
+      mma_loop<FMT>(p, ts, sW, sX, sXq, ub, nunits, tmem);
     else if (warp == 4 || warp == 8 || warp == 12)
       drain_loop(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
-    else if (FP4 && conv_index(warp) >= 0)
-      decode_loop(p, ts, sW, sR, ub, nunits, conv_index(warp) * 32 + (tid & 31));
+    else if (FMT != kFmtBf16 && conv_index(warp) >= 0)
+      decode_loop<FMT>(p, ts, sW, sR, ub, nunits, conv_index(warp) * 32 + (tid & 31));
   }
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
-  if (aborted && tid == 0) land_issued<FP4>(p, ts, ub, issued_total);  // TMA in flight lands before exit
+  if (aborted && tid == 0) land_issued<FMT>(p, ts, ub, issued_total);  // TMA in flight lands before exit
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -837,29 +888,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
 }
 
-const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, bool fp4) {
+const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt) {
 #define GDN_PICK(R, B, D, F) \
-  if (has_res == R && state_bf16 == B && dk == D && fp4 == F) return (const void*)&gdn_step_tc_kernel<R, B, D, F>;
-  GDN_PICK(true, false, 128, false) GDN_PICK(true, true, 128, false) GDN_PICK(false, false, 128, false)
-  GDN_PICK(false, true, 128, false) GDN_PICK(true, false, 64, false) GDN_PICK(true, true, 64, false)
-  GDN_PICK(false, false, 64, false) GDN_PICK(false, true, 64, false)
-  // MXFP4 in_proj_qkvz: head dim 128
-  GDN_PICK(true, false, 128, true) GDN_PICK(true, true, 128, true) GDN_PICK(false, false, 128, true)
-  GDN_PICK(false, true, 128, true)
+  if (has_res == R && state_bf16 == B && dk == D && fmt == F) return (const void*)&gdn_step_tc_kernel<R, B, D, F>;
+  GDN_PICK(true, false, 128, kFmtBf16) GDN_PICK(true, true, 128, kFmtBf16) GDN_PICK(false, false, 128, kFmtBf16)
+  GDN_PICK(false, true, 128, kFmtBf16) GDN_PICK(true, false, 64, kFmtBf16) GDN_PICK(true, true, 64, kFmtBf16)
+  GDN_PICK(false, false, 64, kFmtBf16) GDN_PICK(false, true, 64, kFmtBf16)
+  // MXFP4 and MXFP6 in_proj_qkvz: head dim 128
+  GDN_PICK(true, false, 128, kFmtMxfp4) GDN_PICK(true, true, 128, kFmtMxfp4) GDN_PICK(false, false, 128, kFmtMxfp4)
+  GDN_PICK(false, true, 128, kFmtMxfp4)
+  GDN_PICK(true, false, 128, kFmtMxfp6) GDN_PICK(true, true, 128, kFmtMxfp6) GDN_PICK(false, false, 128, kFmtMxfp6)
+  GDN_PICK(false, true, 128, kFmtMxfp6)
 #undef GDN_PICK
   return nullptr;
 }
 
-// Dynamic shared memory of a launch: the bf16 weight ring, the MXFP4 code
-// ring, the normed-input window (and with MXFP4 weights its quantised copy)
-// with the pad an M = 64 MMA reads past the last slice (also the norm sums'
-// scratch), the window's input-norm weights, and 1 KB of alignment.
+// Dynamic shared memory of a launch: the bf16 weight ring, the code ring
+// (MXFP4 or MXFP6), the normed-input window (and with MXFP4 weights its
+// quantised copy) with the pad an M = 64 MMA reads past the last slice (also
+// the norm sums' scratch), the window's input-norm weights, and 1 KB of
+// alignment.
 uint32_t tensor_core_xpad(int xslots) {
   const uint32_t sums = (uint32_t)(kMaxRows * xslots * 8 * sizeof(float));
   return sums > kXPadMin ? (sums + 127) / 128 * 128 : kXPadMin;
 }
-size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, bool fp4) {
-  return (size_t)stages * kWBytes + (size_t)rstages * kRBytes + (size_t)(fp4 ? 2 : 1) * xslots * kXBytes +
+size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, int fmt) {
+  const size_t rtile = fmt == kFmtMxfp6 ? code_tile_bytes<kFmtMxfp6>() : code_tile_bytes<kFmtMxfp4>();
+  return (size_t)stages * kWBytes + (size_t)rstages * rtile + (size_t)(fmt == kFmtMxfp4 ? 2 : 1) * xslots * kXBytes +
          tensor_core_xpad(xslots) + (size_t)xslots * kWinBytes + 1024;
 }
 size_t tensor_core_static_smem() { return sizeof(SmemPhases) + sizeof(SmemTask) + sizeof(TcShared); }

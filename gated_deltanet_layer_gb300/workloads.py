@@ -18,6 +18,10 @@ Value distributions (one recipe for every shape):
   MXFP4 in_proj_qkvz                      e2m1 codes uniform over all 16
                                           codes, block exponents ~ U{-8..-4}
                                           (e8m0 byte = 127 + exponent)
+  MXFP6 in_proj_qkvz                      packed code bytes uniform (so the
+                                          e2m3 codes are uniform over all 64),
+                                          block exponents ~ U{-10..-6} (weight
+                                          std ~0.03, the bf16 layers' scale)
 """
 from __future__ import annotations
 
@@ -40,7 +44,7 @@ class LayerShape:
     num_slots: int
     conv_kernel: int = 4
     ssm_dtype: str = "f32"  # "f32" or "bf16"
-    qkvz_format: str = "bf16"  # "bf16" or "mxfp4"
+    qkvz_format: str = "bf16"  # "bf16", "mxfp4" or "mxfp6"
     max_rows: int = 16
     norm_eps: float = 1e-6
     gated_norm_eps: float = 1e-6
@@ -75,6 +79,8 @@ class LayerShape:
         H = self.hidden
         if self.qkvz_format == "mxfp4":
             qkvz = self.n_qkvz * (H // 2) + self.n_qkvz * (H // 32)
+        elif self.qkvz_format == "mxfp6":
+            qkvz = self.n_qkvz * (H * 3 // 4) + self.n_qkvz * (H // 32)
         else:
             qkvz = self.n_qkvz * H * 2
         ba = self.n_ba * H * 2
@@ -100,10 +106,10 @@ class LayerShape:
                 + rows * self.activation_bytes_per_row(first_layer))
 
 
-# The five workloads: a tiny correctness layer, one tensor-parallel rank's
-# shard of a large layer, the same large layer unsharded, the shard with a
-# bf16 state (first-layer variant and pad rows in its cases), and a dense
-# layer with an MXFP4 in_proj_qkvz.
+# The workloads: a tiny correctness layer, one tensor-parallel rank's shard
+# of a large layer, the same large layer unsharded, the shard with a bf16
+# state (first-layer variant and pad rows in its cases), and a dense layer
+# with an MXFP4 or an MXFP6 in_proj_qkvz.
 TINY = LayerShape("tiny", hidden=1024, num_k_heads=4, num_v_heads=8,
                   head_k_dim=64, head_v_dim=64, num_slots=16)
 SHARD = LayerShape("shard", hidden=8192, num_k_heads=2, num_v_heads=8,
@@ -115,7 +121,9 @@ DENSE_MXFP4 = LayerShape("dense_mxfp4", hidden=5120, num_k_heads=16, num_v_heads
                          head_k_dim=128, head_v_dim=128, num_slots=20,
                          qkvz_format="mxfp4")
 
-SHAPES = {s.name: s for s in (TINY, SHARD, FULL, SHARD_BF16, DENSE_MXFP4)}
+DENSE_MXFP6 = DENSE_MXFP4.with_(name="dense_mxfp6", qkvz_format="mxfp6")
+
+SHAPES = {s.name: s for s in (TINY, SHARD, FULL, SHARD_BF16, DENSE_MXFP4, DENSE_MXFP6)}
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -144,6 +152,12 @@ def make_weights(shape: LayerShape, seed: int, *, weight_std: float = 0.02,
         packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
         exps = rng.integers(-8, -3, size=(n, H // 32))
         w["qkvz"] = torch.from_numpy(np.ascontiguousarray(packed))
+        w["qkvz_scales"] = torch.from_numpy((127 + exps).astype(np.uint8))
+    elif shape.qkvz_format == "mxfp6":
+        n = shape.n_qkvz
+        packed = rng.integers(0, 256, size=(n, H * 3 // 4), dtype=np.uint8)
+        exps = rng.integers(-10, -5, size=(n, H // 32))
+        w["qkvz"] = torch.from_numpy(packed)
         w["qkvz_scales"] = torch.from_numpy((127 + exps).astype(np.uint8))
     else:
         w["qkvz"] = _bf16(_normal(rng, (shape.n_qkvz, H), weight_std))

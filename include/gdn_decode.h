@@ -46,6 +46,14 @@
  *                              tensor-core engine only, H a multiple of
  *                              512, dk = 128; the normed input is then
  *                              quantised to MXFP4 per block of 32 as well
+ *  qkvz (MXFP6)                codes [Nqkvz][3H/4] uint8: each block of 32
+ *                              OCP E2M3 codes (sign bit 5, 2 exponent and 3
+ *                              mantissa bits) is 24 bytes, code i at bits
+ *                              6i..6i+5 little-endian; qkvz_scales as for
+ *                              MXFP4; the normed input stays bf16 (W6A16;
+ *                              vLLM #60833, review "How to make the MXFP6
+ *                              weights"); tensor-core engine only, H a
+ *                              multiple of 512, dk = 128
  *  ba                          [Nba][H] bf16, rows b(Hv) | a(Hv)
  *  conv_w                      [C][K] bf16, tap K-1 multiplies the new input
  *  input_norm_w                [H] bf16 (Gemma form: x * rstd * (1 + w))
@@ -82,7 +90,7 @@ typedef enum {
 #define GDN_MAX_ROWS 64
 
 typedef enum { GDN_STATE_F32 = 0, GDN_STATE_BF16 = 1 } gdn_state_dtype;
-typedef enum { GDN_W_BF16 = 0, GDN_W_MXFP4 = 1 } gdn_weight_format;
+typedef enum { GDN_W_BF16 = 0, GDN_W_MXFP4 = 1, GDN_W_MXFP6 = 2 } gdn_weight_format;
 
 /* Which unit runs the in_proj_qkvz / in_proj_ba dot products. */
 typedef enum {
@@ -142,8 +150,8 @@ typedef struct {
 
 typedef struct {
   const void* input_norm_w;     /* [H] bf16 */
-  const void* qkvz;             /* [Nqkvz][H] bf16, or [Nqkvz][H/2] uint8 MXFP4 codes */
-  const uint8_t* qkvz_scales;   /* [Nqkvz][H/32] e8m0; MXFP4 only, else NULL */
+  const void* qkvz;             /* [Nqkvz][H] bf16, [Nqkvz][H/2] MXFP4 or [Nqkvz][3H/4] MXFP6 codes */
+  const uint8_t* qkvz_scales;   /* [Nqkvz][H/32] e8m0; MXFP4 / MXFP6 only, else NULL */
   const void* ba;               /* [Nba][H] bf16 */
   const void* conv_w;           /* [C][K] bf16 */
   const float* A_log;           /* [Hv] f32 */

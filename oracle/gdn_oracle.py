@@ -315,17 +315,19 @@ def mxfp6_quantize_block(v):
 
 def mxfp6_quantize_matrix(W):
     """[N, K] weights (K a multiple of 32) to E2M3 codes [N, K] and e8m0
-    scale bytes [N, K/32], block by block along K."""
+    scale bytes [N, K/32]: mxfp6_quantize_block's steps applied to every
+    block of 32 along K at once."""
     W = np.asarray(W, dtype=np.float64)
     N, K = W.shape
-    codes = np.empty((N, K), dtype=np.uint8)
-    scales = np.empty((N, K // 32), dtype=np.uint8)
-    for n in range(N):
-        for b in range(K // 32):
-            c, _, byte = mxfp6_quantize_block(W[n, 32 * b:32 * b + 32])
-            codes[n, 32 * b:32 * b + 32] = c
-            scales[n, b] = byte
-    return codes, scales
+    v = W.reshape(N, K // 32, 32)
+    amax = np.max(np.abs(v), axis=-1).astype(np.float32)
+    bits = amax.view(np.uint32).astype(np.int64)
+    e_field = ((bits + (1 << 19)) >> 23) & 0xFF
+    exp = np.clip(e_field - 127 - 2, -126, 127)
+    mag = _e2m3_round_magnitude(np.abs(v) / np.ldexp(1.0, exp)[..., None])
+    codes = _e2m3_code(mag)
+    codes = np.where(np.signbit(v) & (mag > 0), codes | 32, codes).astype(np.uint8)
+    return codes.reshape(N, K), (exp + 127).astype(np.uint8)
 
 
 def mxfp6_pack(codes):

@@ -173,11 +173,41 @@ def test_dense_mxfp4_first_layer_with_pad_rows():
     _run(WL.DENSE_MXFP4, 9, 8100, "tcgen05", first_layer=True, pad_rows=WL.default_pad_rows(9))
 
 
+# The dense layer with MXFP6 E2M3 in_proj_qkvz (W6A16: bf16 activations).
+@pytest.mark.parametrize("rows", [1, 6, 16])
+def test_dense_mxfp6_layer(rows):
+    _run(WL.DENSE_MXFP6, rows, 8200 + rows, "auto")
+
+
+def test_dense_mxfp6_first_layer_bf16_state_with_pad_rows():
+    _run(WL.DENSE_MXFP6.with_(ssm_dtype="bf16"), 9, 8300, "tcgen05", first_layer=True,
+         pad_rows=WL.default_pad_rows(9))
+
+
+def test_dense_mxfp6_weights_made_as_the_pages_make_them():
+    """bf16 weights ~N(0, 0.02) rounded to E2M3 block by block and packed
+    (the review comment's steps 2 and 3, by the oracle's quantiser), then
+    the whole step against the oracle on the packed weights."""
+    from oracle import gdn_oracle as O
+    shape = WL.DENSE_MXFP6
+    case = Case(shape, 5, 8400)
+    dense = WL.make_weights(shape.with_(qkvz_format="bf16"), 8401)["qkvz"].to(torch.float64).numpy()
+    codes, scales = O.mxfp6_quantize_matrix(dense)
+    case.w["qkvz"] = torch.from_numpy(O.mxfp6_pack(codes))
+    case.w["qkvz_scales"] = torch.from_numpy(scales)
+    case.to_device()
+    layer = GdnDecode(shape)
+    core, res_out = case.run_gpu(layer)
+    assert layer.check()[0] == 0
+    compare(case, case.run_oracle(), core, res_out)
+
+
 def test_mxfp4_needs_the_tensor_core_engine():
     from gated_deltanet_layer_gb300 import GdnError, _native
-    with pytest.raises(GdnError) as e:
-        GdnDecode(WL.DENSE_MXFP4, engine="cuda_core")
-    assert e.value.code == _native.GDN_ERR_UNSUPPORTED
+    for shape in (WL.DENSE_MXFP4, WL.DENSE_MXFP6):
+        with pytest.raises(GdnError) as e:
+            GdnDecode(shape, engine="cuda_core")
+        assert e.value.code == _native.GDN_ERR_UNSUPPORTED
 
 
 # Steps wider than one launch's 16 rows run as one launch per tile of 16

@@ -553,6 +553,18 @@ def test_mxfp6_quantize_block_scale_rule():
         assert np.all(np.abs(deq - v) <= 0.25 * 2.0**exp + 1e-300)
 
 
+def test_mxfp6_quantize_matrix_is_the_block_rule_everywhere():
+    rng = np.random.default_rng(19)
+    W = rng.standard_normal((6, 128)) * 10.0 ** rng.uniform(-3, 1, size=(6, 1))
+    W[2, 32:64] = 0.0  # an all-zero block
+    codes, scales = O.mxfp6_quantize_matrix(W)
+    for n in range(6):
+        for b in range(4):
+            c, _, byte = O.mxfp6_quantize_block(W[n, 32 * b:32 * b + 32])
+            np.testing.assert_array_equal(codes[n, 32 * b:32 * b + 32], c)
+            assert scales[n, b] == byte
+
+
 def test_mxfp6_packing_bit_positions():
     """32 codes in 24 bytes, code i at bits 6i..6i+5 of the little-endian
     group (review comment step 3); bytes worked by hand."""
