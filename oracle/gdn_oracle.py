@@ -58,7 +58,7 @@ __all__ = [
     "mxfp4_unpack_codes", "mxfp4_quantize_block", "mxfp4_quantize_row",
     "project_mxfp4", "e2m3_value", "mxfp6_quantize_block", "mxfp6_quantize_matrix",
     "mxfp6_pack", "mxfp6_unpack", "project_mxfp6", "split_projection", "conv_update", "l2norm",
-    "gates", "delta_rule", "gated_rmsnorm", "gdn_step",
+    "gates", "delta_rule", "gated_rmsnorm", "gdn_step", "gdn_verify",
 ]
 
 # --------------------------------------------------------------------------
@@ -528,3 +528,76 @@ def gdn_step(shape, x, residual, weights, state_indices, conv_state, ssm_state):
         "residual_out": r, "core": core, "conv_state": conv_new, "ssm_state": ssm_new,
         "index_error": index_error, "xn": xn, "p_qkvz": p_qkvz, "p_ba": p_ba,
     }
+
+
+# --------------------------------------------------------------------------
+# Multi-token verify with a state per token (the follow-up the pages name:
+# sgl-amd-mono #89, Motivation, "keeps no state for each draft token, so a
+# rejected draft token cannot roll back"; vLLM #60833, Details,
+# "Limitations / follow-ups": MTP verify steps). Reading: sequence s has T
+# tokens, rows s*T .. s*T + T - 1; it starts from slot state_in[s], and after
+# token t its conv and SSM state go to their own slot state_out[s, t]. Each
+# token continues from the state as stored (f32 or bf16), so the T tokens
+# give what T decode steps would, and accepting the first a tokens means
+# taking slot state_out[s, a - 1]. A sequence with state_in <= 0 is padding.
+# --------------------------------------------------------------------------
+
+def gdn_verify(shape, x, residual, weights, state_in, state_out, conv_state, ssm_state):
+    """One verify step: len(state_in) sequences of T = state_out.shape[1]
+    tokens. Arguments as for gdn_step, plus state_in [S] and state_out [S, T]
+    int32 slots. Returns a dict as gdn_step's (residual_out, core, conv_state,
+    ssm_state, index_error); the input state arrays are not modified."""
+    H, Hk, Hv = shape.hidden, shape.num_k_heads, shape.num_v_heads
+    dk, dv = shape.head_k_dim, shape.head_v_dim
+    G = Hv // Hk
+    sin = np.asarray(state_in, dtype=np.int64)
+    sout = np.asarray(state_out, dtype=np.int64)
+    S, T = sout.shape
+    conv_new = np.array(conv_state, dtype=np.float64, copy=True)
+    ssm_new = np.array(ssm_state, dtype=np.float64, copy=True)
+
+    r = residual_add(x, residual)
+    xn = gemma_rmsnorm(r, weights["input_norm_w"], shape.norm_eps)
+    if shape.qkvz_format == "mxfp4":
+        p_qkvz = project_mxfp4(xn, weights["qkvz"], weights["qkvz_scales"])
+    elif shape.qkvz_format == "mxfp6":
+        p_qkvz = project_mxfp6(xn, weights["qkvz"], weights["qkvz_scales"])
+    else:
+        p_qkvz = project_bf16(xn, weights["qkvz"])
+    p_ba = project_bf16(xn, weights["ba"])
+    q, k, v, z, b, a = split_projection(p_qkvz, p_ba, Hk, Hv, dk, dv)
+
+    core = np.zeros((S * T, Hv * dv))
+    index_error = False
+    for s in range(S):
+        slot = int(sin[s])
+        outs = [int(o) for o in sout[s]]
+        if slot >= shape.num_slots or any(o <= 0 or o >= shape.num_slots for o in outs):
+            index_error = True
+            continue
+        if slot <= 0:
+            continue  # a padding sequence: zero core rows, no state read or written
+        conv_prev = conv_state[slot]
+        ssm_prev = ssm_state[slot]
+        for t in range(T):
+            w = s * T + t
+            u = np.concatenate([q[w].reshape(-1), k[w].reshape(-1), v[w].reshape(-1)])
+            y, conv_t = conv_update(conv_prev, weights["conv_w"], u)
+            yq = y[:Hk * dk].reshape(Hk, dk)
+            yk = y[Hk * dk:2 * Hk * dk].reshape(Hk, dk)
+            yv = y[2 * Hk * dk:].reshape(Hv, dv)
+            qn = l2norm(yq, shape.l2_eps) * shape.scale_q
+            kn = l2norm(yk, shape.l2_eps)
+            g, beta = gates(a[w], b[w], weights["A_log"], weights["dt_bias"])
+            ssm_t = np.empty_like(ssm_prev, dtype=np.float64)
+            for h in range(Hv):
+                kh = h // G
+                St, o = delta_rule(ssm_prev[h], kn[kh], yv[h], qn[kh], g[h], beta[h])
+                ssm_t[h] = bf16_round(St) if shape.ssm_dtype == "bf16" else f32_round(St)
+                core[w, h * dv:(h + 1) * dv] = gated_rmsnorm(o, z[w, h], weights["gated_norm_w"],
+                                                             shape.gated_norm_eps)
+            conv_new[outs[t]] = conv_t
+            ssm_new[outs[t]] = ssm_t
+            conv_prev, ssm_prev = conv_t, ssm_t
+    return {"residual_out": r, "core": core, "conv_state": conv_new, "ssm_state": ssm_new,
+            "index_error": index_error, "xn": xn, "p_qkvz": p_qkvz, "p_ba": p_ba}

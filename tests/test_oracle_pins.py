@@ -599,3 +599,71 @@ def test_project_mxfp6_brute_force():
             total = sum(table[int(codes[n, h])] * Fraction(2) ** (int(scales[n, h // 32]) - 127) * Fraction(float(xn[w, h]))
                         for h in range(K))
             assert got[w, n] == O.bf16_round(float(total))
+
+
+
+# ---------------------------------------------------------------- multi-token verify
+
+def _verify_case(shape, S, T, seed, pad=()):
+    rng = np.random.default_rng(seed)
+    x, res, w, _, conv, ssm = _np_inputs(shape, S * T, seed)
+    slots = rng.permutation(np.arange(1, shape.num_slots))[:S + S * T]
+    sin = slots[:S].astype(np.int32)
+    sout = slots[S:].reshape(S, T).astype(np.int32)
+    for s in pad:
+        sin[s] = 0
+    return x, res, w, sin, sout, conv, ssm
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_verify_equals_sequential_decode_steps(T):
+    """Verifying T tokens equals T decode steps: the t-th token's core row
+    and its state slot are those of the t-th of T gdn_step calls, each on
+    the state the previous one stored (the state-per-token reading)."""
+    shape = WL.TINY.with_(num_slots=64)
+    S = 3
+    x, res, w, sin, sout, conv, ssm = _verify_case(shape, S, T, 170 + T)
+    out = O.gdn_verify(shape, x, res, w, sin, sout, conv, ssm)
+    for s in range(S):
+        c, m = conv.copy(), ssm.copy()
+        for t in range(T):
+            row = s * T + t
+            step = O.gdn_step(shape, x[row:row + 1], res[row:row + 1], w, np.array([sin[s]], np.int32), c, m)
+            np.testing.assert_array_equal(out["core"][row], step["core"][0])
+            np.testing.assert_array_equal(out["residual_out"][row], step["residual_out"][0])
+            np.testing.assert_array_equal(out["ssm_state"][sout[s, t]], step["ssm_state"][sin[s]])
+            np.testing.assert_array_equal(out["conv_state"][sout[s, t]], step["conv_state"][sin[s]])
+            c, m = step["conv_state"], step["ssm_state"]  # the next step reads what this one stored
+    # the input slots are read, never written
+    np.testing.assert_array_equal(out["ssm_state"][sin], ssm[sin])
+    np.testing.assert_array_equal(out["conv_state"][sin], conv[sin])
+
+
+def test_verify_bf16_state_continues_from_the_stored_state():
+    shape = WL.TINY.with_(num_slots=64, ssm_dtype="bf16")
+    x, res, w, sin, sout, conv, ssm = _verify_case(shape, 2, 3, 180)
+    ssm = O.bf16_round(ssm)
+    out = O.gdn_verify(shape, x, res, w, sin, sout, conv, ssm)
+    for s in range(2):
+        m = ssm.copy()
+        c = conv.copy()
+        for t in range(3):
+            row = s * 3 + t
+            step = O.gdn_step(shape, x[row:row + 1], res[row:row + 1], w, np.array([sin[s]], np.int32), c, m)
+            np.testing.assert_array_equal(out["ssm_state"][sout[s, t]], step["ssm_state"][sin[s]])
+            c, m = step["conv_state"], step["ssm_state"]
+        assert np.array_equal(O.bf16_round(out["ssm_state"][sout[s, 2]]), out["ssm_state"][sout[s, 2]])
+
+
+def test_verify_padding_sequence_and_untouched_slots():
+    shape = WL.TINY.with_(num_slots=64)
+    S, T = 3, 2
+    x, res, w, sin, sout, conv, ssm = _verify_case(shape, S, T, 190, pad=(1,))
+    out = O.gdn_verify(shape, x, res, w, sin, sout, conv, ssm)
+    assert np.all(out["core"][2:4] == 0.0)
+    written = set(int(o) for s in (0, 2) for o in sout[s])
+    others = [i for i in range(shape.num_slots) if i not in written]
+    np.testing.assert_array_equal(out["ssm_state"][others], ssm[others])
+    np.testing.assert_array_equal(out["conv_state"][others], conv[others])
+    bad = sout.copy(); bad[0, 1] = shape.num_slots
+    assert O.gdn_verify(shape, x, res, w, sin, bad, conv, ssm)["index_error"]
