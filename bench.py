@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--workload", default="full")
     ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
     ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width tables")
-    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,dense_mxfp6,shard_wide",
+    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,dense_mxfp6,shard_wide,shard_verify",
                     help="workloads of the per-width tables ('' for none)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--engine", default="auto")
@@ -79,6 +79,8 @@ TABLES = {
     "dense_mxfp6": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
     # steps wider than one launch (one launch per 16-row tile)
     "shard_wide": {"shape": "shard", "max_rows": 64, "widths": [16, 24, 32, 48, 64]},
+    # verify steps: (sequences, tokens) with a state slot per token
+    "shard_verify": {"shape": "shard", "verify": [(1, 2), (1, 4), (2, 4), (4, 4), (8, 2), (2, 8)]},
 }
 
 
@@ -304,6 +306,37 @@ class Rig:
         torch.cuda.synchronize()
         return graph
 
+    def capture_verify(self, seqs, tokens, n):
+        """A CUDA graph of n verify steps (seqs sequences of `tokens` tokens,
+        fresh random input and per-token output slots each), each on the next
+        weight copy."""
+        import torch
+        sh = self.shape
+        steps = []
+        for _ in range(min(n, 64)):
+            perm = torch.randperm(sh.num_slots - 1, generator=self.g, device="cuda")[:seqs * (tokens + 1)] + 1
+            perm = perm.to(torch.int32)
+            rows = seqs * tokens
+            steps.append((self.bf16(rows, sh.hidden, std=1.0), self.bf16(rows, sh.hidden, std=1.0),
+                          perm[:seqs].contiguous(), perm[seqs:].reshape(seqs, tokens).contiguous(),
+                          torch.empty(rows, sh.num_v_heads * sh.head_v_dim, dtype=torch.bfloat16, device="cuda"),
+                          torch.empty(rows, sh.hidden, dtype=torch.bfloat16, device="cuda")))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            x, r, si, so, c, ro = steps[0]
+            self.layer.verify(x, r, self.copies[0], si, so, self.conv, self.ssm, c, ro, weights_struct=self.wstructs[0])
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(graph, stream=s):
+                for k in range(n):
+                    x, r, si, so, c, ro = steps[k % len(steps)]
+                    self.layer.verify(x, r, self.copies[k % self.ncopy], si, so, self.conv, self.ssm, c, ro,
+                                      weights_struct=self.wstructs[k % self.ncopy])
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return graph
+
     def check(self):
         st, detail = self.layer.check()
         if st != 0:
@@ -436,6 +469,25 @@ def native(args):
             torch.cuda.empty_cache()
             tshape = WL.SHAPES[rec.get("shape", name)].with_(max_rows=rec.get("max_rows", 16))
             rig = Rig(tshape, g, l2, args.engine, rec.get("min_copies", 4))
+        if "verify" in rec:
+            vt = {}
+            for S, T in rec["verify"]:
+                gg = rig.capture_verify(S, T, 100)
+                times = []
+                t_end = time.time() + 0.3
+                while time.time() < t_end or len(times) < 5:
+                    times.append(time_graph(gg) * 10.0)
+                times.sort()
+                u = times[len(times) // 2]
+                b = rig.shape.verify_bytes(S, T)
+                vt[f"{S}x{T}"] = {"us": round(u, 3), "GBps": round(b / u / 1e3, 1),
+                                  "frac_of_" + peak_kind: round(b / u / 1e3 / peak, 4), "bytes": b,
+                                  "rows": S * T, "launches": -(-S // (16 // T))}
+                del gg
+            rig.check()
+            tables[name] = {"copies": rig.ncopy, "verify": vt}
+            rig = None
+            continue
         ws = rec["widths"] if name != args.workload else sorted(set(rec["widths"]) | set(widths))
         tables[name] = {"copies": rig.ncopy, "first_layer": rec.get("first_layer", False),
                         "pad_fraction": rec.get("pad", 0.0),

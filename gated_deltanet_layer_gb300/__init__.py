@@ -108,6 +108,31 @@ class GdnDecode:
             raise GdnError("gdn_decode_step", st)
         return core_out, residual_out
 
+    def verify(self, x, residual, weights: dict, state_in, state_out, conv_state, ssm_state,
+               core_out=None, residual_out=None, stream=None, weights_struct=None):
+        """A verify step: state_in [S] int32, state_out [S, T] int32 (one slot
+        per token), x [S*T, H] (sequence-major). Returns (core_out, residual_out)."""
+        import torch
+        S, T = state_out.shape
+        rows = x.shape[0]
+        if rows != S * T or state_in.shape[0] != S:
+            raise ValueError("x must have S*T rows and state_in S entries")
+        if core_out is None:
+            core_out = torch.empty(rows, self.shape.num_v_heads * self.shape.head_v_dim,
+                                   dtype=torch.bfloat16, device=x.device)
+        if residual_out is None:
+            residual_out = torch.empty_like(x)
+        for t in (x, residual, state_in, state_out, conv_state, ssm_state, core_out, residual_out):
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("tensors must be contiguous CUDA tensors")
+        ws = weights_struct if weights_struct is not None else self.weights_struct(weights)
+        st = _native.lib().gdn_decode_verify(
+            self._h, S, T, _ptr(x), _ptr(residual), ctypes.byref(ws), _ptr(state_in), _ptr(state_out),
+            _ptr(conv_state), _ptr(ssm_state), _ptr(core_out), _ptr(residual_out), _stream_ptr(stream))
+        if st != GDN_OK:
+            raise GdnError("gdn_decode_verify", st)
+        return core_out, residual_out
+
     def timeline(self, stream=None):
         """Phase stamps of the last step (handle made with GDN_DEBUG_TIMELINE):
         per-CTA [G][48] nanosecond stamps as nested lists."""

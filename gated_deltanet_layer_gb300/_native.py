@@ -25,7 +25,7 @@ GDN_LAUNCH_NO_EARLY_WEIGHTS = 0x2
 EXPORTS = (
     "gdn_decode_workspace_bytes", "gdn_decode_create", "gdn_decode_step", "gdn_decode_check",
     "gdn_decode_reset", "gdn_decode_destroy", "gdn_status_string", "gdn_decode_launch_info",
-    "gdn_decode_plan", "gdn_decode_debug_timeline", "gdn_decode_step_static",
+    "gdn_decode_plan", "gdn_decode_debug_timeline", "gdn_decode_step_static", "gdn_decode_verify",
 )
 
 # Size of the library's fixed device scratch (gdn_decode_step_static).
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
     L.gdn_decode_create.restype = ctypes.c_int
     L.gdn_decode_step.argtypes = [vp, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp]
     L.gdn_decode_step.restype = ctypes.c_int
+    L.gdn_decode_verify.argtypes = [vp, i32, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp, vp]
+    L.gdn_decode_verify.restype = ctypes.c_int
     L.gdn_decode_check.argtypes = [vp, vp, u32p]
     L.gdn_decode_check.restype = ctypes.c_int
     L.gdn_decode_reset.argtypes = [vp, vp]

@@ -255,10 +255,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res) {
+// The step kernel of a config: the engine's, for a decode step or (multi) a
+// verify step (tensor-core engine with bf16 weights only); nullptr if none.
+const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res, bool multi = false) {
   const bool b16 = c.ssm_dtype == GDN_STATE_BF16;
-  return engine == GDN_ENGINE_TCGEN05 ? tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format)
-                                      : cuda_core_kernel(has_res, b16, c.head_k_dim);
+  if (engine == GDN_ENGINE_TCGEN05) return tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format, multi);
+  return multi ? nullptr : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
 size_t kernel_smem(const Plan& pl) { return pl.smem; }
@@ -358,7 +360,9 @@ bool encode_maps(const gdn_decode_config& c, const gdn_decode_weights* w, CUtens
 }
 
 
-// The tensors of one step call.
+// The tensors of one step call. A verify step has `tokens` rows per
+// sequence, idx holds one slot per sequence and idx_out one per row; a
+// decode step has tokens = 1 and no idx_out.
 struct StepArgs {
   int32_t rows;
   const void* x;
@@ -369,6 +373,8 @@ struct StepArgs {
   void* ssm_state;
   void* core_out;
   void* residual_out;
+  int32_t tokens = 1;
+  const int32_t* idx_out = nullptr;
 };
 
 // Host-side checks of a step's arguments (before any launch): rows in range,
@@ -388,6 +394,7 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
   for (const void* q : a16)
     if (q && !aligned(q, 16)) return GDN_ERR_ARG;
   if (!aligned(a.idx, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
+  if (a.tokens > 1 && (!a.idx_out || !aligned(a.idx_out, 4))) return GDN_ERR_ARG;
   const size_t H = (size_t)c.hidden;
   const size_t xb = (size_t)a.rows * H * 2;
   const size_t coreb = (size_t)a.rows * c.num_v_heads * c.head_v_dim * 2;
@@ -395,7 +402,8 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
   const size_t ssmb = (size_t)c.num_slots * c.num_v_heads * c.head_v_dim * c.head_k_dim * sdt;
   const size_t convb = (size_t)c.num_slots * n_conv(c) * (c.conv_kernel - 1) * 2;
   struct Rg { const void* p; size_t n; };
-  const Rg ins[] = {{a.x, xb}, {a.residual, a.residual ? xb : 0}, {a.idx, (size_t)a.rows * 4},
+  const Rg ins[] = {{a.x, xb}, {a.residual, a.residual ? xb : 0}, {a.idx, (size_t)(a.rows / a.tokens) * 4},
+                    {a.idx_out, a.idx_out ? (size_t)a.rows * 4 : 0},
                     {a.conv_state, convb}, {a.ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
                     {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
                     {w->qkvz_scales, c.qkvz_format != GDN_W_BF16 ? (size_t)n_qkvz(c) * H / 32 : 0},
@@ -417,6 +425,8 @@ void fill_params(const gdn_decode_config& c, const Plan& pl, const Layout& lay, 
   p->H = c.hidden; p->Hk = c.num_k_heads; p->Hv = c.num_v_heads;
   p->dk = c.head_k_dim; p->dv = c.head_v_dim; p->C = n_conv(c);
   p->Nqkvz = n_qkvz(c); p->Nba = n_ba(c); p->num_slots = c.num_slots; p->rows = a.rows;
+  p->tokens = a.tokens;
+  p->idx_out = a.idx_out;
   p->group = c.num_v_heads / c.num_k_heads;
   set_plan_params(pl, p);
   p->norm_eps = c.norm_eps; p->gnorm_eps = c.gated_norm_eps; p->l2_eps = c.l2_eps; p->q_scale = c.q_scale;
@@ -470,7 +480,8 @@ bool weight_maps(const gdn_decode_config& c, const gdn_decode_weights* w, MapCac
 // serialisation, *pdl is cleared and the launch goes without it.
 gdn_status launch_step(const gdn_decode_config& c, const Plan& pl, bool* pdl, const StepParams& p, bool has_res,
                        cudaStream_t s) {
-  const void* kern = pick_kernel(c, pl.engine, has_res);
+  const void* kern = pick_kernel(c, pl.engine, has_res, p.tokens > 1 || p.idx_out != nullptr);
+  if (!kern) return GDN_ERR_UNSUPPORTED;
   cudaLaunchConfig_t lc;
   memset(&lc, 0, sizeof(lc));
   lc.gridDim = dim3(pl.G);
@@ -502,17 +513,20 @@ gdn_status launch_step(const gdn_decode_config& c, const Plan& pl, bool* pdl, co
 
 // The launches of one step: rows in tiles of at most kMaxRows, one launch
 // per tile in row order, each a whole step over its rows (rows are
-// independent: distinct state slots). A step of up to kMaxRows rows is one
-// launch; wider steps stream the weights once per tile.
+// independent: distinct state slots; a verify step's tiles hold whole
+// sequences). A step of up to kMaxRows rows is one launch; wider steps
+// stream the weights once per tile.
 gdn_status launch_row_tiles(const gdn_decode_config& c, const Plan& pl, const Layout& lay, char* base,
                             const StepArgs& a, MapCache* maps, bool* pdl, cudaStream_t s) {
   const size_t xrow = (size_t)c.hidden * 2, crow = (size_t)c.num_v_heads * c.head_v_dim * 2;
-  for (int r0 = 0; r0 < a.rows; r0 += kMaxRows) {
+  const int tile_rows = kMaxRows / a.tokens * a.tokens;
+  for (int r0 = 0; r0 < a.rows; r0 += tile_rows) {
     StepArgs t = a;
-    t.rows = std::min(kMaxRows, a.rows - r0);
+    t.rows = std::min(tile_rows, a.rows - r0);
     t.x = (const char*)a.x + r0 * xrow;
     t.residual = a.residual ? (const char*)a.residual + r0 * xrow : nullptr;
-    t.idx = a.idx + r0;
+    t.idx = a.idx + r0 / a.tokens;
+    t.idx_out = a.idx_out ? a.idx_out + r0 : nullptr;
     t.core_out = (char*)a.core_out + r0 * crow;
     t.residual_out = (char*)a.residual_out + r0 * xrow;
     StepParams p;  // on the stack: the step allocates nothing
@@ -584,8 +598,9 @@ gdn_status gdn_decode_create(const gdn_decode_config* cfg, void* workspace, size
   }
   // Every CTA of the persistent grid must be co-resident.
   const size_t smem = kernel_smem(h->plan);
-  for (int r = 0; r < 2; ++r) {
-    const void* k = pick_kernel(h->cfg, h->plan.engine, r == 1);
+  for (int r = 0; r < 4; ++r) {
+    const void* k = pick_kernel(h->cfg, h->plan.engine, r & 1, r >= 2);
+    if (!k && r >= 2) continue;  // no verify kernel for this config
     int per_sm = 0;
     if (!k || (smem && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                            cudaSuccess) ||
@@ -629,6 +644,22 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   const StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
   gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
   if (st != GDN_OK) return st;
+  return launch_row_tiles(h->cfg, h->plan, h->lay, (char*)h->ws, a, &h->maps, &h->pdl, (cudaStream_t)stream);
+}
+
+gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, const void* x, const void* residual,
+                             const gdn_decode_weights* w, const int32_t* state_in, const int32_t* state_out,
+                             void* conv_state, void* ssm_state, void* core_out, void* residual_out,
+                             void* stream) {
+  if (!h) return GDN_ERR_ARG;
+  if (seqs < 1 || tokens < 1 || tokens > kMaxRows || (long long)seqs * tokens > h->cfg.max_rows) return GDN_ERR_ARG;
+  StepArgs a{seqs * tokens, x, residual, w, state_in, conv_state, ssm_state, core_out, residual_out};
+  a.tokens = tokens;
+  a.idx_out = state_out;
+  if (!state_out) return GDN_ERR_ARG;
+  gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
+  if (st != GDN_OK) return st;
+  if (!pick_kernel(h->cfg, h->plan.engine, residual != nullptr, true)) return GDN_ERR_UNSUPPORTED;
   return launch_row_tiles(h->cfg, h->plan, h->lay, (char*)h->ws, a, &h->maps, &h->pdl, (cudaStream_t)stream);
 }
 

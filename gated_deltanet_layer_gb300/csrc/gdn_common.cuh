@@ -64,6 +64,7 @@ enum TlPoint { TL_START = 0, TL_NORM_OUT, TL_NORM_IN, TL_XN_OUT, TL_PROJ_START, 
 struct StepParams {
   // shapes
   int H, Hk, Hv, dk, dv, C, Nqkvz, Nba, num_slots, rows;
+  int tokens;          // tokens per sequence (rows = sequences x tokens); 1 for a decode step
   int group;           // Hv / Hk
   int tiles_qkvz;      // Nqkvz / kTileM
   int num_tiles;       // tiles_qkvz + ceil(Nba / kTileM)
@@ -86,7 +87,8 @@ struct StepParams {
   const __nv_bfloat16* res;   // nullptr: first layer
   __nv_bfloat16* res_out;
   __nv_bfloat16* core_out;
-  const int* idx;
+  const int* idx;             // [rows / tokens] state slot each sequence starts from (and, decoding, updates)
+  const int* idx_out;         // verify: [rows] slot of each token's state; nullptr when decoding
   __nv_bfloat16* conv_state;
   void* ssm_state;
   // weights

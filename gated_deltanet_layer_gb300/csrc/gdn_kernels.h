@@ -11,12 +11,13 @@ namespace gdn {
 const void* cuda_core_kernel(bool has_res, bool state_bf16, int dk);
 size_t cuda_core_smem_bytes();
 
-// The same for the tensor-core (tcgen05) projection engine. Its dynamic
+// The same for the tensor-core (tcgen05) projection engine, for a decode step
+// or (multi) a verify step. Its dynamic
 // shared memory depends on the weight ring's depth (stages), the code
 // ring's (rstages; MXFP4 or MXFP6), the normed input window (xslots k-steps,
 // doubled for MXFP4 weights); the pad past the window; the static shared memory of the
 // kernel; the deepest ring it supports.
-const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt);
+const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt, bool multi);
 size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, int fmt);
 uint32_t tensor_core_xpad(int xslots);
 size_t tensor_core_static_smem();

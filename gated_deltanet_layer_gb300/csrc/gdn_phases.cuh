@@ -200,10 +200,11 @@ struct StateRegs {
   float4 f[NR][CH];  // f32 state
 };
 
-// The CTA's recurrence tasks: (row w, value head h) = task / Hv, task % Hv
-// for task in [t0, t1).
+// The CTA's recurrence tasks: (sequence, value head h) = task / Hv, task % Hv
+// for task in [t0, t1); a sequence is one row when decoding, `tokens` rows
+// in a verify step.
 __device__ __forceinline__ void task_range(const StepParams& p, int& t0, int& t1) {
-  const int T = p.rows * p.Hv;
+  const int T = p.rows / p.tokens * p.Hv;
   t0 = (int)(((long long)blockIdx.x * T) / p.num_ctas);
   t1 = (int)(((long long)(blockIdx.x + 1) * T) / p.num_ctas);
 }
@@ -214,8 +215,8 @@ template <int DK, bool STATE_BF16>
 __device__ __forceinline__ void load_state(const StepParams& p, int task, StateRegs<DK>& r) {
   constexpr int NR = StateRegs<DK>::NR, CH = StateRegs<DK>::CH, LPR = StateRegs<DK>::LPR;
   constexpr int RPW = StateRegs<DK>::RPW;
-  const int w = task / p.Hv, h = task - w * p.Hv;
-  const int slot = p.idx[w];
+  const int sq = task / p.Hv, h = task - sq * p.Hv;  // sequence, value head
+  const int slot = p.idx[sq];
   if (!row_is_live(p, slot)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t sbase = ((size_t)slot * p.Hv + h) * (size_t)DK * DK;
@@ -237,7 +238,14 @@ __device__ __forceinline__ void load_state(const StepParams& p, int task, StateR
 // that its latency hides under the projection); later tasks load into it.
 // sm.flag is 1 on entry (every earlier phase of the launch succeeded); a
 // thread whose wait runs out clears it.
-template <int DK, bool STATE_BF16>
+// MULTI (verify steps): a task is (sequence, value head) and runs the
+// sequence's tokens in order; token t starts from the state (and conv taps)
+// token t - 1 stored, and its state goes to its own slot idx_out[row]. The
+// conv taps of a channel stay in its thread's registers from token to token;
+// the state between tokens is the stored one (rounded to bf16 for a bf16
+// state), held in `raw`. The q/k taps of a key-head group are written by its
+// first value head's task (no counter: the input slot is never written).
+template <int DK, bool STATE_BF16, bool MULTI = false>
 __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, SmemTask& st, int L,
                                                  StateRegs<DK>& raw, bool have_first) {
   constexpr int LPR = StateRegs<DK>::LPR;
@@ -250,20 +258,35 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
   const int sub = lane % LPR, rw = lane / LPR;
   int t0, t1;
   task_range(p, t0, t1);
+  const int TK = MULTI ? p.tokens : 1;
   for (int task = t0; task < t1; ++task) {
-    const int w = task / p.Hv, h = task - w * p.Hv;
-    const int slot = p.idx[w];
-    __nv_bfloat16* core = p.core_out + (size_t)w * p.Hv * DK + (size_t)h * DK;
-    if (!row_is_live(p, slot)) {
-      if (slot >= p.num_slots && h == 0 && tid == 0) record_error(p.ctr, kStatusIndex, 0, w);
-      for (int i = tid; i < DK; i += kThreads) core[i] = __float2bfloat16_rn(0.f);
+    const int sq = task / p.Hv, h = task - sq * p.Hv;  // sequence (one row when decoding), value head
+    const int slot = p.idx[sq];
+    bool live = row_is_live(p, slot);
+    bool bad = slot >= p.num_slots;
+    if (MULTI && live)
+      for (int t = 0; t < TK; ++t) {
+        const int o = p.idx_out[sq * TK + t];
+        if (!(o > 0 && o < p.num_slots)) live = false, bad = true;
+      }
+    if (!live) {
+      if (bad && h == 0 && tid == 0) record_error(p.ctr, kStatusIndex, 0, sq * TK);
+      for (int i = tid; i < DK * TK; i += kThreads)
+        p.core_out[(size_t)(sq * TK + i / DK) * p.Hv * DK + (size_t)h * DK + i % DK] = __float2bfloat16_rn(0.f);
       continue;
     }
     const int kh = h / p.group;
     // The state rows go into registers first, so their latency overlaps the
     // wait for the projections (the first task's were loaded earlier still).
-    const size_t sbase = ((size_t)slot * p.Hv + h) * (size_t)DK * DK;
     if (!(have_first && task == t0)) load_state<DK, STATE_BF16>(p, task, raw);
+    // the conv taps of this thread's channel, carried from token to token (MULTI)
+    float tap0 = 0.f, tap1 = 0.f, tap2 = 0.f;
+#pragma unroll 1
+    for (int tk = 0; tk < TK; ++tk) {
+    const int w = sq * TK + tk;  // the row of this token
+    const int oslot = MULTI ? p.idx_out[w] : slot;  // where its state goes
+    __nv_bfloat16* core = p.core_out + (size_t)w * p.Hv * DK + (size_t)h * DK;
+    const size_t sbase = ((size_t)oslot * p.Hv + h) * (size_t)DK * DK;
     // Per-head constants, also loaded now.
     const float A_log_h = p.A_log[h];
     const float dt_bias_h = bf16_to_f(p.dt_bias[h]);
@@ -303,11 +326,12 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       const int n = proj_row(i);
       int nc;
       const unsigned long long* src = part_src(n, nc);
-      __nv_bfloat16 cb0, cb1, cb2;
       uint2 cwv;
       if (i < 3 * DK) {  // old taps and weights of channel n
-        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
-        cb0 = cs[0]; cb1 = cs[1]; cb2 = cs[2];
+        if (tk == 0) {
+          const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+          tap0 = bf16_to_f(cs[0]); tap1 = bf16_to_f(cs[1]); tap2 = bf16_to_f(cs[2]);
+        }
         cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)n * 4);
       }
       unsigned long long pw[kMaxSlots];
@@ -322,7 +346,8 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
         if (jj < nc) acc += tagged_value(pw[jj]);
       const float pv = round_bf16(acc);
       if (i < 3 * DK) {
-        const float c0 = bf16_to_f(cb0), c1 = bf16_to_f(cb1), c2 = bf16_to_f(cb2);
+        const float c0 = tap0, c1 = tap1, c2 = tap2;
+        tap0 = c1; tap1 = c2; tap2 = pv;  // the taps after this token
         float y = bf16_lo(cwv.x) * c0;
         y = fmaf(bf16_hi(cwv.x), c1, y);
         y = fmaf(bf16_lo(cwv.y), c2, y);
@@ -334,15 +359,24 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
           st.k[i - DK] = y;
         } else {
           st.v[i - 2 * DK] = y;
-          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;  // this head's own channel
+          __nv_bfloat16* cs = p.conv_state + ((size_t)oslot * p.C + n) * 3;  // this head's own channel
           cs[0] = __float2bfloat16_rn(c1);
           cs[1] = __float2bfloat16_rn(c2);
           cs[2] = __float2bfloat16_rn(pv);
         }
         if (i < 2 * DK) {
-          st.cnew[i][0] = c1;
-          st.cnew[i][1] = c2;
-          st.cnew[i][2] = pv;
+          if (MULTI) {
+            if (h % p.group == 0) {  // the group's first value head writes its q/k taps
+              __nv_bfloat16* cs = p.conv_state + ((size_t)oslot * p.C + n) * 3;
+              cs[0] = __float2bfloat16_rn(c1);
+              cs[1] = __float2bfloat16_rn(c2);
+              cs[2] = __float2bfloat16_rn(pv);
+            }
+          } else {
+            st.cnew[i][0] = c1;
+            st.cnew[i][1] = c2;
+            st.cnew[i][2] = pv;
+          }
         }
       } else {
         st.z[i - 3 * DK] = pv;
@@ -362,7 +396,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     __syncthreads();
     if (!sm.flag) return false;
     unsigned int group_old = 0;
-    if (tid == 0) {
+    if (!MULTI && tid == 0) {
       // Every thread's reads of the old q/k taps are done: their values were
       // used before the barrier above, so no later store can reach them. The
       // count needs no release (a release here waits for every store the CTA
@@ -442,10 +476,12 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
         ov[j] = fmaf(s[j][c].w, q4[c].w, ov[j]);
         const size_t off = sbase + (size_t)v * DK + (sub + LPR * c) * 4;
         if (STATE_BF16) {
-          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ssm_state) + off) =
-              make_uint2(pack_bf16x2(s[j][c].x, s[j][c].y), pack_bf16x2(s[j][c].z, s[j][c].w));
+          const uint2 sb = make_uint2(pack_bf16x2(s[j][c].x, s[j][c].y), pack_bf16x2(s[j][c].z, s[j][c].w));
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ssm_state) + off) = sb;
+          if (MULTI) raw.b[j][c] = sb;  // the next token starts from the stored state
         } else {
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.ssm_state) + off) = s[j][c];
+          if (MULTI) raw.f[j][c] = s[j][c];
         }
       }
     }
@@ -456,7 +492,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
 #pragma unroll
     for (int j = 0; j < NR; ++j)
       if (sub == 0) st.o[(j * kWarps + warp) * RPW + rw] = ov[j];
-    if (tid == 0) st.last = ((group_old + 1) % (unsigned)p.group) == 0;
+    if (tid == 0) st.last = !MULTI && ((group_old + 1) % (unsigned)p.group) == 0;
     __syncthreads();
     float rn = 0.f;
     if (warp < DK / 32) {  // the warps that write core: each sums o^2 itself (same order)
@@ -469,7 +505,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     if (st.last) {  // the last reader of the group writes the new q/k taps
       for (int i = tid; i < 2 * DK; i += kThreads) {
         const int n = proj_row(i);
-        __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + n) * 3;
+        __nv_bfloat16* cs = p.conv_state + ((size_t)oslot * p.C + n) * 3;
         cs[0] = __float2bfloat16_rn(st.cnew[i][0]);
         cs[1] = __float2bfloat16_rn(st.cnew[i][1]);
         cs[2] = __float2bfloat16_rn(st.cnew[i][2]);
@@ -479,6 +515,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     if ((p.debug_flags & kDebugTimeline) && task == t0 && tid == 0)
       p.ctr->tl_cta[cta][TL_REC_STATE] = globaltimer_ns();
     __syncthreads();
+    }  // tokens
   }
   return true;
 }

@@ -764,7 +764,8 @@ static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, in
 
 // FMT: the in_proj_qkvz weight format (kFmtBf16, kFmtMxfp4, kFmtMxfp6; the
 // coded formats alone carry the decoding warps' code; p.fmt equals FMT).
-template <bool HAS_RES, bool STATE_BF16, int DK, int FMT>
+// MULTI: a verify step (sequences of p.tokens rows, a state slot per token).
+template <bool HAS_RES, bool STATE_BF16, int DK, int FMT, bool MULTI>
 __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_constant__ StepParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SmemPhases sm;
@@ -883,22 +884,29 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   }
   tl_stamp(p, TL_PROJ_END);
   if (!aborted) {
-    phase_recurrence<DK, STATE_BF16>(p, sm, st, L, first_state, rt0 < rt1);
+    phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
     tl_stamp(p, TL_END);
   }
 }
 
-const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt) {
-#define GDN_PICK(R, B, D, F) \
-  if (has_res == R && state_bf16 == B && dk == D && fmt == F) return (const void*)&gdn_step_tc_kernel<R, B, D, F>;
-  GDN_PICK(true, false, 128, kFmtBf16) GDN_PICK(true, true, 128, kFmtBf16) GDN_PICK(false, false, 128, kFmtBf16)
-  GDN_PICK(false, true, 128, kFmtBf16) GDN_PICK(true, false, 64, kFmtBf16) GDN_PICK(true, true, 64, kFmtBf16)
-  GDN_PICK(false, false, 64, kFmtBf16) GDN_PICK(false, true, 64, kFmtBf16)
-  // MXFP4 and MXFP6 in_proj_qkvz: head dim 128
-  GDN_PICK(true, false, 128, kFmtMxfp4) GDN_PICK(true, true, 128, kFmtMxfp4) GDN_PICK(false, false, 128, kFmtMxfp4)
-  GDN_PICK(false, true, 128, kFmtMxfp4)
-  GDN_PICK(true, false, 128, kFmtMxfp6) GDN_PICK(true, true, 128, kFmtMxfp6) GDN_PICK(false, false, 128, kFmtMxfp6)
-  GDN_PICK(false, true, 128, kFmtMxfp6)
+const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt, bool multi) {
+#define GDN_PICK(R, B, D, F, M)                                                         \
+  if (has_res == R && state_bf16 == B && dk == D && fmt == F && multi == M)             \
+    return (const void*)&gdn_step_tc_kernel<R, B, D, F, M>;
+  // decode steps: bf16 weights (head dim 64 or 128), MXFP4 and MXFP6 (head dim 128)
+  GDN_PICK(true, false, 128, kFmtBf16, false) GDN_PICK(true, true, 128, kFmtBf16, false)
+  GDN_PICK(false, false, 128, kFmtBf16, false) GDN_PICK(false, true, 128, kFmtBf16, false)
+  GDN_PICK(true, false, 64, kFmtBf16, false) GDN_PICK(true, true, 64, kFmtBf16, false)
+  GDN_PICK(false, false, 64, kFmtBf16, false) GDN_PICK(false, true, 64, kFmtBf16, false)
+  GDN_PICK(true, false, 128, kFmtMxfp4, false) GDN_PICK(true, true, 128, kFmtMxfp4, false)
+  GDN_PICK(false, false, 128, kFmtMxfp4, false) GDN_PICK(false, true, 128, kFmtMxfp4, false)
+  GDN_PICK(true, false, 128, kFmtMxfp6, false) GDN_PICK(true, true, 128, kFmtMxfp6, false)
+  GDN_PICK(false, false, 128, kFmtMxfp6, false) GDN_PICK(false, true, 128, kFmtMxfp6, false)
+  // verify steps: bf16 weights
+  GDN_PICK(true, false, 128, kFmtBf16, true) GDN_PICK(true, true, 128, kFmtBf16, true)
+  GDN_PICK(false, false, 128, kFmtBf16, true) GDN_PICK(false, true, 128, kFmtBf16, true)
+  GDN_PICK(true, false, 64, kFmtBf16, true) GDN_PICK(true, true, 64, kFmtBf16, true)
+  GDN_PICK(false, false, 64, kFmtBf16, true) GDN_PICK(false, true, 64, kFmtBf16, true)
 #undef GDN_PICK
   return nullptr;
 }

@@ -100,6 +100,12 @@ class LayerShape:
         H = self.hidden
         return H * 2 * (1 if first_layer else 2) + H * 2 + self.num_v_heads * self.head_v_dim * 2 + 4
 
+    def verify_bytes(self, seqs: int, tokens: int) -> int:
+        """A verify step: the weights, each sequence's input state read once,
+        one conv + SSM state written per token, and the rows' activations."""
+        return (self.weight_bytes() + seqs * self.state_bytes_per_row() // 2
+                + seqs * tokens * (self.state_bytes_per_row() // 2 + self.activation_bytes_per_row()))
+
     def launch_bytes(self, rows: int, live_rows: int | None = None, first_layer: bool = False) -> int:
         live = rows if live_rows is None else live_rows
         return (self.weight_bytes() + live * self.state_bytes_per_row()

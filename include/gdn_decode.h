@@ -204,6 +204,31 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
                            void* ssm_state, void* core_out, void* residual_out,
                            void* stream);
 
+/* A verify step (multi-token, a state per token): `seqs` sequences of
+ * `tokens` tokens each (rows s*tokens + t of x, residual, core_out and
+ * residual_out; seqs * tokens <= max_rows, tokens <= GDN_ROWS_PER_LAUNCH).
+ * Sequence s starts from the conv and SSM state in slot state_in[s]; after
+ * token t, its conv and SSM state are written to slot state_out[s*tokens + t],
+ * and token t + 1 continues from that stored state. So the tokens give what
+ * as many decode steps would, and accepting a sequence's first a tokens is
+ * taking slot state_out[s*tokens + a - 1]: a rejected draft token rolls back
+ * by choosing a slot. The pages leave this as a follow-up (sgl-amd-mono #89,
+ * Motivation: the launch keeps no state for each draft token, so a rejected
+ * draft cannot roll back; vLLM #60833, Details, "Limitations / follow-ups":
+ * MTP verify steps).
+ * state_in [seqs] and state_out [seqs*tokens] are int32 device arrays; a
+ * sequence with state_in <= 0 is padding (zero core rows, no state read or
+ * written). Live sequences need distinct state_in slots, and all their
+ * state_out slots distinct and apart from every state_in slot; the input
+ * slots are only read. A slot >= num_slots (in or out) records GDN_ERR_INDEX
+ * and makes the sequence padding. Each launch takes whole sequences
+ * (floor(16 / tokens) of them). Tensor-core engine with bf16 in_proj_qkvz
+ * only (else GDN_ERR_UNSUPPORTED). Other behaviour as gdn_decode_step. */
+gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, const void* x,
+                             const void* residual, const gdn_decode_weights* w,
+                             const int32_t* state_in, const int32_t* state_out, void* conv_state,
+                             void* ssm_state, void* core_out, void* residual_out, void* stream);
+
 /* Synchronise `stream` and read the sticky error word. Returns GDN_OK, or the
  * recorded device status; *detail (optional) receives the raw word:
  * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
