@@ -23,6 +23,7 @@ Launches; SGLang #43558 "Qwen3.8-27B dense mono decode", Modifications, K1):
   8. gated delta rule on the slot state S <- e^g S;  S += k (x) beta (v - S^T k);
                                         o = S^T q
   9. gated RMSNorm over the head        core = rmsnorm(o) * w_g * silu(z)
+  10. (with out_proj weights) out_proj   out = W_o core   over the Hv*dv core columns
   Pad rows (state index <= 0) write a zero core row and no state.
 
 Arithmetic: float64 throughout. Values are rounded to their storage type
@@ -58,7 +59,7 @@ __all__ = [
     "mxfp4_unpack_codes", "mxfp4_quantize_block", "mxfp4_quantize_row",
     "project_mxfp4", "e2m3_value", "mxfp6_quantize_block", "mxfp6_quantize_matrix",
     "mxfp6_pack", "mxfp6_unpack", "project_mxfp6", "split_projection", "conv_update", "l2norm",
-    "gates", "delta_rule", "gated_rmsnorm", "gdn_step", "gdn_verify",
+    "gates", "delta_rule", "gated_rmsnorm", "out_proj", "gdn_step", "gdn_verify",
 ]
 
 # --------------------------------------------------------------------------
@@ -465,6 +466,19 @@ def gated_rmsnorm(o, z, w_g, eps: float):
 
 
 # --------------------------------------------------------------------------
+# out_proj folded into the launch (SGLang #43558, commit text of the
+# SGLANG_QWEN3_8_DENSE_MONO_OPROJ fold, "dense_gdn (K1Build.oproj)": every
+# CTA publishes its core rows, then each runs its hidden columns of
+# out_proj over the K share and the launch writes the out_proj result)
+# --------------------------------------------------------------------------
+
+def out_proj(core, W_o):
+    """out[w, n] = bf16(sum_j W_o[n, j] core[w, j]) over the Hv*dv core
+    columns of the bf16 core rows; the float64 sum is rounded once."""
+    return bf16_round(np.asarray(core, dtype=np.float64) @ np.asarray(W_o, dtype=np.float64).T)
+
+
+# --------------------------------------------------------------------------
 # The whole step
 # --------------------------------------------------------------------------
 
@@ -524,10 +538,13 @@ def gdn_step(shape, x, residual, weights, state_indices, conv_state, ssm_state):
             ssm_new[slot, h] = bf16_round(S) if shape.ssm_dtype == "bf16" else f32_round(S)
             core[w, h * dv:(h + 1) * dv] = gated_rmsnorm(o, z[w, h], weights["gated_norm_w"],
                                                          shape.gated_norm_eps)
-    return {
+    out = {
         "residual_out": r, "core": core, "conv_state": conv_new, "ssm_state": ssm_new,
         "index_error": index_error, "xn": xn, "p_qkvz": p_qkvz, "p_ba": p_ba,
     }
+    if weights.get("out_proj") is not None:
+        out["out"] = out_proj(core, weights["out_proj"])
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -599,5 +616,8 @@ def gdn_verify(shape, x, residual, weights, state_in, state_out, conv_state, ssm
             conv_new[outs[t]] = conv_t
             ssm_new[outs[t]] = ssm_t
             conv_prev, ssm_prev = conv_t, ssm_t
-    return {"residual_out": r, "core": core, "conv_state": conv_new, "ssm_state": ssm_new,
-            "index_error": index_error, "xn": xn, "p_qkvz": p_qkvz, "p_ba": p_ba}
+    out = {"residual_out": r, "core": core, "conv_state": conv_new, "ssm_state": ssm_new,
+           "index_error": index_error, "xn": xn, "p_qkvz": p_qkvz, "p_ba": p_ba}
+    if weights.get("out_proj") is not None:
+        out["out"] = out_proj(core, weights["out_proj"])
+    return out

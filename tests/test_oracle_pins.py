@@ -667,3 +667,34 @@ def test_verify_padding_sequence_and_untouched_slots():
     np.testing.assert_array_equal(out["conv_state"][others], conv[others])
     bad = sout.copy(); bad[0, 1] = shape.num_slots
     assert O.gdn_verify(shape, x, res, w, sin, bad, conv, ssm)["index_error"]
+
+
+
+# ---------------------------------------------------------------- out_proj
+
+def test_out_proj_one_hot_and_brute_force():
+    """A one-hot core row returns the weight column; a tiny case against a
+    brute-force double loop with an exact rational sum rounded once."""
+    rng = np.random.default_rng(200)
+    N, K = 5, 12
+    Wo = _torch_bf16(rng.standard_normal((N, K)) * 0.5)
+    onehot = np.zeros((1, K)); onehot[0, 7] = 1.0
+    np.testing.assert_array_equal(O.out_proj(onehot, Wo)[0], Wo[:, 7])
+    core = _torch_bf16(rng.standard_normal((3, K)))
+    got = O.out_proj(core, Wo)
+    for w in range(3):
+        for n in range(N):
+            total = sum(Fraction(float(Wo[n, j])) * Fraction(float(core[w, j])) for j in range(K))
+            assert got[w, n] == O.bf16_round(float(total))
+
+
+def test_step_out_proj_of_a_padding_row_is_zero():
+    shape = WL.TINY
+    x, res, w, idx, conv, ssm = _np_inputs(shape, 4, 210, pad_rows=2)
+    rng = np.random.default_rng(211)
+    w["out_proj"] = _torch_bf16(rng.standard_normal((shape.hidden, shape.num_v_heads * shape.head_v_dim)) * 0.02)
+    out = O.gdn_step(shape, x, res, w, idx, conv, ssm)
+    for r, i in enumerate(idx):
+        if i <= 0:
+            assert np.all(out["out"][r] == 0.0)
+    np.testing.assert_array_equal(out["out"], O.out_proj(out["core"], w["out_proj"]))
