@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--workload", default="full")
     ap.add_argument("--rows", type=int, default=16, help="rows of the headline step")
     ap.add_argument("--widths", default="1,2,4,8,16", help="widths of the per-width tables")
-    ap.add_argument("--tables", default="shard,full,shard_bf16,dense_mxfp4,dense_mxfp6,shard_wide,shard_verify",
+    ap.add_argument("--tables",
+                    default="shard,full,shard_bf16,dense_mxfp4,dense_mxfp6,shard_wide,shard_verify,shard_out,full_out",
                     help="workloads of the per-width tables ('' for none)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--engine", default="auto")
@@ -79,6 +80,9 @@ TABLES = {
     "dense_mxfp6": {"widths": [1, 2, 4, 8, 16], "min_copies": 48},
     # steps wider than one launch (one launch per 16-row tile)
     "shard_wide": {"shape": "shard", "max_rows": 64, "widths": [16, 24, 32, 48, 64]},
+    # the step with out_proj folded in
+    "shard_out": {"shape": "shard", "widths": [1, 4, 8, 16], "out_proj": True},
+    "full_out": {"shape": "full", "widths": [1, 16], "out_proj": True},
     # verify steps: (sequences, tokens) with a state slot per token
     "shard_verify": {"shape": "shard", "verify": [(1, 2), (1, 4), (2, 4), (4, 4), (8, 2), (2, 8)]},
 }
@@ -227,11 +231,12 @@ class Rig:
     (together larger than 3x L2, and at least `min_copies`), the conv and SSM
     state of every slot, and a handle."""
 
-    def __init__(self, shape, g, l2, engine, min_copies=4):
+    def __init__(self, shape, g, l2, engine, min_copies=4, out_proj=False):
         import torch
         from gated_deltanet_layer_gb300 import GdnDecode
         self.shape, self.g = shape, g
-        wbytes = shape.weight_bytes()
+        self.out_proj = out_proj
+        wbytes = shape.weight_bytes() + (shape.out_proj_bytes(0) if out_proj else 0)
         self.ncopy = max(min_copies, int((3 * l2 + wbytes - 1) // wbytes) + 1)
         self.wbytes = wbytes
         H, Hv = shape.hidden, shape.num_v_heads
@@ -256,6 +261,7 @@ class Rig:
                 "A_log": -2.0 * torch.rand(Hv, generator=g, device="cuda"),
                 "dt_bias": self.bf16(Hv, std=0.5),
                 "gated_norm_w": self.bf16(shape.head_v_dim, std=0.1),
+                "out_proj": self.bf16(H, Hv * shape.head_v_dim, std=0.02) if out_proj else None,
             })
         sdt = torch.bfloat16 if shape.ssm_dtype == "bf16" else torch.float32
         self.conv = self.bf16(shape.num_slots, shape.conv_channels, shape.conv_kernel - 1, std=1.0)
@@ -282,7 +288,8 @@ class Rig:
             out.append((self.bf16(rows, sh.hidden, std=1.0), None if first_layer else self.bf16(rows, sh.hidden, std=1.0),
                         perm.to(torch.int32).contiguous(),
                         torch.empty(rows, sh.num_v_heads * sh.head_v_dim, dtype=torch.bfloat16, device="cuda"),
-                        torch.empty(rows, sh.hidden, dtype=torch.bfloat16, device="cuda")))
+                        torch.empty(rows, sh.hidden, dtype=torch.bfloat16, device="cuda"),
+                        torch.empty(rows, sh.hidden, dtype=torch.bfloat16, device="cuda") if self.out_proj else None))
         return out
 
     def capture(self, rows, n, pad=0.0, first_layer=False):
@@ -292,16 +299,21 @@ class Rig:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         graph = torch.cuda.CUDAGraph()
+        def one(k, b):
+            x, r, i, c, ro, o = b
+            if self.out_proj:
+                self.layer.step_out(x, r, self.copies[k % self.ncopy], i, self.conv, self.ssm, c, ro, o,
+                                    weights_struct=self.wstructs[k % self.ncopy])
+            else:
+                self.layer.step(x, r, self.copies[k % self.ncopy], i, self.conv, self.ssm, c, ro,
+                                weights_struct=self.wstructs[k % self.ncopy])
+
         with torch.cuda.stream(s):
-            # one eager launch first (lazy set-up outside the capture)
-            x, r, i, c, ro = batch[0]
-            self.layer.step(x, r, self.copies[0], i, self.conv, self.ssm, c, ro, weights_struct=self.wstructs[0])
+            one(0, batch[0])  # one eager launch first (lazy set-up outside the capture)
             torch.cuda.current_stream().synchronize()
             with torch.cuda.graph(graph, stream=s):
                 for k in range(n):
-                    x, r, i, c, ro = batch[k % len(batch)]
-                    self.layer.step(x, r, self.copies[k % self.ncopy], i, self.conv, self.ssm, c, ro,
-                                    weights_struct=self.wstructs[k % self.ncopy])
+                    one(k, batch[k % len(batch)])
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         return graph
@@ -376,14 +388,15 @@ def native(args):
             dist.barrier()
         return e0.elapsed_time(e1)  # ms
 
-    def row_of(sh, u, rows, live, first_layer):
-        b = sh.launch_bytes(rows, live, first_layer=first_layer)
+    def row_of(sh, u, rows, live, first_layer, extra=0):
+        b = sh.launch_bytes(rows, live, first_layer=first_layer) + extra
         gbs = b / u / 1e3
         return {"us": round(u, 3), "GBps": round(gbs, 1), "frac_of_" + peak_kind: round(gbs / peak, 4),
                 "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": b, "live_rows": live,
                 "launches": -(-rows // 16)}
 
     def width_table(rig, widths, pad=0.0, first_layer=False):
+        extra = (lambda r: rig.shape.out_proj_bytes(r)) if rig.out_proj else (lambda r: 0)
         """µs per launch of a graph of 100 launches, median of replays over
         ~0.3 s (so the clock sampler sees the GPU under load)."""
         out = {}
@@ -395,7 +408,7 @@ def native(args):
                 times.append(time_graph(gg) * 10.0)  # µs per launch
             times.sort()
             live = wdt - int(round(pad * wdt))
-            out[str(wdt)] = row_of(rig.shape, times[len(times) // 2], wdt, live, first_layer)
+            out[str(wdt)] = row_of(rig.shape, times[len(times) // 2], wdt, live, first_layer, extra(wdt))
             del gg
         rig.check()
         return out
@@ -468,7 +481,7 @@ def native(args):
             rig = None
             torch.cuda.empty_cache()
             tshape = WL.SHAPES[rec.get("shape", name)].with_(max_rows=rec.get("max_rows", 16))
-            rig = Rig(tshape, g, l2, args.engine, rec.get("min_copies", 4))
+            rig = Rig(tshape, g, l2, args.engine, rec.get("min_copies", 4), rec.get("out_proj", False))
         if "verify" in rec:
             vt = {}
             for S, T in rec["verify"]:

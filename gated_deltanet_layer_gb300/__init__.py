@@ -18,7 +18,8 @@ _FORMATS = {"bf16": GDN_W_BF16, "mxfp4": GDN_W_MXFP4, "mxfp6": GDN_W_MXFP6}
 __all__ = ["GdnDecode", "GdnError", "ENGINES", "step_static"]
 
 ENGINES = {"auto": GDN_ENGINE_AUTO, "cuda_core": GDN_ENGINE_CUDA_CORE, "tcgen05": GDN_ENGINE_TCGEN05}
-_WEIGHT_KEYS = ("input_norm_w", "qkvz", "qkvz_scales", "ba", "conv_w", "A_log", "dt_bias", "gated_norm_w")
+_WEIGHT_KEYS = ("input_norm_w", "qkvz", "qkvz_scales", "ba", "conv_w", "A_log", "dt_bias", "gated_norm_w",
+                "out_proj")
 
 
 def _stream_ptr(stream):
@@ -107,6 +108,30 @@ class GdnDecode:
         if st != GDN_OK:
             raise GdnError("gdn_decode_step", st)
         return core_out, residual_out
+
+    def step_out(self, x, residual, weights: dict, state_indices, conv_state, ssm_state,
+                 core_out=None, residual_out=None, out=None, stream=None, weights_struct=None):
+        """A decode step followed by out_proj in the same launch (weights must
+        hold "out_proj" [H, Hv*dv] bf16). Returns (core_out, residual_out, out)."""
+        import torch
+        rows = x.shape[0]
+        if core_out is None:
+            core_out = torch.empty(rows, self.shape.num_v_heads * self.shape.head_v_dim,
+                                   dtype=torch.bfloat16, device=x.device)
+        if residual_out is None:
+            residual_out = torch.empty_like(x)
+        if out is None:
+            out = torch.empty_like(x)
+        for t in (x, residual, state_indices, conv_state, ssm_state, core_out, residual_out, out):
+            if t is not None and (not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("tensors must be contiguous CUDA tensors")
+        ws = weights_struct if weights_struct is not None else self.weights_struct(weights)
+        st = _native.lib().gdn_decode_step_out(
+            self._h, rows, _ptr(x), _ptr(residual), ctypes.byref(ws), _ptr(state_indices),
+            _ptr(conv_state), _ptr(ssm_state), _ptr(core_out), _ptr(residual_out), _ptr(out), _stream_ptr(stream))
+        if st != GDN_OK:
+            raise GdnError("gdn_decode_step_out", st)
+        return core_out, residual_out, out
 
     def verify(self, x, residual, weights: dict, state_in, state_out, conv_state, ssm_state,
                core_out=None, residual_out=None, stream=None, weights_struct=None):

@@ -26,6 +26,7 @@ EXPORTS = (
     "gdn_decode_workspace_bytes", "gdn_decode_create", "gdn_decode_step", "gdn_decode_check",
     "gdn_decode_reset", "gdn_decode_destroy", "gdn_status_string", "gdn_decode_launch_info",
     "gdn_decode_plan", "gdn_decode_debug_timeline", "gdn_decode_step_static", "gdn_decode_verify",
+    "gdn_decode_step_out",
 )
 
 # Size of the library's fixed device scratch (gdn_decode_step_static).
@@ -48,7 +49,7 @@ class Weights(ctypes.Structure):
     _fields_ = [
         ("input_norm_w", ctypes.c_void_p), ("qkvz", ctypes.c_void_p), ("qkvz_scales", ctypes.c_void_p),
         ("ba", ctypes.c_void_p), ("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
-        ("dt_bias", ctypes.c_void_p), ("gated_norm_w", ctypes.c_void_p),
+        ("dt_bias", ctypes.c_void_p), ("gated_norm_w", ctypes.c_void_p), ("out_proj", ctypes.c_void_p),
     ]
 
 
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
     L.gdn_decode_create.restype = ctypes.c_int
     L.gdn_decode_step.argtypes = [vp, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp]
     L.gdn_decode_step.restype = ctypes.c_int
+    L.gdn_decode_step_out.argtypes = [vp, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp, vp]
+    L.gdn_decode_step_out.restype = ctypes.c_int
     L.gdn_decode_verify.argtypes = [vp, i32, i32, vp, vp, ctypes.POINTER(Weights), vp, vp, vp, vp, vp, vp, vp]
     L.gdn_decode_verify.restype = ctypes.c_int
     L.gdn_decode_check.argtypes = [vp, vp, u32p]

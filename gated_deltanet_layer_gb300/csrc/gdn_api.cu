@@ -19,7 +19,7 @@ namespace {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t ctr, plan, norm_part, xn, proj_part, total;
+  size_t ctr, plan, norm_part, core_flag, xn, proj_part, total;
 };
 
 struct Plan {
@@ -43,8 +43,10 @@ struct Plan {
 struct MapCache {
   const void* qkvz_ptr = nullptr;
   const void* ba_ptr = nullptr;
+  const void* out_ptr = nullptr;
   CUtensorMap qkvz;
   CUtensorMap ba;
+  CUtensorMap out;
 };
 
 // Shared memory a CTA may use on sm_100-class GPUs (opt-in limit per block).
@@ -230,6 +232,7 @@ Layout make_layout(const gdn_decode_config& c, const Plan& pl) {
   l.ctr = off;        off += align_up(sizeof(WsCounters), 256);
   l.plan = off;       off += align_up(sizeof(PlanDev), 256);
   l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(unsigned long long), 256);
+  l.core_flag = off;  off += align_up((size_t)pl.G * sizeof(unsigned long long), 256);
   l.xn = off;         off += align_up((size_t)kMaxRows * c.hidden * 2, 256);
   l.proj_part = off;
   off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(unsigned long long), 256);
@@ -329,6 +332,20 @@ bool encode_weight_map(CUtensorMap* m, const void* base, int rows, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile map of out_proj [H][K] bf16 (K = Hv*dv): box 64 columns x 64 rows,
+// 128-byte swizzle, zero fill past the last row.
+bool encode_out_map(CUtensorMap* m, const void* base, int rows, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tile map of codes [rows][H * bits / 8] uint8 (MXFP4 4 bits, MXFP6 6 bits a
 // code): box of one k-step's codes (32 or 48 bytes) x 256 rows, no swizzle
 // (the decoding warps read each row's bytes).
@@ -375,6 +392,7 @@ struct StepArgs {
   void* residual_out;
   int32_t tokens = 1;
   const int32_t* idx_out = nullptr;
+  void* out = nullptr;  // out_proj result [rows][H] (weights out_proj), or nullptr
 };
 
 // Host-side checks of a step's arguments (before any launch): rows in range,
@@ -395,6 +413,7 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
     if (q && !aligned(q, 16)) return GDN_ERR_ARG;
   if (!aligned(a.idx, 4) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 2)) return GDN_ERR_ARG;
   if (a.tokens > 1 && (!a.idx_out || !aligned(a.idx_out, 4))) return GDN_ERR_ARG;
+  if (a.out && (!w->out_proj || !aligned(a.out, 16) || !aligned(w->out_proj, 16))) return GDN_ERR_ARG;
   const size_t H = (size_t)c.hidden;
   const size_t xb = (size_t)a.rows * H * 2;
   const size_t coreb = (size_t)a.rows * c.num_v_heads * c.head_v_dim * 2;
@@ -407,12 +426,15 @@ gdn_status check_step_args(const gdn_decode_config& c, const StepArgs& a, const 
                     {a.conv_state, convb}, {a.ssm_state, ssmb}, {w->qkvz, qkvz_bytes(c)},
                     {w->ba, (size_t)n_ba(c) * H * 2}, {w->input_norm_w, H * 2},
                     {w->qkvz_scales, c.qkvz_format != GDN_W_BF16 ? (size_t)n_qkvz(c) * H / 32 : 0},
+                    {a.out ? w->out_proj : nullptr, a.out ? H * c.num_v_heads * c.head_v_dim * 2 : 0},
                     {scratch, scratch_bytes}};
-  const Rg outs[] = {{a.core_out, coreb}, {a.residual_out, xb}};
+  const Rg outs[] = {{a.core_out, coreb}, {a.residual_out, xb}, {a.out, a.out ? xb : 0}};
   for (const Rg& o : outs)
     for (const Rg& i : ins)
       if (overlaps(o.p, o.n, i.p, i.n)) return GDN_ERR_ARG;
   if (overlaps(a.core_out, coreb, a.residual_out, xb)) return GDN_ERR_ARG;
+  if (overlaps(a.out, a.out ? xb : 0, a.core_out, coreb) || overlaps(a.out, a.out ? xb : 0, a.residual_out, xb))
+    return GDN_ERR_ARG;
   if (overlaps(a.conv_state, convb, a.ssm_state, ssmb)) return GDN_ERR_ARG;
   return GDN_OK;
 }
@@ -450,7 +472,10 @@ void fill_params(const gdn_decode_config& c, const Plan& pl, const Layout& lay, 
   p->A_log = w->A_log;
   p->dt_bias = (const __nv_bfloat16*)w->dt_bias;
   p->gnorm_w = (const __nv_bfloat16*)w->gated_norm_w;
+  p->out = (__nv_bfloat16*)a.out;
+  p->w_out = a.out ? (const __nv_bfloat16*)w->out_proj : nullptr;
   p->ctr = (WsCounters*)(base + lay.ctr);
+  p->core_flag = (unsigned long long*)(base + lay.core_flag);
   p->norm_part = (unsigned long long*)(base + lay.norm_part);
   p->xn = (__nv_bfloat16*)(base + lay.xn);
   p->proj_part = (unsigned long long*)(base + lay.proj_part);
@@ -468,6 +493,16 @@ bool weight_maps(const gdn_decode_config& c, const gdn_decode_weights* w, MapCac
   }
   p->tm_qkvz = m->qkvz;
   p->tm_ba = m->ba;
+  if (p->out) {
+    if (m->out_ptr != w->out_proj) {
+      if (!encode_out_map(&m->out, w->out_proj, c.hidden, c.num_v_heads * c.head_v_dim)) {
+        m->out_ptr = nullptr;
+        return false;
+      }
+      m->out_ptr = w->out_proj;
+    }
+    p->tm_out = m->out;
+  }
   return true;
 }
 
@@ -527,6 +562,7 @@ gdn_status launch_row_tiles(const gdn_decode_config& c, const Plan& pl, const La
     t.residual = a.residual ? (const char*)a.residual + r0 * xrow : nullptr;
     t.idx = a.idx + r0 / a.tokens;
     t.idx_out = a.idx_out ? a.idx_out + r0 : nullptr;
+    t.out = a.out ? (char*)a.out + r0 * xrow : nullptr;
     t.core_out = (char*)a.core_out + r0 * crow;
     t.residual_out = (char*)a.residual_out + r0 * xrow;
     StepParams p;  // on the stack: the step allocates nothing
@@ -645,6 +681,25 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x, const v
   gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
   if (st != GDN_OK) return st;
   return launch_row_tiles(h->cfg, h->plan, h->lay, (char*)h->ws, a, &h->maps, &h->pdl, (cudaStream_t)stream);
+}
+
+gdn_status gdn_decode_step_out(gdn_decode_t* h, int32_t rows, const void* x, const void* residual,
+                               const gdn_decode_weights* w, const int32_t* state_indices, void* conv_state,
+                               void* ssm_state, void* core_out, void* residual_out, void* out, void* stream) {
+  if (!h || !out) return GDN_ERR_ARG;
+  StepArgs a{rows, x, residual, w, state_indices, conv_state, ssm_state, core_out, residual_out};
+  a.out = out;
+  gdn_status st = check_step_args(h->cfg, a, h->ws, h->lay.total);
+  if (st != GDN_OK) return st;
+  // the tensor-core kernel's out_proj phase: a freed weight ring large enough,
+  // at most kOpMaxCols output columns per CTA, K a multiple of its chunk
+  const Plan& pl = h->plan;
+  const size_t ring = (size_t)pl.stages * kTileM * kKStep * 2 + (size_t)pl.rstages * (size_t)kTileM *
+                                                                     (h->cfg.qkvz_format == GDN_W_MXFP6 ? 48 : 32);
+  if (pl.engine != GDN_ENGINE_TCGEN05 || ring < tensor_core_out_proj_smem() ||
+      (h->cfg.hidden + pl.G - 1) / pl.G > 64 || (h->cfg.num_v_heads * h->cfg.head_v_dim) % 256 != 0)
+    return GDN_ERR_UNSUPPORTED;
+  return launch_row_tiles(h->cfg, pl, h->lay, (char*)h->ws, a, &h->maps, &h->pdl, (cudaStream_t)stream);
 }
 
 gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, const void* x, const void* residual,

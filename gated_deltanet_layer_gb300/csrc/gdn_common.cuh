@@ -100,9 +100,12 @@ struct StepParams {
   const float* A_log;
   const __nv_bfloat16* dt_bias;
   const __nv_bfloat16* gnorm_w;
+  const __nv_bfloat16* w_out;   // out_proj [H][Hv * dv] (with `out`)
+  __nv_bfloat16* out;           // out_proj result [rows][H], or nullptr: no out_proj
   // workspace
   WsCounters* ctr;
   unsigned long long* norm_part;  // [kMaxRows][num_ctas] tagged words
+  unsigned long long* core_flag;  // [num_ctas] tagged words: a CTA's core rows are written (out_proj)
   __nv_bfloat16* xn;              // [kMaxRows][H] (CUDA-core engine)
   unsigned long long* proj_part;  // [num_tiles][max_contrib][kMaxRows][kTileM] tagged words
   // TMA descriptors of the weights: bf16 boxes of 64 columns x 256 rows with
@@ -110,6 +113,7 @@ struct StepParams {
   // codes) x 256 rows (tensor-core engine).
   CUtensorMap tm_qkvz;
   CUtensorMap tm_ba;
+  CUtensorMap tm_out;  // out_proj [H][Hv*dv] bf16: boxes of 64 columns x 64 rows, 128-byte swizzle
   const struct PlanDev* plan;  // stream-K plan, in the workspace (written once at create)
 };
 

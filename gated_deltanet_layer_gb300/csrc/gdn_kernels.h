@@ -22,6 +22,8 @@ size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, int fmt);
 uint32_t tensor_core_xpad(int xslots);
 size_t tensor_core_static_smem();
 int tensor_core_max_stages();
+// Shared memory the out_proj phase needs in the freed weight ring.
+size_t tensor_core_out_proj_smem();
 int tensor_core_max_rstages();
 
 }  // namespace gdn

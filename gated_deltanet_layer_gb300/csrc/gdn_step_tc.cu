@@ -40,6 +40,7 @@
 // deadline error, and the CTA waits for its own copies and MMAs in flight,
 // frees its TMEM and returns.
 #include "gdn_kernels.h"
+#include "gdn_outproj.cuh"
 #include "gdn_phases.cuh"
 #include "gdn_tc_ptx.cuh"
 
@@ -83,6 +84,7 @@ struct TcShared {
   uint64_t acc_full[2];     // accumulator ready for the drain
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
+  uint64_t obar[kOpMaxStages];  // out_proj: a stage's weight rows landed
   uint32_t tmem_base;
   int abort;
 };
@@ -787,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
     tc::prefetch_tensormap(&p.tm_ba);
+    if (p.out) tc::prefetch_tensormap(&p.tm_out);
     ts.abort = 0;
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
@@ -801,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
       tc::mbar_init(&ts.rempty[r], 1);
     }
     tc::mbar_init(&ts.mma_done, 1);
+    for (int s = 0; s < kOpMaxStages; ++s) tc::mbar_init(&ts.obar[s], 1);
     tc::fence_mbar_init();
   }
   __syncthreads();
@@ -883,8 +887,26 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     tc::tmem_dealloc(tmem, kTmemCols);
   }
   tl_stamp(p, TL_PROJ_END);
+  // out_proj's first weight chunks stream into the freed ring: now in a CTA
+  // without recurrence tasks, after its tasks in one with (so they do not
+  // compete with the tasks' loads)
+  const size_t ring_bytes = (size_t)p.stages * kWBytes + (size_t)p.rstages * code_tile_bytes<FMT>();
+  if (!aborted && p.out && warp == 0 && rt0 >= rt1) out_proj_prefetch(p, sW, ring_bytes, ts.obar);
   if (!aborted) {
-    phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
+    const bool rec_ok = phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
+    // out_proj over the core rows of every CTA, in the freed weight ring
+    if (p.out) {
+      if (rec_ok) {
+        phase_out_proj(p, sW, ring_bytes, ts.obar, L, rt0 < rt1);
+      } else if (warp == 0 && rt0 >= rt1) {  // let the prefetched chunks land before the CTA ends (bounded)
+        const OpShape o(p, ring_bytes);
+        for (int s2 = 0; s2 < min(o.ns, o.nch); ++s2) {
+          const unsigned long long c0 = globaltimer_ns();
+          for (uint32_t it = 0; !tc::mbar_try_wait(&ts.obar[s2], 0); ++it)
+            if ((it & 63) == 0 && globaltimer_ns() - c0 > kCleanupNs) break;
+        }
+      }
+    }
     tl_stamp(p, TL_END);
   }
 }
@@ -927,6 +949,7 @@ size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, int fmt) {
 }
 size_t tensor_core_static_smem() { return sizeof(SmemPhases) + sizeof(SmemTask) + sizeof(TcShared); }
 int tensor_core_max_stages() { return kMaxStages; }
+size_t tensor_core_out_proj_smem() { return kOpRing; }
 int tensor_core_max_rstages() { return kMaxRStages; }
 
 }  // namespace gdn

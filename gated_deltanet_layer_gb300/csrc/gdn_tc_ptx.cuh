@@ -70,6 +70,30 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
                "r"(x), "r"(y)
                : "memory");
 }
+// 1-D bulk copy of `bytes` from global to shared memory, completing on the
+// mbarrier (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// 16-byte asynchronous copy global -> shared memory at L2 (no L1 copy kept:
+// the source may be written by other CTAs of the same launch); groups of
+// them are committed and waited for by the issuing thread.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n (0..2) of this thread's committed groups are pending.
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  if (n <= 0)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1)
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

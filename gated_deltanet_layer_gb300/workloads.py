@@ -100,6 +100,10 @@ class LayerShape:
         H = self.hidden
         return H * 2 * (1 if first_layer else 2) + H * 2 + self.num_v_heads * self.head_v_dim * 2 + 4
 
+    def out_proj_bytes(self, rows: int) -> int:
+        """What out_proj adds to a step: its weights and the rows' output."""
+        return self.hidden * self.num_v_heads * self.head_v_dim * 2 + rows * self.hidden * 2
+
     def verify_bytes(self, seqs: int, tokens: int) -> int:
         """A verify step: the weights, each sequence's input state read once,
         one conv + SSM state written per token, and the rows' activations."""
@@ -174,6 +178,12 @@ def make_weights(shape: LayerShape, seed: int, *, weight_std: float = 0.02,
     w["dt_bias"] = _bf16(_normal(rng, (Hv,), 0.5))
     w["gated_norm_w"] = _bf16(_normal(rng, (shape.head_v_dim,), norm_std))
     return w
+
+
+def make_out_proj(shape: LayerShape, seed: int, *, std: float = 0.02) -> torch.Tensor:
+    """The layer's out_proj [H, Hv*dv] as a bf16 CPU tensor ~N(0, std)."""
+    rng = _rng(seed)
+    return _bf16(_normal(rng, (shape.hidden, shape.num_v_heads * shape.head_v_dim), std))
 
 
 def make_state(shape: LayerShape, seed: int, *, ssm_std: float = 0.1) -> dict:

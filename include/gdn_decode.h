@@ -157,6 +157,7 @@ typedef struct {
   const float* A_log;           /* [Hv] f32 */
   const void* dt_bias;          /* [Hv] bf16 */
   const void* gated_norm_w;     /* [dv] bf16 */
+  const void* out_proj;         /* [H][Hv*dv] bf16, read by gdn_decode_step_out only; else NULL */
 } gdn_decode_weights;
 
 typedef struct gdn_decode gdn_decode_t;
@@ -204,6 +205,23 @@ gdn_status gdn_decode_step(gdn_decode_t* h, int32_t rows, const void* x,
                            void* ssm_state, void* core_out, void* residual_out,
                            void* stream);
 
+/* A decode step followed by the layer's out_proj in the same launch:
+ * out[w][n] = bf16(sum_j out_proj[n][j] core[w][j]) over the Hv*dv core
+ * columns, written to `out` ([rows][H] bf16; core_out is still written).
+ * The pages fold out_proj into the GDN launch this way (SGLang #43558,
+ * commit text of the SGLANG_QWEN3_8_DENSE_MONO_OPROJ fold, "dense_gdn
+ * (K1Build.oproj)": every CTA publishes its core rows with a flag, CTAs poll
+ * the flags and each runs its hidden columns of out_proj over the K share);
+ * for one tensor-parallel rank's shard `out` is the rank's partial, to be
+ * summed across ranks by the caller. Needs w->out_proj, the tensor-core
+ * engine, at most 64 output columns per CTA (H <= 64 x grid) and Hv*dv a
+ * multiple of 256 (else GDN_ERR_UNSUPPORTED). The out_proj weights are read
+ * early like in_proj's (see "Launch options"). Other behaviour as
+ * gdn_decode_step. */
+gdn_status gdn_decode_step_out(gdn_decode_t* h, int32_t rows, const void* x, const void* residual,
+                               const gdn_decode_weights* w, const int32_t* state_indices, void* conv_state,
+                               void* ssm_state, void* core_out, void* residual_out, void* out, void* stream);
+
 /* A verify step (multi-token, a state per token): `seqs` sequences of
  * `tokens` tokens each (rows s*tokens + t of x, residual, core_out and
  * residual_out; seqs * tokens <= max_rows, tokens <= GDN_ROWS_PER_LAUNCH).
@@ -232,8 +250,9 @@ gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, cons
 /* Synchronise `stream` and read the sticky error word. Returns GDN_OK, or the
  * recorded device status; *detail (optional) receives the raw word:
  * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
- * 3 projection tile, 4 a tensor-core pipeline stage, 5 a recurrence state
- * tile), 15..0 the CTA (deadline) or row (index error). This is the host
+ * 3 projection tile, 4 a tensor-core pipeline stage, 6 the core rows before
+ * out_proj, 7 an out_proj weight chunk), 15..0 the CTA (deadline) or row
+ * (index error). This is the host
  * side of the pages' failure design: every wait in the launch is bounded, a
  * CTA that gives up records which wait in a sticky failed word, and the host
  * reads that word after the step without a fallback path (vLLM #60833,
