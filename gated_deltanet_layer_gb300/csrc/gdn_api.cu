@@ -110,8 +110,10 @@ gdn_status validate(const gdn_decode_config* c) {
 // (k-block kb = g / T, tile t = g % T) holds the `kblock` k-steps kb*kblock ..
 // of tile t. With kblock = ksteps the order is tile-major (a CTA sweeps K of
 // one tile, then the next); the tensor-core engine of a large layer uses
-// kblock = 16, so a CTA's units touch at most two k-blocks and the normed
-// input it needs (<= 32 k-steps) fits in shared memory. Every unit counts the
+// kblock = 16 (8 with MXFP4 weights, whose two windows halve the room), so a
+// CTA's units touch at most two k-blocks and the normed input it needs (<= 32
+// k-steps; 24 with MXFP4) fits in shared memory. Longer k-blocks also mean
+// fewer partials per tile for the recurrence to add. Every unit counts the
 // same, also one of the partial in_proj_ba tile: a unit's time is set by its
 // fixed per-unit cost, not by its row count. CTA c takes units
 // [unit_begin[c], unit_begin[c+1]) with unit_begin[c] = floor(c * U / G).
@@ -130,10 +132,14 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
   if (chunk > kMaxNormChunk) return GDN_ERR_UNSUPPORTED;
   const long long U = (long long)T * KS;
   const long long per_cta = (U + G - 1) / G;
+  // the normed-input window of the tensor-core engine, in k-steps, and the
+  // k-block that keeps a CTA's units inside it
+  const bool mx4 = c.qkvz_format == GDN_W_MXFP4;
+  const int max_window = mx4 ? kMaxBSlotsMxfp4 : kMaxBSlots;
   int KB = KS;
-  if (engine == GDN_ENGINE_TCGEN05 && per_cta + 1 > kMaxBSlots) {
-    if (KS % kKBlock != 0) return GDN_ERR_UNSUPPORTED;
-    KB = kKBlock;
+  if (engine == GDN_ENGINE_TCGEN05 && per_cta + 1 > max_window) {
+    KB = mx4 ? kKBlockMxfp4 : kKBlock;
+    if (KS % KB != 0) return GDN_ERR_UNSUPPORTED;
   }
   pl->kblock = KB;
   for (int cta = 0; cta <= G; ++cta) pl->unit_begin[cta] = (int)((long long)cta * U / G);
@@ -178,7 +184,7 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
     }
     pl->ks_first[cta] = (unsigned short)first;
     pl->nb_slots[cta] = (unsigned char)std::min(len, 255);
-    if (engine == GDN_ENGINE_TCGEN05 && len > kMaxBSlots) return GDN_ERR_UNSUPPORTED;
+    if (engine == GDN_ENGINE_TCGEN05 && len > max_window) return GDN_ERR_UNSUPPORTED;
   }
   // k-step owners (tensor-core engine): the first CTA whose window holds it
   for (int cta = 0; cta < G; ++cta) pl->own_mask[cta] = 0;
@@ -282,6 +288,7 @@ void set_plan_params(const Plan& pl, StepParams* p) {
   p->norm_chunk = pl.norm_chunk; p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
   p->kblock = pl.kblock;
   p->stages = pl.stages; p->rstages = pl.rstages; p->xslots = pl.xslots; p->xpad = pl.xpad;
+  p->dyn_free = pl.smem > 1024 ? (unsigned int)(pl.smem - 1024) : 0u;  // 1 KB of it aligns the ring
 }
 
 // The engine a config runs with and its plan: the requested engine, or for

@@ -19,8 +19,10 @@ constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
 constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
 constexpr int kMaxSegs = 16;               // tile segments in one CTA's unit range
-constexpr int kKBlock = 8;                 // k-steps per k-block in the k-block-major order
-constexpr int kMaxBSlots = 24;             // normed-input k-steps a CTA keeps in shared memory
+constexpr int kKBlock = 16;                // k-steps per k-block in the k-block-major order
+constexpr int kKBlockMxfp4 = 8;            // the same with MXFP4 weights (two windows: xn and its quantised copy)
+constexpr int kMaxBSlots = 32;             // normed-input k-steps a CTA keeps in shared memory
+constexpr int kMaxBSlotsMxfp4 = 24;        // the same with MXFP4 weights
 constexpr int kMaxKHeads = 64;             // key heads of a layer (conv-group counters)
 
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
@@ -59,7 +61,7 @@ struct WsCounters {
 // Timeline stamp points of a CTA.
 enum TlPoint { TL_START = 0, TL_NORM_OUT, TL_NORM_IN, TL_XN_OUT, TL_PROJ_START, TL_PROJ_END,
                TL_REC_WAITED, TL_END, TL_REC_INPUTS, TL_MMA_FIRST, TL_MMA_LAST, TL_ISSUED,
-               TL_R_STAGED, TL_REC_STATE, TL_UNIT_READY = 16, TL_UNIT_ISSUED = 32 };
+               TL_R_STAGED, TL_REC_STATE, TL_TASK = 16, TL_UNIT_ISSUED = 32 };
 
 struct StepParams {
   // shapes
@@ -78,6 +80,7 @@ struct StepParams {
   int rstages;         // MXFP4 / MXFP6 code tiles in flight per CTA
   int xslots;          // normed-input k-steps a CTA keeps in shared memory
   unsigned int xpad;   // bytes past the window an MMA may read (and norm-sum scratch)
+  unsigned int dyn_free;  // dynamic shared memory from the ring's start, free once the projection is done
   float norm_eps, gnorm_eps, l2_eps, q_scale;
   unsigned long long deadline_ns;
   int debug_flags;

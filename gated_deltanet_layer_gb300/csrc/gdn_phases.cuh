@@ -345,6 +345,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       for (int jj = 0; jj < kMaxSlots; ++jj)
         if (jj < nc) acc += tagged_value(pw[jj]);
       const float pv = round_bf16(acc);
+      float y2 = 0.f;  // y^2 of a q or k output, for the L2 norms
       if (i < 3 * DK) {
         const float c0 = tap0, c1 = tap1, c2 = tap2;
         tap0 = c1; tap1 = c2; tap2 = pv;  // the taps after this token
@@ -365,6 +366,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
           cs[2] = __float2bfloat16_rn(pv);
         }
         if (i < 2 * DK) {
+          y2 = y * y;
           if (MULTI) {
             if (h % p.group == 0) {  // the group's first value head writes its q/k taps
               __nv_bfloat16* cs = p.conv_state + ((size_t)oslot * p.C + n) * 3;
@@ -380,6 +382,10 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
         }
       } else {
         st.z[i - 3 * DK] = pv;
+      }
+      if (warp < 2 * DK / 32) {  // whole warps of q (then k) outputs: their sums of squares
+        y2 = warp_sum(y2);
+        if (lane == 0) st.red[warp] = y2;
       }
     }
     if (ba_warp) {
@@ -404,17 +410,14 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
       group_old = atom_add_relaxed_u32(&p.ctr->conv_group[w][kh], 1u);
       if ((p.debug_flags & kDebugTimeline) && task == t0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
     }
-    // L2 norms of q and k: every warp sums all of q^2 and k^2 itself (the
-    // same order in every warp), which saves a CTA barrier
+    // L2 norms of q and k from the per-warp sums of squares, added in warp
+    // order (the same arithmetic in every thread, and in the pipelined phase)
     float sq = 0.f, sk = 0.f;
 #pragma unroll
     for (int i = 0; i < DK / 32; ++i) {
-      const float a = st.q[i * 32 + lane], b = st.k[i * 32 + lane];
-      sq = fmaf(a, a, sq);
-      sk = fmaf(b, b, sk);
+      sq += st.red[i];
+      sk += st.red[DK / 32 + i];
     }
-    sq = warp_sum(sq);
-    sk = warp_sum(sk);
     const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
     const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
     float4 k4[CH], q4[CH];  // this lane's chunks of k^ and q^

@@ -1,0 +1,440 @@
+// The recurrence phase of a CTA with two or more (row, value head) tasks,
+// with the state traffic moved off the threads and the input loads issued a
+// task ahead:
+//   * state tiles (DK x DK contiguous elements per task) live in a ring of
+//     three shared-memory buffers, task j in buffer j % 3: bulk copies bring
+//     task j + 2's tile in while task j runs; the threads update a tile in
+//     place; a bulk copy takes it back out (task 0's tile was prefetched
+//     into L2 under the projection);
+//   * the projection partials of task j + 1 (and its old conv taps) are
+//     loaded while task j updates its state, and polled when j + 1 starts;
+//   * the key-head group's counter of task j is read back at task j + 1, and
+//     the new q/k taps of task j (held in the registers of their threads)
+//     are written then if j was the group's last reader.
+// Every value is computed with the single-task phase's arithmetic in the
+// same order (the same state layout per row, the same sums), so a row's
+// results do not depend on which path ran it. All threads pass the same
+// barriers; a wait that runs out stops the phase at the next barrier (the
+// error is recorded) after the copies in flight have landed.
+#pragma once
+
+#include "gdn_phases.cuh"
+#include "gdn_tc_ptx.cuh"
+
+namespace gdn {
+
+constexpr uint32_t kWaitState = 8;  // error-word id: a state tile's copy into shared memory
+
+// One task's inputs (two, alternating between tasks).
+struct StagedTask {
+  alignas(16) float q[128];  // q, k after conv + SiLU (not yet normalised)
+  alignas(16) float k[128];
+  alignas(16) float v[128];  // v after conv + SiLU
+  alignas(16) float z[128];  // z (bf16 projection)
+  alignas(16) float o[128];  // o = S q^
+  float red[kWarps];         // per-warp sums of q^2 (warps 0 .. dk/32-1), then k^2
+  float ba[2];               // b, a (bf16 projections)
+  int last;                  // the previous task was its key-head group's last reader
+};
+
+template <int DK, bool STATE_BF16>
+struct StagedLayout {
+  static constexpr uint32_t kStateBytes = DK * DK * (STATE_BF16 ? 2 : 4);
+  static constexpr int kBufs = 3;
+  static constexpr size_t kBytes = kBufs * (size_t)kStateBytes + 2 * sizeof(StagedTask);
+  static_assert(kStateBytes % 16 == 0, "bulk copy size");
+};
+
+// The shared memory the staged phase needs.
+template <int DK, bool STATE_BF16>
+__host__ __device__ constexpr size_t staged_recurrence_bytes() {
+  return StagedLayout<DK, STATE_BF16>::kBytes;
+}
+
+// A thread's loads of one task's inputs: the partials of output `i` = tid
+// (q, k, v, z) and its conv taps and weights; b and a one slot per lane of
+// the last two warps.
+struct StagedLoads {
+  static constexpr int kMaxSlots = 24;  // partials per tile (the plan's bound)
+  unsigned long long pw[kMaxSlots];
+  const unsigned long long* src;
+  int nc;
+  unsigned long long baw[1];
+  const unsigned long long* ba_src;
+  int ba_nc;
+  uint2 cwv;                 // conv weights of the channel
+  __nv_bfloat16 tap[3];      // its old taps
+  float A_log;               // the head's constants
+  __nv_bfloat16 dt_bias;
+};
+
+// The L2 prefetch of a task's state tile (nothing for a pad row).
+template <int DK, bool STATE_BF16>
+__device__ __forceinline__ void prefetch_state_l2(const StepParams& p, int task) {
+  using SL = StagedLayout<DK, STATE_BF16>;
+  const int w = task / p.Hv, h = task - w * p.Hv;
+  const int slot = p.idx[w];
+  if (!row_is_live(p, slot)) return;
+  tc::prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(p.ssm_state) + ((size_t)slot * p.Hv + h) * SL::kStateBytes,
+                       SL::kStateBytes);
+}
+
+template <int DK, bool STATE_BF16>
+__device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint64_t* sbar, int L, int t0,
+                                        int t1) {
+  using SL = StagedLayout<DK, STATE_BF16>;
+  constexpr int LPR = StateRegs<DK>::LPR;
+  constexpr int RPW = StateRegs<DK>::RPW;
+  constexpr int NR = StateRegs<DK>::NR;
+  constexpr int CH = StateRegs<DK>::CH;
+  constexpr int kMaxSlots = StagedLoads::kMaxSlots;
+  constexpr size_t kSlot = (size_t)kMaxRows * kTileM;
+  static_assert(4 * DK <= kThreads, "task layout");
+  const int cta = blockIdx.x, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int sub = lane % LPR, rw = lane / LPR;
+  const int n = t1 - t0;
+  auto sbuf = [&](int j) { return ring + (size_t)(j % SL::kBufs) * SL::kStateBytes; };  // task j's tile
+  StagedTask* tb = reinterpret_cast<StagedTask*>(ring + SL::kBufs * (size_t)SL::kStateBytes);
+  const bool ba_warp = warp >= kWarps - 2;
+
+  auto proj_row = [&](int i, int h, int kh) -> int {
+    if (i < DK) return kh * DK + i;
+    if (i < 2 * DK) return p.Hk * DK + kh * DK + (i - DK);
+    if (i < 3 * DK) return 2 * p.Hk * DK + h * DK + (i - 2 * DK);
+    if (i < 4 * DK) return p.C + h * DK + (i - 3 * DK);
+    return p.Nqkvz + (i == 4 * DK ? h : p.Hv + h);
+  };
+  auto part_src = [&](int n_row, int w, int& nc) {
+    const int t = n_row < p.Nqkvz ? (n_row >> kTileShift) : p.tiles_qkvz + ((n_row - p.Nqkvz) >> kTileShift);
+    const int r = (n_row < p.Nqkvz ? n_row : n_row - p.Nqkvz) & (kTileM - 1);
+    nc = p.plan->tile_num_ctas[t];
+    return p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
+  };
+
+  auto state_src = [&](int slot, int h) {
+    return reinterpret_cast<uint8_t*>(p.ssm_state) + ((size_t)slot * p.Hv + h) * SL::kStateBytes;
+  };
+  // Thread 0: the bulk copy of task j's state tile into its buffer,
+  // completing on that buffer's mbarrier. Returns whether one was issued
+  // (not for a pad row).
+  auto issue_state = [&](int j) -> bool {
+    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv;
+    const int slot = p.idx[w];
+    if (!row_is_live(p, slot)) return false;
+    uint64_t* bar = &sbar[j % SL::kBufs];
+    tc::mbar_arrive_expect_tx(bar, SL::kStateBytes);
+    tc::bulk_load(sbuf(j), state_src(slot, h), SL::kStateBytes, bar);
+    return true;
+  };
+  // Every thread: issue its loads of task j's inputs (nothing for a pad row,
+  // or when `real` is false: then the fields are only cleared).
+  StagedLoads ld;
+  auto issue_inputs = [&](int j, bool real) {
+    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int slot = real ? p.idx[w] : 0;
+    // every field is assigned on every path (and the call made after every
+    // task), so nothing of a task's loads stays live past its use
+    ld.nc = 0;
+    ld.ba_nc = 0;
+    ld.src = nullptr;
+    ld.ba_src = nullptr;
+    ld.baw[0] = 0ull;
+#pragma unroll
+    for (int jj = 0; jj < kMaxSlots; ++jj) ld.pw[jj] = 0ull;
+    ld.cwv = make_uint2(0u, 0u);
+    ld.tap[0] = ld.tap[1] = ld.tap[2] = __float2bfloat16_rn(0.f);
+    ld.A_log = 0.f;
+    ld.dt_bias = __float2bfloat16_rn(0.f);
+    if (!row_is_live(p, slot)) return;
+    ld.A_log = p.A_log[h];
+    ld.dt_bias = p.dt_bias[h];
+    if (ba_warp) {  // first: these lanes also have an output of their own
+      ld.ba_src = part_src(proj_row(4 * DK + (warp - (kWarps - 2)), h, kh), w, ld.ba_nc) + (size_t)lane * kSlot;
+      if (lane < ld.ba_nc) ld.baw[0] = ld_tagged(ld.ba_src);
+    }
+    if (tid < 4 * DK) {
+      const int nr = proj_row(tid, h, kh);
+      ld.src = part_src(nr, w, ld.nc);
+#pragma unroll
+      for (int jj = 0; jj < kMaxSlots; ++jj)
+        if (jj < ld.nc) ld.pw[jj] = ld_tagged(ld.src + (size_t)jj * kSlot);
+      if (tid < 3 * DK) {
+        const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + nr) * 3;
+        ld.tap[0] = cs[0];
+        ld.tap[1] = cs[1];
+        ld.tap[2] = cs[2];
+        ld.cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)nr * 4);
+      }
+    }
+  };
+
+  // bulk copies in flight into each buffer (thread 0) and the buffers'
+  // mbarrier phases (every thread)
+  uint32_t pending = 0, ph = 0;
+  if (tid == 0) {
+    tc::fence_proxy_async_smem();  // the ring's earlier generic accesses before the copies
+    for (int j = 0; j < min(n, SL::kBufs); ++j)
+      if (issue_state(j)) pending |= 1u << j;
+  }
+  issue_inputs(0, true);
+  // timeline (test hook): stamps 16 + 4 j + k of the first four tasks
+  auto stamp = [&](int j, int k) {
+    if ((p.debug_flags & kDebugTimeline) && j < 4 && tid == 0) p.ctr->tl_cta[cta][TL_TASK + 4 * j + k] = globaltimer_ns();
+  };
+  const float gw = tid < DK ? bf16_to_f(p.gnorm_w[tid]) : 0.f;
+  bool ok = true;
+  unsigned int group_old = 0;  // thread 0: the previous task's group counter
+  bool prev_live = false;
+  int prev_slot = 0, prev_row = 0;
+  float nt0 = 0.f, nt1 = 0.f, nt2 = 0.f;  // the previous task's new q/k taps of this thread's channel
+  for (int j = 0; j < n; ++j) {
+    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int slot = p.idx[w];
+    const bool live = row_is_live(p, slot);
+    StagedTask& T = tb[j & 1];
+    __nv_bfloat16* core = p.core_out + (size_t)w * p.Hv * DK + (size_t)h * DK;
+    const int b = j % SL::kBufs;  // the tile's buffer and its mbarrier
+    float c1 = 0.f, c2 = 0.f, pvq = 0.f;  // this task's new taps (threads < 2 dk)
+    if (live) {
+      // ---- inputs: partial sums, conv update + SiLU, per-warp sums of squares
+      if (tid < 4 * DK) {
+        const int i = tid;
+        if (!poll_tagged<kMaxSlots>(p, ld.pw, ld.src, kSlot, ld.nc, L, kWaitTile)) ok = false;
+        if (i == 0 && (p.debug_flags & kDebugTimeline) && j == 0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
+        float acc = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < kMaxSlots; ++jj)
+          if (jj < ld.nc) acc += tagged_value(ld.pw[jj]);
+        const float pv = round_bf16(acc);
+        float y2 = 0.f;
+        if (i < 3 * DK) {
+          const float c0 = bf16_to_f(ld.tap[0]);
+          c1 = bf16_to_f(ld.tap[1]);
+          c2 = bf16_to_f(ld.tap[2]);
+          float y = bf16_lo(ld.cwv.x) * c0;
+          y = fmaf(bf16_hi(ld.cwv.x), c1, y);
+          y = fmaf(bf16_lo(ld.cwv.y), c2, y);
+          y = fmaf(bf16_hi(ld.cwv.y), pv, y);
+          y = silu_f(y);
+          if (i < DK) {
+            T.q[i] = y;
+          } else if (i < 2 * DK) {
+            T.k[i - DK] = y;
+          } else {
+            T.v[i - 2 * DK] = y;
+            __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + proj_row(i, h, kh)) * 3;  // own channel
+            cs[0] = __float2bfloat16_rn(c1);
+            cs[1] = __float2bfloat16_rn(c2);
+            cs[2] = __float2bfloat16_rn(pv);
+          }
+          if (i < 2 * DK) {
+            y2 = y * y;
+            pvq = pv;
+          }
+        } else {
+          T.z[i - 3 * DK] = pv;
+        }
+        if (warp < 2 * DK / 32) {
+          y2 = warp_sum(y2);
+          if (lane == 0) T.red[warp] = y2;
+        }
+      }
+      if (ba_warp) {
+        if (!poll_tagged<1>(p, ld.baw, ld.ba_src, 0, lane < ld.ba_nc ? 1 : 0, L, kWaitTile)) ok = false;
+        const float v = tagged_value(ld.baw[0]);
+        float acc = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < kMaxSlots; ++jj) {  // slot order, as for the other outputs
+          const float x = __shfl_sync(0xffffffffu, v, jj);
+          if (jj < ld.ba_nc) acc += x;
+        }
+        if (lane == 0) T.ba[warp - (kWarps - 2)] = round_bf16(acc);
+      }
+      stamp(j, 0);  // inputs in
+      // ---- this task's state tile in shared memory (bounded wait)
+      if (ok) {
+        const uint32_t par = (ph >> b) & 1u;
+        bool landed = tc::mbar_try_wait(&sbar[b], par);
+        if (!landed) {
+          const unsigned long long c0 = globaltimer_ns();
+          for (uint32_t it = 1;; ++it) {
+            if (tc::mbar_try_wait(&sbar[b], par)) { landed = true; break; }
+            if ((it & 63) == 0) {
+              if ((ld_relaxed_u32(&p.ctr->error) >> 24) == kStatusDeadline) break;
+              if (globaltimer_ns() - c0 > p.deadline_ns) {
+                record_error(p.ctr, kStatusDeadline, kWaitState, cta);
+                break;
+              }
+            }
+          }
+        }
+        if (landed) {
+          ph ^= 1u << b;  // this buffer's copy is consumed
+          if (tid == 0) pending &= ~(1u << b);
+        } else {
+          ok = false;
+        }
+      }
+    }
+    if (!__syncthreads_and(ok)) {  // S1: T complete, the state tile landed
+      ok = false;
+      break;
+    }
+    stamp(j, 1);
+    // thread 0: this task's group counter (read back at the next task); the
+    // previous task's flag for its new q/k taps
+    if (tid == 0) {
+      T.last = prev_live && ((group_old + 1) % (unsigned)p.group) == 0;
+      if (live) group_old = atom_add_relaxed_u32(&p.ctr->conv_group[w][kh], 1u);
+      if ((p.debug_flags & kDebugTimeline) && j == 0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
+    }
+    if (live) {
+      // ---- L2 norms of q and k, gates (the single-task phase's arithmetic)
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int i = 0; i < DK / 32; ++i) {
+        sq += T.red[i];
+        sk += T.red[DK / 32 + i];
+      }
+      const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
+      const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
+      const float sp_in = T.ba[1] + bf16_to_f(ld.dt_bias);
+      const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
+      const float g = -expf(ld.A_log) * sp;
+      const float eg = expf(g);
+      const float beta = 1.0f / (1.0f + expf(-T.ba[0]));
+      uint8_t* sb = sbuf(j);  // each thread reads and writes only its own elements
+      float4 k4[CH], q4[CH];  // this lane's chunks of k^ and q^
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const float4 kq = *reinterpret_cast<const float4*>(&T.k[(sub + LPR * c) * 4]);
+        const float4 qq = *reinterpret_cast<const float4*>(&T.q[(sub + LPR * c) * 4]);
+        k4[c] = make_float4(kq.x * inv_k, kq.y * inv_k, kq.z * inv_k, kq.w * inv_k);
+        q4[c] = make_float4(qq.x * inv_q, qq.y * inv_q, qq.z * inv_q, qq.w * inv_q);
+      }
+      // one state row of this lane at a time (the tile is in shared memory):
+      // the same arithmetic per row as with all rows in registers
+#pragma unroll 1
+      for (int jr = 0; jr < NR; ++jr) {
+        const int v = (jr * kWarps + warp) * RPW + rw;
+        float4 s[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int e = v * DK + (sub + LPR * c) * 4;  // element offset in the tile
+          if (STATE_BF16) {
+            const uint2 u = *reinterpret_cast<const uint2*>(sb + (size_t)e * 2);
+            s[c] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+          } else {
+            s[c] = *reinterpret_cast<const float4*>(sb + (size_t)e * 4);
+          }
+        }
+        float a = 0.f;  // (S k)[v]
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          s[c].x *= eg; s[c].y *= eg; s[c].z *= eg; s[c].w *= eg;
+          a = fmaf(s[c].x, k4[c].x, a);
+          a = fmaf(s[c].y, k4[c].y, a);
+          a = fmaf(s[c].z, k4[c].z, a);
+          a = fmaf(s[c].w, k4[c].w, a);
+        }
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        const float u = beta * (T.v[v] - a);
+        float ov = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          s[c].x = fmaf(k4[c].x, u, s[c].x); s[c].y = fmaf(k4[c].y, u, s[c].y);
+          s[c].z = fmaf(k4[c].z, u, s[c].z); s[c].w = fmaf(k4[c].w, u, s[c].w);
+          ov = fmaf(s[c].x, q4[c].x, ov);
+          ov = fmaf(s[c].y, q4[c].y, ov);
+          ov = fmaf(s[c].z, q4[c].z, ov);
+          ov = fmaf(s[c].w, q4[c].w, ov);
+          const int e = v * DK + (sub + LPR * c) * 4;
+          if (STATE_BF16)
+            *reinterpret_cast<uint2*>(sb + (size_t)e * 2) =
+                make_uint2(pack_bf16x2(s[c].x, s[c].y), pack_bf16x2(s[c].z, s[c].w));
+          else
+            *reinterpret_cast<float4*>(sb + (size_t)e * 4) = s[c];
+        }
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) ov += __shfl_xor_sync(0xffffffffu, ov, o);
+        if (sub == 0) T.o[v] = ov;
+      }
+    }
+    stamp(j, 2);
+    // the next task's inputs, while this one finishes
+    issue_inputs(j + 1, j + 1 < n);
+    tc::fence_proxy_async_smem();  // this thread's tile writes before the bulk copy out
+    __syncthreads();  // S2: o, last and the updated tile complete
+    stamp(j, 3);
+    if (tid == 0) {
+      // the tile back to its slot (an empty group for a pad row), then task
+      // j + 2's tile into the buffer task j - 1's copy out has finished reading
+      if (live) tc::bulk_store(state_src(slot, h), sbuf(j), SL::kStateBytes);
+      tc::bulk_commit();
+      if (j >= 1 && j + 2 < n) {
+        tc::bulk_wait_read_1();
+        if (issue_state(j + 2)) pending |= 1u << ((j + 2) % SL::kBufs);
+      }
+    }
+    // the previous task's new q/k taps, if it was its group's last reader
+    if (T.last && tid < 2 * DK) {
+      __nv_bfloat16* cs = p.conv_state + ((size_t)prev_slot * p.C + prev_row) * 3;
+      cs[0] = __float2bfloat16_rn(nt0);
+      cs[1] = __float2bfloat16_rn(nt1);
+      cs[2] = __float2bfloat16_rn(nt2);
+    }
+    if (live) {
+      float rn = 0.f;
+      if (warp < DK / 32) {  // the warps that write core: each sums o^2 itself (same order)
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < DK / 32; ++i) q = fmaf(T.o[i * 32 + lane], T.o[i * 32 + lane], q);
+        q = warp_sum(q);
+        rn = 1.0f / sqrtf(q / (float)DK + p.gnorm_eps);
+      }
+      if (tid < DK) {
+        core[tid] = __float2bfloat16_rn(T.o[tid] * rn * gw * silu_f(T.z[tid]));
+      }
+    } else if (tid < DK) {
+      core[tid] = __float2bfloat16_rn(0.f);
+      if (slot >= p.num_slots && h == 0 && tid == 0) record_error(p.ctr, kStatusIndex, 0, w);
+    }
+    if ((p.debug_flags & kDebugTimeline) && j == 0 && tid == 0) p.ctr->tl_cta[cta][TL_REC_STATE] = globaltimer_ns();
+    prev_live = live;
+    prev_slot = slot;
+    prev_row = tid < 2 * DK ? proj_row(tid, h, kh) : 0;
+    nt0 = c1;
+    nt1 = c2;
+    nt2 = pvq;
+  }
+  if (ok) {
+    // the last task's new q/k taps
+    StagedTask& T = tb[n & 1];
+    if (tid == 0) T.last = prev_live && ((group_old + 1) % (unsigned)p.group) == 0;
+    __syncthreads();
+    if (T.last && tid < 2 * DK) {
+      __nv_bfloat16* cs = p.conv_state + ((size_t)prev_slot * p.C + prev_row) * 3;
+      cs[0] = __float2bfloat16_rn(nt0);
+      cs[1] = __float2bfloat16_rn(nt1);
+      cs[2] = __float2bfloat16_rn(nt2);
+    }
+  } else if (tid == 0) {
+    // let the copies in flight land before the ring is reused or the CTA ends (bounded)
+    for (int bb = 0; bb < SL::kBufs; ++bb) {
+      if (!((pending >> bb) & 1u)) continue;
+      const unsigned long long c0 = globaltimer_ns();
+      for (uint32_t it = 0; !tc::mbar_try_wait(&sbar[bb], (ph >> bb) & 1u); ++it)
+        if ((it & 63) == 0 && globaltimer_ns() - c0 > p.deadline_ns) break;
+    }
+  }
+  // the tiles' copies out complete (written to global memory, the ring free)
+  if (tid == 0) tc::bulk_wait_all();
+  // the buffers' generic accesses before any later copy into the ring
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  return ok;
+}
+
+}  // namespace gdn

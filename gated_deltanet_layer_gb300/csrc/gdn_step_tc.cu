@@ -42,6 +42,7 @@
 #include "gdn_kernels.h"
 #include "gdn_outproj.cuh"
 #include "gdn_phases.cuh"
+#include "gdn_recurrence_staged.cuh"
 #include "gdn_tc_ptx.cuh"
 
 namespace gdn {
@@ -85,8 +86,10 @@ struct TcShared {
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
   uint64_t obar[kOpMaxStages];  // out_proj: a stage's weight rows landed
+  uint64_t sbar[3];             // recurrence: a state tile landed (one per buffer)
   uint32_t tmem_base;
   int abort;
+  int dec_issued;  // coded formats: units [0, dec_issued) passed by the decode warps (bf16 tiles issued)
 };
 
 // Walks a CTA's units in plan order without divisions: unit u is k-step
@@ -302,7 +305,7 @@ static __device__ __forceinline__ void stage_residual_slices(const StepParams& p
 }
 
 // The input-norm weights of the window, one 16-byte chunk per thread (at
-// most 24 k-steps x 8 chunks < 512 threads). A weight no step writes: the
+// most 32 k-steps x 8 chunks <= 512 threads). A weight no step writes: the
 // load goes out before the previous step is done, the value is stored to
 // shared memory once the x and residual loads are out, off the norm path.
 static_assert(kMaxBSlots * 8 <= kThreads, "one norm-weight chunk per thread");
@@ -421,7 +424,11 @@ static __device__ __forceinline__ void finish_normed_slices(const StepParams& p,
 
 // TMA producer (one whole warp; lane 0 issues): units `issued`.. into the
 // rings, each into a stage that has been released (a bf16 stage by the MMAs,
-// a code stage by the decode). Returns the number of units issued. (An L2 prefetch ahead of the ring was
+// a code stage by the decode). With coded weights it issues the code tiles
+// only: the bf16 tiles of the other units (in_proj_ba) go out from the decode
+// warps, which wait for every phase of every bf16 stage in unit order. A
+// waiter that skipped some phases of a stage could take an older phase's
+// parity for the one it waits for. Returns the number of units passed. (An L2 prefetch ahead of the ring was
 // measured: the tensor form does not bring tiles in early, and per-row
 // prefetches delay the latency-bound norm hand-off more than they shorten
 // the projection.)
@@ -435,10 +442,10 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
     const bool coded = unit_coded<FMT>(p, it);
     if (coded) {
       if (!pipe_wait_warp(p, ts, &ts.rempty[pos.r], pos.rph ^ 1)) return n;
-    } else if (!pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) {
-      return n;
+    } else if (FMT == kFmtBf16) {
+      if (!pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1)) return n;
     }
-    if (leader) issue_unit<FMT>(p, ts, sW, sR, it, n, pos, pol);
+    if (leader && (coded || FMT == kFmtBf16)) issue_unit<FMT>(p, ts, sW, sR, it, n, pos, pol);
     __syncwarp();
     pos.advance(p, coded);
     it.next();
@@ -544,9 +551,10 @@ static __device__ __forceinline__ uint4 scale_block(const StepParams& p, const U
 }
 template <int FMT>
 static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                   const uint8_t* sR, int ub, int nunits, int ci) {
+                                                   const uint8_t* sR, int ub, int nunits, int prefill, int ci) {
   UnitIter it(p, ub);
   RingPos pos;
+  const uint64_t pol = tc::policy_evict_first();
   int blk_t = -1, blk_k = -1;  // the 8-k-step scale block held in `cur`
   uint4 cur = make_uint4(0, 0, 0, 0), nxt = make_uint4(0, 0, 0, 0);
   int nxt_t = -1, nxt_k = -1;
@@ -563,6 +571,16 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
   }
   for (int n = 0; n < nunits; ++n) {
     const bool coded = unit_coded<FMT>(p, it);
+    if (!coded) {
+      // a bf16 tile: once the stage's previous unit is multiplied, its load
+      // (the prefill has issued the first ones). A stage's first use has no
+      // wait: the MMA may already have taken a prefilled tile.
+      if (n >= p.stages && !bar_and(pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1))) return;
+      if (ci == 0) {
+        if (n >= prefill) issue_unit<FMT>(p, ts, sW, nullptr, it, n, pos, pol);
+        *reinterpret_cast<volatile int*>(&ts.dec_issued) = n + 1;
+      }
+    }
     if (coded) {
       if (it.t != blk_t || (it.ks >> 3) != blk_k) {
         // this unit starts a new scale block: take the prefetched one, prefetch the next
@@ -738,21 +756,28 @@ static __device__ void land_prefill(const StepParams& p, TcShared& ts, int ub, i
   }
 }
 // On an aborted projection: wait (bounded) for the last TMA load issued into
-// each stage of either ring (units [0, issued)).
+// each stage of either ring: the producer's units [0, issued) (with coded
+// weights its code tiles and the prefill's bf16 tiles), and with coded
+// weights the bf16 tiles of units [0, dec_issued) from the decode warps.
 template <int FMT>
-static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, int issued) {
+static __device__ void land_issued(const StepParams& p, TcShared& ts, int ub, int issued, int prefill,
+                                   int dec_issued) {
+  const int bf16_end = FMT == kFmtBf16 ? issued : max(prefill, dec_issued);
+  const int end = max(issued, bf16_end);
   int last_s[kMaxStages], last_r[kMaxRStages];
   uint32_t ph_s[kMaxStages], ph_r[kMaxRStages];
   for (int i = 0; i < kMaxStages; ++i) last_s[i] = -1;
   for (int i = 0; i < kMaxRStages; ++i) last_r[i] = -1;
   RingPos pos;
   UnitIter it(p, ub);
-  for (int j = 0; j < issued; ++j, it.next()) {
+  for (int j = 0; j < end; ++j, it.next()) {
     const bool coded = unit_coded<FMT>(p, it);
     if (coded) {
-      last_r[pos.r] = j;
-      ph_r[pos.r] = pos.rph;
-    } else {
+      if (j < issued) {
+        last_r[pos.r] = j;
+        ph_r[pos.r] = pos.rph;
+      }
+    } else if (j < bf16_end) {
       last_s[pos.s] = j;
       ph_s[pos.s] = pos.ph;
     }
@@ -791,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     tc::prefetch_tensormap(&p.tm_ba);
     if (p.out) tc::prefetch_tensormap(&p.tm_out);
     ts.abort = 0;
+    ts.dec_issued = 0;
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
       tc::mbar_init(&ts.empty[s], 1);
@@ -805,6 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     }
     tc::mbar_init(&ts.mma_done, 1);
     for (int s = 0; s < kOpMaxStages; ++s) tc::mbar_init(&ts.obar[s], 1);
+    for (int s = 0; s < 3; ++s) tc::mbar_init(&ts.sbar[s], 1);
     tc::fence_mbar_init();
   }
   __syncthreads();
@@ -866,7 +893,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   StateRegs<DK> first_state;
   int rt0, rt1;
   task_range(p, rt0, rt1);
-  if (rt0 < rt1) load_state<DK, STATE_BF16>(p, rt0, first_state);
+  // two or more decode tasks: the staged recurrence, in the shared memory
+  // the projection leaves
+  const bool staged = !MULTI && rt1 - rt0 >= 2 && p.dyn_free >= staged_recurrence_bytes<DK, STATE_BF16>();
+  if (rt0 < rt1 && !staged) load_state<DK, STATE_BF16>(p, rt0, first_state);
+  if (staged && tid == 0) prefetch_state_l2<DK, STATE_BF16>(p, rt0);  // its bulk copy reads L2
   int issued_total = issued;
   if (nunits > 0) {
     if (warp == 0)
@@ -876,12 +907,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     else if (warp == 4 || warp == 8 || warp == 12)
       drain_loop(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
     else if (FMT != kFmtBf16 && conv_index(warp) >= 0)
-      decode_loop<FMT>(p, ts, sW, sR, ub, nunits, conv_index(warp) * 32 + (tid & 31));
+      decode_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, conv_index(warp) * 32 + (tid & 31));
   }
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
-  if (aborted && tid == 0) land_issued<FMT>(p, ts, ub, issued_total);  // TMA in flight lands before exit
+  if (aborted && tid == 0)  // TMA in flight lands before exit
+    land_issued<FMT>(p, ts, ub, issued_total, issued, *reinterpret_cast<volatile int*>(&ts.dec_issued));
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -893,7 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const size_t ring_bytes = (size_t)p.stages * kWBytes + (size_t)p.rstages * code_tile_bytes<FMT>();
   if (!aborted && p.out && warp == 0 && rt0 >= rt1) out_proj_prefetch(p, sW, ring_bytes, ts.obar);
   if (!aborted) {
-    const bool rec_ok = phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
+    const bool rec_ok = staged ? phase_recurrence_staged<DK, STATE_BF16>(p, sW, ts.sbar, L, rt0, rt1)
+                               : phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
     // out_proj over the core rows of every CTA, in the freed weight ring
     if (p.out) {
       if (rec_ok) {

@@ -43,10 +43,12 @@ def test_bf16_state_matches_f32_kernel_on_widened_state(rows):
     assert torch.equal(_bits(case16.dssm), _bits(case32.dssm.to(torch.bfloat16)))
 
 
-def test_batch_invariance():
+@pytest.mark.parametrize("shape", [WL.SHARD, WL.FULL], ids=["shard", "full"])
+def test_batch_invariance(shape):
     """A probe row's outputs (core, residual_out, its state slot) do not change
-    with the other rows, its position or the width."""
-    shape = WL.SHARD
+    with the other rows, its position or the width. On the full layer the
+    wider steps give a CTA several (row, value head) tasks, so the pipelined
+    recurrence and the one-task path must agree bit for bit."""
     base = Case(shape, 16, 6100)
     probe_x = base.step["x"][0].clone()
     probe_r = base.step["residual"][0].clone()
