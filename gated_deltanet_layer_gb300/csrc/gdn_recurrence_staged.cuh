@@ -36,12 +36,16 @@ struct StagedTask {
   float ba[2];               // b, a (bf16 projections)
   int last;                  // the previous task was its key-head group's last reader
 };
+// The state slots of the launch's rows (read once per phase).
+struct StagedSlots {
+  int idx[kMaxRows];
+};
 
 template <int DK, bool STATE_BF16>
 struct StagedLayout {
   static constexpr uint32_t kStateBytes = DK * DK * (STATE_BF16 ? 2 : 4);
   static constexpr int kBufs = 3;
-  static constexpr size_t kBytes = kBufs * (size_t)kStateBytes + 2 * sizeof(StagedTask);
+  static constexpr size_t kBytes = kBufs * (size_t)kStateBytes + 2 * sizeof(StagedTask) + sizeof(StagedSlots);
   static_assert(kStateBytes % 16 == 0, "bulk copy size");
 };
 
@@ -96,6 +100,9 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   const int n = t1 - t0;
   auto sbuf = [&](int j) { return ring + (size_t)(j % SL::kBufs) * SL::kStateBytes; };  // task j's tile
   StagedTask* tb = reinterpret_cast<StagedTask*>(ring + SL::kBufs * (size_t)SL::kStateBytes);
+  int* sidx = reinterpret_cast<StagedSlots*>(tb + 2)->idx;  // the rows' state slots
+  if (tid < p.rows) sidx[tid] = p.idx[tid];
+  __syncthreads();
   const bool ba_warp = warp >= kWarps - 2;
 
   auto proj_row = [&](int i, int h, int kh) -> int {
@@ -120,19 +127,27 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   // (not for a pad row).
   auto issue_state = [&](int j) -> bool {
     const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv;
-    const int slot = p.idx[w];
+    const int slot = sidx[w];
     if (!row_is_live(p, slot)) return false;
     uint64_t* bar = &sbar[j % SL::kBufs];
     tc::mbar_arrive_expect_tx(bar, SL::kStateBytes);
     tc::bulk_load(sbuf(j), state_src(slot, h), SL::kStateBytes, bar);
     return true;
   };
+  // Task j reads the same q/k channels (row and key head) as task j - 1:
+  // their conv + SiLU outputs are the previous task's, copied, not reloaded.
+  auto same_qk = [&](int j) {
+    if (j == 0) return false;
+    const int a = t0 + j - 1, b = t0 + j;
+    const int wa = a / p.Hv, wb = b / p.Hv;
+    return wa == wb && (a - wa * p.Hv) / p.group == (b - wb * p.Hv) / p.group;
+  };
   // Every thread: issue its loads of task j's inputs (nothing for a pad row,
   // or when `real` is false: then the fields are only cleared).
   StagedLoads ld;
   auto issue_inputs = [&](int j, bool real) {
     const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
-    const int slot = real ? p.idx[w] : 0;
+    const int slot = real ? sidx[w] : 0;
     // every field is assigned on every path (and the call made after every
     // task), so nothing of a task's loads stays live past its use
     ld.nc = 0;
@@ -153,7 +168,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
       ld.ba_src = part_src(proj_row(4 * DK + (warp - (kWarps - 2)), h, kh), w, ld.ba_nc) + (size_t)lane * kSlot;
       if (lane < ld.ba_nc) ld.baw[0] = ld_tagged(ld.ba_src);
     }
-    if (tid < 4 * DK) {
+    if (tid < 4 * DK && !(tid < 2 * DK && same_qk(j))) {
       const int nr = proj_row(tid, h, kh);
       ld.src = part_src(nr, w, ld.nc);
 #pragma unroll
@@ -190,7 +205,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   float nt0 = 0.f, nt1 = 0.f, nt2 = 0.f;  // the previous task's new q/k taps of this thread's channel
   for (int j = 0; j < n; ++j) {
     const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
-    const int slot = p.idx[w];
+    const int slot = sidx[w];
     const bool live = row_is_live(p, slot);
     StagedTask& T = tb[j & 1];
     __nv_bfloat16* core = p.core_out + (size_t)w * p.Hv * DK + (size_t)h * DK;
@@ -198,7 +213,20 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     float c1 = 0.f, c2 = 0.f, pvq = 0.f;  // this task's new taps (threads < 2 dk)
     if (live) {
       // ---- inputs: partial sums, conv update + SiLU, per-warp sums of squares
-      if (tid < 4 * DK) {
+      if (tid < 2 * DK && same_qk(j)) {
+        // q/k as the previous task had them (same values, so the same sums)
+        const StagedTask& P = tb[(j - 1) & 1];
+        const float y = tid < DK ? P.q[tid] : P.k[tid - DK];
+        if (tid < DK)
+          T.q[tid] = y;
+        else
+          T.k[tid - DK] = y;
+        c1 = nt0;
+        c2 = nt1;
+        pvq = nt2;
+        const float y2 = warp_sum(y * y);
+        if (lane == 0) T.red[warp] = y2;
+      } else if (tid < 4 * DK) {
         const int i = tid;
         if (!poll_tagged<kMaxSlots>(p, ld.pw, ld.src, kSlot, ld.nc, L, kWaitTile)) ok = false;
         if (i == 0 && (p.debug_flags & kDebugTimeline) && j == 0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
