@@ -14,6 +14,7 @@ struct SmemPhases {
   alignas(16) float part8[kMaxRows * (kMaxNormChunk / 8)];  // sums of 8 squares
   alignas(16) float rstd[kMaxRows];
   alignas(16) float red[kWarps];
+  unsigned char tiles[kMaxTiles];  // partials per projection tile (tensor-core engine: the plan's, staged)
   int L;                 // launch number on this workspace
   int flag;              // CTA-wide decision (set by thread 0, cleared by any thread that gives up)
 };
@@ -236,6 +237,8 @@ __device__ __forceinline__ void load_state(const StepParams& p, int task, StateR
 
 // `raw` holds the first task's state when `have_first` (loaded early, so
 // that its latency hides under the projection); later tasks load into it.
+// tile_cnt[t]: the partials of projection tile t (the plan's table, or its
+// copy in shared memory).
 // sm.flag is 1 on entry (every earlier phase of the launch succeeded); a
 // thread whose wait runs out clears it.
 // MULTI (verify steps): a task is (sequence, value head) and runs the
@@ -247,7 +250,8 @@ __device__ __forceinline__ void load_state(const StepParams& p, int task, StateR
 // first value head's task (no counter: the input slot is never written).
 template <int DK, bool STATE_BF16, bool MULTI = false>
 __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases& sm, SmemTask& st, int L,
-                                                 StateRegs<DK>& raw, bool have_first) {
+                                                 StateRegs<DK>& raw, bool have_first,
+                                                 const unsigned char* tile_cnt) {
   constexpr int LPR = StateRegs<DK>::LPR;
   constexpr int RPW = StateRegs<DK>::RPW;
   constexpr int NR = StateRegs<DK>::NR;
@@ -310,7 +314,7 @@ __device__ __forceinline__ bool phase_recurrence(const StepParams& p, SmemPhases
     auto part_src = [&](int n, int& nc) {
       const int t = tile_of(n);
       const int r = (n < p.Nqkvz ? n : n - p.Nqkvz) & (kTileM - 1);
-      nc = p.plan->tile_num_ctas[t];
+      nc = tile_cnt[t];
       return p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
     };
     const bool ba_warp = warp >= kWarps - 2;

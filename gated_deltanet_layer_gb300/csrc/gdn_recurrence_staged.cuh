@@ -85,7 +85,7 @@ __device__ __forceinline__ void prefetch_state_l2(const StepParams& p, int task)
 
 template <int DK, bool STATE_BF16>
 __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint64_t* sbar, int L, int t0,
-                                        int t1) {
+                                        int t1, const unsigned char* tile_cnt) {
   using SL = StagedLayout<DK, STATE_BF16>;
   constexpr int LPR = StateRegs<DK>::LPR;
   constexpr int RPW = StateRegs<DK>::RPW;
@@ -115,7 +115,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   auto part_src = [&](int n_row, int w, int& nc) {
     const int t = n_row < p.Nqkvz ? (n_row >> kTileShift) : p.tiles_qkvz + ((n_row - p.Nqkvz) >> kTileShift);
     const int r = (n_row < p.Nqkvz ? n_row : n_row - p.Nqkvz) & (kTileM - 1);
-    nc = p.plan->tile_num_ctas[t];
+    nc = tile_cnt[t];
     return p.proj_part + ((size_t)t * p.max_contrib * kMaxRows + w) * kTileM + r;
   };
 

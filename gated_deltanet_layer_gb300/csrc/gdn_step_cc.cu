@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_cc_kernel(const __grid_c
   if (!phase_normed_input(p, sm, L)) return;
   if (!phase_proj_cuda_core(p, sm, ds.xs, L)) return;
   StateRegs<DK> none;
-  phase_recurrence<DK, STATE_BF16>(p, sm, st, L, none, false);
+  phase_recurrence<DK, STATE_BF16>(p, sm, st, L, none, false, p.plan->tile_num_ctas);
   tl_stamp(p, TL_END);
 }
 

@@ -847,6 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const int first = min(issued, kFirstTiles);
   if (tid == 32) start_weight_stream<FMT>(p, ts, sW, sR, ub, 0, first);
   const uint4 wnorm = load_norm_weights(p);  // also warms this SM's cache lines of the plan
+  // the partials per tile, for the recurrence's loads (kept in shared memory:
+  // the L1 left beside this kernel's shared memory does not keep the plan)
+  static_assert(kMaxTiles <= kThreads, "one tile count per thread");
+  const unsigned tile_cnt = tid < p.num_tiles ? p.plan->tile_num_ctas[tid] : 0u;
   griddep_wait();  // from here on the previous kernel's writes are visible (a no-op if already waited)
   griddep_launch_dependents();
   if (tid == 0) {
@@ -909,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     else if (FMT != kFmtBf16 && conv_index(warp) >= 0)
       decode_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, conv_index(warp) * 32 + (tid & 31));
   }
+  if (tid < p.num_tiles) sm.tiles[tid] = (unsigned char)tile_cnt;
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
@@ -925,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   const size_t ring_bytes = (size_t)p.stages * kWBytes + (size_t)p.rstages * code_tile_bytes<FMT>();
   if (!aborted && p.out && warp == 0 && rt0 >= rt1) out_proj_prefetch(p, sW, ring_bytes, ts.obar);
   if (!aborted) {
-    const bool rec_ok = staged ? phase_recurrence_staged<DK, STATE_BF16>(p, sW, ts.sbar, L, rt0, rt1)
-                               : phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1);
+    const bool rec_ok = staged ? phase_recurrence_staged<DK, STATE_BF16>(p, sW, ts.sbar, L, rt0, rt1, sm.tiles)
+                               : phase_recurrence<DK, STATE_BF16, MULTI>(p, sm, st, L, first_state, rt0 < rt1, sm.tiles);
     // out_proj over the core rows of every CTA, in the freed weight ring
     if (p.out) {
       if (rec_ok) {
