@@ -110,9 +110,10 @@ gdn_status validate(const gdn_decode_config* c) {
 // (k-block kb = g / T, tile t = g % T) holds the `kblock` k-steps kb*kblock ..
 // of tile t. With kblock = ksteps the order is tile-major (a CTA sweeps K of
 // one tile, then the next); the tensor-core engine of a large layer uses
-// kblock = 16 (8 with MXFP4 weights, whose two windows halve the room), so a
-// CTA's units touch at most two k-blocks and the normed input it needs (<= 32
-// k-steps; 24 with MXFP4) fits in shared memory. Longer k-blocks also mean
+// kblock = 16 (8 with MXFP4 or MXFP6 weights, whose second window or code
+// ring takes the room), so a CTA's units touch at most two k-blocks and the
+// normed input it needs (<= 32 k-steps; 24 with coded weights) fits in shared
+// memory. Longer k-blocks also mean
 // fewer partials per tile for the recurrence to add. Every unit counts the
 // same, also one of the partial in_proj_ba tile: a unit's time is set by its
 // fixed per-unit cost, not by its row count. CTA c takes units
@@ -134,11 +135,13 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
   const long long per_cta = (U + G - 1) / G;
   // the normed-input window of the tensor-core engine, in k-steps, and the
   // k-block that keeps a CTA's units inside it
-  const bool mx4 = c.qkvz_format == GDN_W_MXFP4;
-  const int max_window = mx4 ? kMaxBSlotsMxfp4 : kMaxBSlots;
+  // coded weights (MXFP4: two windows; MXFP6: the code ring) keep the ring
+  // deeper with the shorter k-block
+  const bool coded = c.qkvz_format != GDN_W_BF16;
+  const int max_window = coded ? kMaxBSlotsMxfp4 : kMaxBSlots;
   int KB = KS;
   if (engine == GDN_ENGINE_TCGEN05 && per_cta + 1 > max_window) {
-    KB = mx4 ? kKBlockMxfp4 : kKBlock;
+    KB = coded ? kKBlockMxfp4 : kKBlock;
     if (KS % KB != 0) return GDN_ERR_UNSUPPORTED;
   }
   pl->kblock = KB;

@@ -20,9 +20,9 @@ constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
 constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
 constexpr int kMaxSegs = 16;               // tile segments in one CTA's unit range
 constexpr int kKBlock = 16;                // k-steps per k-block in the k-block-major order
-constexpr int kKBlockMxfp4 = 8;            // the same with MXFP4 weights (two windows: xn and its quantised copy)
+constexpr int kKBlockMxfp4 = 8;            // the same with coded (MXFP4, MXFP6) weights
 constexpr int kMaxBSlots = 32;             // normed-input k-steps a CTA keeps in shared memory
-constexpr int kMaxBSlotsMxfp4 = 24;        // the same with MXFP4 weights
+constexpr int kMaxBSlotsMxfp4 = 24;        // the same with coded weights
 constexpr int kMaxKHeads = 64;             // key heads of a layer (conv-group counters)
 
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.

@@ -124,17 +124,18 @@ def test_product_path_never_imports_the_oracle():
 
 
 @pytest.mark.parametrize("engine", ["cuda_core", "auto"])
-@pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16])
-@pytest.mark.parametrize("G", [1, 7, 33, 148, 152, 160])
+@pytest.mark.parametrize("shape,G", [(s, g) for s in (WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16)
+                                     for g in (1, 7, 33, 148, 152, 160)] +
+                         [(s, g) for s in (WL.DENSE_MXFP4, WL.DENSE_MXFP6) for g in (148, 152, 160)])
 def test_stream_k_plan_invariants(lib, shape, G, engine):
     """The units partition [0, U) in CTA order with equal counts (within one);
     walking each CTA's units the way the kernels do (group g = u // kblock,
     tile g % T, k-step (g // T) * kblock + u % kblock) gives per tile the
     slots 0..count-1 exactly once; with the tensor-core engine every unit's
     normed-input slot lies inside the CTA's window of at most 32 k-steps (24
-    with MXFP4 weights)."""
+    with coded weights)."""
     cfg = make_config(shape, engine=engine)
-    if (shape.hidden + G - 1) // G > 256:
+    if (shape.hidden + G - 1) // G > 256 or (engine == "cuda_core" and shape.qkvz_format != "bf16"):
         with pytest.raises(_native.GdnError):
             _native.plan(cfg, G)
         return
@@ -158,7 +159,7 @@ def test_stream_k_plan_invariants(lib, shape, G, engine):
                 g_prev = g
             if P["engine"] == 2:
                 j = (ks - P["ks_first"][c]) % KS
-                assert j < P["nb_slots"][c] <= (24 if cfg.qkvz_format == _native.GDN_W_MXFP4 else 32)
+                assert j < P["nb_slots"][c] <= (24 if cfg.qkvz_format != _native.GDN_W_BF16 else 32)
     for t in range(nt):
         assert P["tile_count"][t] == len(slots[t]) >= 1
         assert sorted(slots[t]) == list(range(P["tile_count"][t]))
