@@ -466,9 +466,18 @@ def native(args):
         e1.record(st0)
         torch.cuda.synchronize()
         rig.check()
+        # host cost of one call through the binding (argument marshalling, the
+        # C entry point and the launch enqueue; the GPU runs behind)
+        h0 = time.perf_counter()
+        for k in range(K):
+            rig.layer.step(dx, dr, rig.copies[k % rig.ncopy], di, rig.conv, rig.ssm, dc, do,
+                           weights_struct=rig.wstructs[k % rig.ncopy])
+        host_us = (time.perf_counter() - h0) * 1e6 / K
+        torch.cuda.synchronize()
+        rig.check()
         e2e = {"value": round(e0.elapsed_time(e1) * 1e3 / K, 3), "unit": "µs/launch", "h2d_bytes_per_step": Bi,
-               "d2h_bytes_per_step": Bo, "how": "eager gdn_decode_step via the Python binding with "
-                                                "pinned-host copies in and out each step"}
+               "d2h_bytes_per_step": Bo, "host_us_per_call": round(host_us, 2),
+               "how": "eager gdn_decode_step via the Python binding with pinned-host copies in and out each step"}
     n_ctas, engine = rig.layer.launch_info(args.rows)
     ncopy, wbytes = rig.ncopy, rig.wbytes
 
