@@ -73,10 +73,12 @@ def _two_steps_each(shape, rows, seed, **kw):
     # nothing went through torch's allocator on either call
     assert torch.cuda.memory_reserved() == reserved0
     # the second call found its set-up done: no device memory changed hands.
+    # The device-wide free count is only a bound (another process could move
+    # it): an allocation by the call would take at least one 2 MiB granule.
     # The first call may load the library's module that holds the scratch
     # array (lazy module loading), which the driver does, not the call: a
     # loose bound of the array's size plus a few MiB of code and tables.
-    assert torch.cuda.mem_get_info()[0] == free_second
+    assert abs(torch.cuda.mem_get_info()[0] - free_second) < (2 << 20)
     assert free_before - free_second <= _native.GDN_STATIC_SCRATCH_BYTES + (16 << 20)
 
     for (ca, ra), (cb, rb) in zip(ref, got):
