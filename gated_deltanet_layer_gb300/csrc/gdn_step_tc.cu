@@ -65,13 +65,25 @@ template <int FMT>
 __host__ __device__ constexpr uint32_t code_tile_bytes() { return kTileM * code_row_bytes<FMT>(); }
 constexpr int kMaxRStages = 4;                          // code tiles in flight per CTA (MXFP4, MXFP6)
 // Warps that decode MXFP4 / MXFP6 code tiles into bf16 tiles: thread i of them owns
-// row i of the 256-row tile. (Warp 0 holds the TMA producer, warp 1 the MMA
-// issuer, warps 4, 8 and 12 the drain.)
+// row i of the 256-row tile. Warp 0 holds the TMA producer, warp 1 the MMA
+// issuer, warp 4 the drain (with bf16 weights, which have no decode, warps 4,
+// 8 and 12). The decode is bound by the integer pipe of its warps' schedulers
+// (warp w issues on scheduler w % 4), so its eight warps are two per scheduler:
+// 8, 12 | 5, 9 | 2, 6 | 3, 7.
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
 __device__ __forceinline__ int conv_index(int warp) {
-  // warps 2, 3, 5, 6, 7, 9, 10, 11 -> 0..7
-  return warp == 2 ? 0 : warp == 3 ? 1 : (warp >= 5 && warp <= 7) ? warp - 3 : (warp >= 9 && warp <= 11) ? warp - 4 : -1;
+  switch (warp) {
+    case 8: return 0;
+    case 12: return 1;
+    case 5: return 2;
+    case 9: return 3;
+    case 2: return 4;
+    case 6: return 5;
+    case 3: return 6;
+    case 7: return 7;
+    default: return -1;
+  }
 }
 constexpr uint32_t kWaitPipe = 4;                       // error-word id of a pipeline wait
 constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on the abort path
@@ -485,16 +497,22 @@ static __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 // 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0: their high and low bytes are two
 // 8-entry byte tables, looked up four codes at a time with PRMT (the code's
 // low 3 bits select a byte); the sign bits are shifted into bit 15 / 31.
+// The signs: code 2j's sign bit is the top bit of byte j of (w << 4), code
+// 2j + 1's the top bit of byte j of w; a PRMT selector nibble with bit 3 set
+// replicates the top bit of the byte it selects, which puts them at bits 15
+// and 31 (masked in with one logic op).
 static __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&o)[4]) {
   constexpr uint32_t kHiLo = 0x3F3F3F00u, kHiHi = 0x40404040u;  // high bytes of magnitudes 0..3, 4..7
   constexpr uint32_t kLoLo = 0xC0800000u, kLoHi = 0xC0804000u;  // low bytes
   const uint32_t m = w & 0x77777777u, m2 = m >> 16;
   const uint32_t h0 = prmt(kHiLo, kHiHi, m), l0 = prmt(kLoLo, kLoHi, m);
   const uint32_t h1 = prmt(kHiLo, kHiHi, m2), l1 = prmt(kLoLo, kLoHi, m2);
-  o[0] = prmt(l0, h0, 0x5140u) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-  o[1] = prmt(l0, h0, 0x7362u) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
-  o[2] = prmt(l1, h1, 0x5140u) | ((w >> 4) & 0x8000u) | ((w << 8) & 0x80000000u);
-  o[3] = prmt(l1, h1, 0x7362u) | ((w >> 12) & 0x8000u) | (w & 0x80000000u);
+  const uint32_t ev = w << 4;  // even codes' signs at the bytes' top bits (odd codes': w itself)
+  constexpr uint32_t kSignMask = 0x80008000u;
+  o[0] = prmt(l0, h0, 0x5140u) | (prmt(ev, w, 0xC080u) & kSignMask);
+  o[1] = prmt(l0, h0, 0x7362u) | (prmt(ev, w, 0xD090u) & kSignMask);
+  o[2] = prmt(l1, h1, 0x5140u) | (prmt(ev, w, 0xE0A0u) & kSignMask);
+  o[3] = prmt(l1, h1, 0x7362u) | (prmt(ev, w, 0xF0B0u) & kSignMask);
 }
 // Two e2m3 codes (6 bits: sign bit 5, exponent bits 4..3 with bias 1,
 // mantissa bits 2..0) to a bf16x2 word, c0 in the low half. With exponent
@@ -700,14 +718,15 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   if (leader) tl_stamp_here(p, TL_MMA_LAST);
 }
 
-// Drain (warps 4, 8 and 12, all in TMEM sub-partition 0, so lane w reads row
-// w of the step): per segment, the warps split the accumulator's 8 chunks of
-// 32 columns (weight rows) and write the CTA's partial of the tile as tagged
-// words; then the accumulator is released.
-constexpr int kDrainWarps = 3;
-constexpr int kDrainThreads = 32 * kDrainWarps;
+// Drain (warp 4 with coded weights, warps 4, 8 and 12 with bf16 weights; all
+// in TMEM sub-partition 0, so lane w reads row w of the step): per segment,
+// the warps split the accumulator's 8 chunks of 32 columns (weight rows) and
+// write the CTA's partial of the tile as tagged words; then the accumulator
+// is released.
+template <int kDrainWarps>
 static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared& ts, int ub, int nunits,
                                                   uint32_t tmem, int gtid, int L) {
+  constexpr int kDrainThreads = 32 * kDrainWarps;
   const int W = p.rows, lane = gtid & 31, dw = gtid >> 5;
   UnitIter it(p, ub);
   int seg = 0;
@@ -908,8 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
       issued_total = producer_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, tc::policy_evict_first());
     else if (warp == 1)
       mma_loop<FMT>(p, ts, sW, sX, sXq, ub, nunits, tmem);
-    else if (warp == 4 || warp == 8 || warp == 12)
-      drain_loop(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
+    else if (warp == 4 || (FMT == kFmtBf16 && (warp == 8 || warp == 12)))
+      drain_loop<FMT == kFmtBf16 ? 3 : 1>(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
     else if (FMT != kFmtBf16 && conv_index(warp) >= 0)
       decode_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, conv_index(warp) * 32 + (tid & 31));
   }
