@@ -90,10 +90,11 @@ constexpr unsigned long long kCleanupNs = 100000000ull; // bound of the waits on
 }  // namespace
 
 struct TcShared {
-  uint64_t full[kMaxStages];   // bf16 weight tile ready (TMA complete_tx, or the code tile's decode done)
+  uint64_t full[kMaxStages];   // bf16 weight tile landed (TMA complete_tx)
+  uint64_t dfull[kMaxStages];  // coded weights: the stage's code tile decoded (one arrival per decode warp)
   uint64_t empty[kMaxStages];  // MMAs of the stage done (tcgen05.commit)
   uint64_t rfull[kMaxRStages];   // code tile landed (TMA complete_tx)
-  uint64_t rempty[kMaxRStages];  // code tile decoded
+  uint64_t rempty[kMaxRStages];  // code tile read by every decode warp
   uint64_t acc_full[2];     // accumulator ready for the drain
   uint64_t acc_empty[2];    // accumulator drained
   uint64_t mma_done;        // every MMA issued by the CTA done
@@ -466,12 +467,13 @@ static __device__ __forceinline__ int producer_loop(const StepParams& p, TcShare
 }
 
 // Code decode (kConvThreads threads, thread i owns row i of the tile): per
-// coded unit, wait for its code tile and for its bf16 stage to be free, turn
-// each row's 64 codes (MXFP4 e2m1 or MXFP6 e2m3) and their two e8m0 block
-// scales into bf16 (code value x 2^(scale - 127), exact in bf16) in the
-// 128-byte swizzled K-major layout the MMA reads, then release the code
-// stage and hand the bf16 stage to the MMA. A row's scales for 8 k-steps are
-// one aligned 16-byte load, issued a block ahead.
+// coded unit, each warp on its own waits for the code tile and for its bf16
+// stage to be free, turns its rows' 64 codes (MXFP4 e2m1 or MXFP6 e2m3) and
+// their two e8m0 block scales into bf16 (code value x 2^(scale - 127), exact
+// in bf16) in the 128-byte swizzled K-major layout the MMA reads, then
+// arrives on the code stage's release and on the stage's `dfull` (both count
+// one arrival per warp): no barrier among the warps per unit. A row's scales
+// for 8 k-steps are one aligned 16-byte load, issued a block ahead.
 // 2^(e - 127) of an e8m0 byte as bf16x2 (both halves): bf16 exponent field
 // e; e = 0 is 2^-127, the bf16 subnormal 0x0040.
 static __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
@@ -552,17 +554,7 @@ static __device__ __forceinline__ void decode_row_mxfp6(const uint8_t* src, cons
   }
 }
 
-// All-threads-of-a-named-barrier AND of a predicate (every thread gets it).
-static __device__ __forceinline__ bool bar_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "barrier.red.and.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "n"(kConvThreads)
-      : "memory");
-  return r != 0;
-}
+// One row's e8m0 scales of the 8-k-step block of unit `it` (16 bytes).
 static __device__ __forceinline__ uint4 scale_block(const StepParams& p, const UnitIter& it, int row) {
   const int grow = (it.t * kTileM) + row;  // coded units are in_proj_qkvz rows
   return ld_stream_v4(p.w_qkvz_scales + (size_t)grow * (p.H / 32) + (it.ks >> 3) * 16);
@@ -587,19 +579,30 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
         break;
       }
   }
+  // A warp whose wait ran out (the abort flag is then set, and every later
+  // wait returns at once) goes on walking the units without work, so that it
+  // still meets the other decode warps at every barrier below.
+  bool live = true;
   for (int n = 0; n < nunits; ++n) {
     const bool coded = unit_coded<FMT>(p, it);
     if (!coded) {
-      // a bf16 tile: once the stage's previous unit is multiplied, its load
-      // (the prefill has issued the first ones). A stage's first use has no
-      // wait: the MMA may already have taken a prefilled tile.
-      if (n >= p.stages && !bar_and(pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1))) return;
-      if (ci == 0) {
+      // a bf16 tile (the prefill has issued the first ones). A stage's first
+      // use has no wait: the MMA may already have taken a prefilled tile.
+      // Later, every decode warp waits for the stage's release and the tile
+      // goes out only once all of them have: were it to need one warp alone,
+      // it could be multiplied and the stage released again before a slower
+      // warp had waited for the release before (that warp would then wait
+      // for a phase two generations on).
+      if (n >= p.stages) {
+        live = live && pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1);
+        asm volatile("barrier.sync 2, %0;" ::"n"(kConvThreads) : "memory");
+      }
+      if (live && ci == 0) {
         if (n >= prefill) issue_unit<FMT>(p, ts, sW, nullptr, it, n, pos, pol);
         *reinterpret_cast<volatile int*>(&ts.dec_issued) = n + 1;
       }
     }
-    if (coded) {
+    if (coded && live) {
       if (it.t != blk_t || (it.ks >> 3) != blk_k) {
         // this unit starts a new scale block: take the prefetched one, prefetch the next
         cur = nxt;
@@ -616,9 +619,11 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
           }
         }
       }
-      bool ok = pipe_wait(p, ts, &ts.rfull[pos.r], pos.rph);
-      ok = ok && pipe_wait(p, ts, &ts.empty[pos.s], pos.ph ^ 1);
-      if (!bar_and(ok)) return;  // the same decision in every decoding thread (bounded waits)
+      // each warp on its own: it waits for every phase in order, and every
+      // barrier it waits on needs all eight decode warps to advance
+      live = pipe_wait_warp(p, ts, &ts.rfull[pos.r], pos.rph) && pipe_wait_warp(p, ts, &ts.empty[pos.s], pos.ph ^ 1);
+    }
+    if (coded && live) {
       const uint8_t* row = sR + (size_t)pos.r * code_tile_bytes<FMT>() + ci * code_row_bytes<FMT>();
       const int kk = it.ks & 7;  // k-step within the block: scale bytes 2kk, 2kk + 1
       const uint32_t sw4 = (kk >> 1) == 0 ? cur.x : (kk >> 1) == 1 ? cur.y : (kk >> 1) == 2 ? cur.z : cur.w;
@@ -641,10 +646,10 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
         }
       }
       tc::fence_proxy_async_smem();  // the generic-proxy writes, visible to the MMA
-      asm volatile("barrier.sync 2, %0;" ::"n"(kConvThreads) : "memory");
-      if (ci == 0) {
+      __syncwarp();
+      if ((ci & 31) == 0) {  // this warp's rows: code read, bf16 written
         tc::mbar_arrive(&ts.rempty[pos.r]);
-        tc::mbar_arrive(&ts.full[pos.s]);
+        tc::mbar_arrive(&ts.dfull[pos.s]);
       }
     }
     pos.advance(p, coded);
@@ -666,7 +671,10 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
   int seg = -1;
   bool seg_open = false;
   int s = 0;
-  uint32_t ph = 0;
+  // per stage, the phase parity of its two fill barriers: `full` (a TMA fill)
+  // and, with coded weights, `dfull` (a decoded tile); each is waited for at
+  // every one of its phases, in order
+  uint32_t phu = 0, phc = 0;
   const uint32_t sw0 = tc::smem_u32(sW), sx0 = tc::smem_u32(sX), sxq0 = tc::smem_u32(sXq);
   const bool leader = (threadIdx.x & 31) == 0;
   bool landed = false;  // unit n's tile seen complete while unit n - 1 was issued
@@ -678,18 +686,24 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
       if (!pipe_wait_warp(p, ts, &ts.acc_empty[seg & 1], ((seg >> 1) & 1) ^ 1)) break;
       tc::tc_fence_after();  // these MMAs come after the drain's tcgen05.ld of this accumulator
     }
-    // The phase makes the stage's TMA bytes visible to the MMA (both async
-    // proxy): no tcgen05 fence per unit.
-    if (!landed &&
-        !__all_sync(0xffffffffu, tc::mbar_try_wait(&ts.full[s], ph) || pipe_wait(p, ts, &ts.full[s], ph)))
-      break;
+    // The phase makes the stage's TMA bytes (or the decode's writes, fenced
+    // to the async proxy) visible to the MMA: no tcgen05 fence per unit.
+    const bool cd = unit_coded<FMT>(p, it);
+    uint64_t* fb = cd ? &ts.dfull[s] : &ts.full[s];
+    const uint32_t par = ((cd ? phc : phu) >> s) & 1u;
+    if (!landed && !__all_sync(0xffffffffu, tc::mbar_try_wait(fb, par) || pipe_wait(p, ts, fb, par))) break;
     // The next unit's stage, tested now: an mbarrier test takes ~200 cycles,
     // which then pass under this unit's MMA issue instead of idling the
     // tensor core between units.
     int s1 = s + 1;
-    uint32_t ph1 = ph;
-    if (s1 == S) { s1 = 0; ph1 ^= 1; }
-    const bool landed1 = n + 1 < nunits && tc::mbar_test(&ts.full[s1], ph1);
+    if (s1 == S) s1 = 0;
+    bool landed1 = false;
+    if (n + 1 < nunits) {
+      UnitIter nx = it;
+      nx.next();
+      const bool cd1 = unit_coded<FMT>(p, nx);
+      landed1 = tc::mbar_test(cd1 ? &ts.dfull[s1] : &ts.full[s1], ((cd1 ? phc : phu) >> s1) & 1u);
+    }
     int slot = it.ks - ks0;
     if (slot < 0) slot += KS;
     if (n == 0 && leader) tl_stamp_here(p, TL_MMA_FIRST);
@@ -708,9 +722,12 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
     }
     landed = __all_sync(0xffffffffu, landed1);
     if (seg_end) seg_open = false;
+    if (cd)
+      phc ^= 1u << s;
+    else
+      phu ^= 1u << s;
     it.next();
     s = s1;
-    ph = ph1;
   }
   if (leader) tc::mma_commit(&ts.mma_done);
   __syncwarp();
@@ -838,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     ts.dec_issued = 0;
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(&ts.full[s], 1);
+      tc::mbar_init(&ts.dfull[s], kConvWarps);
       tc::mbar_init(&ts.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -846,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     }
     for (int r = 0; r < p.rstages; ++r) {
       tc::mbar_init(&ts.rfull[r], 1);
-      tc::mbar_init(&ts.rempty[r], 1);
+      tc::mbar_init(&ts.rempty[r], kConvWarps);
     }
     tc::mbar_init(&ts.mma_done, 1);
     for (int s = 0; s < kOpMaxStages; ++s) tc::mbar_init(&ts.obar[s], 1);
