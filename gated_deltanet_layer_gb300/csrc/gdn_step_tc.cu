@@ -535,21 +535,26 @@ static __device__ __forceinline__ uint32_t e2m3x2_to_bf16(uint32_t c0, uint32_t 
 // One row's 64 MXFP6 codes (48 bytes: two 24-byte groups of 32 codes, code i
 // of a group at bits 6i..6i+5 little-endian, so code j of the row starts at
 // bit 6j) to eight 16-byte chunks of bf16 (chunk c: columns 8c..8c+7),
-// scaled by the groups' e8m0 scales.
-static __device__ __forceinline__ void decode_row_mxfp6(const uint8_t* src, const uint32_t (&sc)[2], uint8_t* dst,
-                                                        int swz) {
+// scaled by the groups' e8m0 scales, through a table of all 4096 code pairs
+// (entry c0 | c1 << 6 holds e2m3x2_to_bf16(c0, c1), built once per launch in
+// shared memory): per pair a funnel shift, a mask, a table load and the
+// scale. The table's loads are bank-conflicted at random, but they cost the
+// integer pipe, which bounds the decode, far less than the conversion.
+constexpr uint32_t kE2m3LutEntries = 4096;
+static __device__ __forceinline__ void decode_row_mxfp6_lut(const uint8_t* src, const uint32_t (&sc)[2],
+                                                            uint8_t* dst, int swz, const uint32_t* lut) {
   const uint4 q0 = reinterpret_cast<const uint4*>(src)[0], q1 = reinterpret_cast<const uint4*>(src)[1],
               q2 = reinterpret_cast<const uint4*>(src)[2];
-  const uint32_t w[12] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w};
+  const uint32_t w[13] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w, 0u};
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {  // chunk c: codes 8c..8c+7, bits 48c..48c+47 of the row
-    const int k = (3 * c) >> 1, off = (c & 1) * 16;
-    const unsigned long long bits = (((unsigned long long)w[k + 1] << 32) | w[k]) >> off;
+  for (int c = 0; c < 8; ++c) {  // chunk c: code pairs 4c..4c+3, the 12-bit field of pair j at bit 12j
     uint32_t o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      o[e] = mul_bf16x2(e2m3x2_to_bf16((uint32_t)(bits >> (12 * e)) & 63u, (uint32_t)(bits >> (12 * e + 6)) & 63u),
-                        sc[c >> 2]);
+    for (int e = 0; e < 4; ++e) {
+      const int b = 48 * c + 12 * e;
+      const uint32_t idx = __funnelshift_r(w[b >> 5], w[(b >> 5) + 1], b & 31) & (kE2m3LutEntries - 1);
+      o[e] = mul_bf16x2(lut[idx], sc[c >> 2]);
+    }
     *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -561,7 +566,8 @@ static __device__ __forceinline__ uint4 scale_block(const StepParams& p, const U
 }
 template <int FMT>
 static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared& ts, uint8_t* sW,
-                                                   const uint8_t* sR, int ub, int nunits, int prefill, int ci) {
+                                                   const uint8_t* sR, int ub, int nunits, int prefill, int ci,
+                                                   const uint32_t* lut) {
   UnitIter it(p, ub);
   RingPos pos;
   const uint64_t pol = tc::policy_evict_first();
@@ -631,7 +637,7 @@ static __device__ __forceinline__ void decode_loop(const StepParams& p, TcShared
       const uint32_t sc[2] = {e8m0_bf16x2(sword & 0xffu), e8m0_bf16x2((sword >> 8) & 0xffu)};
       uint8_t* dst = sW + (size_t)pos.s * kWBytes + ci * 128;
       if (FMT == kFmtMxfp6) {
-        decode_row_mxfp6(row, sc, dst, ci & 7);
+        decode_row_mxfp6_lut(row, sc, dst, ci & 7, lut);
       } else {
         const uint4 c0 = reinterpret_cast<const uint4*>(row)[0], c1 = reinterpret_cast<const uint4*>(row)[1];
         const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -841,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   uint8_t* sXq = sX + (size_t)p.xslots * kXBytes;                            // its MXFP4-quantised copy
   uint8_t* sPad = sX + (size_t)kWindows * p.xslots * kXBytes;                // read past the windows; scratch
   uint8_t* sWin = sPad + p.xpad;
+  uint32_t* sLut = reinterpret_cast<uint32_t*>(sWin + (size_t)p.xslots * kWinBytes);  // MXFP6 code-pair table
   const int tid = threadIdx.x, warp = tid >> 5, cta = blockIdx.x;
   // Without early weight reads nothing is read before the previous kernel in
   // the stream is done (the caller's kernel just before may write weights).
@@ -914,6 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   publish_norm_partials(p, sq, L);
   if (tid == 32) start_weight_stream<FMT>(p, ts, sW, sR, ub, first, issued);
   write_residual_out(p, sX);
+  if (FMT == kFmtMxfp6)  // the code-pair table, while the norm hand-off is in flight
+    for (uint32_t i = tid; i < kE2m3LutEntries; i += kThreads) sLut[i] = e2m3x2_to_bf16(i & 63u, i >> 6);
   if (!phase_wait_rstd(p, sm, L)) {
     if (tid == 32) land_prefill<FMT>(p, ts, ub, issued);  // let the weight tiles in flight land
     if (warp == 1) {
@@ -948,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
     else if (warp == 4 || (FMT == kFmtBf16 && (warp == 8 || warp == 12)))
       drain_loop<FMT == kFmtBf16 ? 3 : 1>(p, ts, ub, nunits, tmem, (warp / 4 - 1) * 32 + (tid & 31), L);
     else if (FMT != kFmtBf16 && conv_index(warp) >= 0)
-      decode_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, conv_index(warp) * 32 + (tid & 31));
+      decode_loop<FMT>(p, ts, sW, sR, ub, nunits, issued, conv_index(warp) * 32 + (tid & 31), sLut);
   }
   if (tid < p.num_tiles) sm.tiles[tid] = (unsigned char)tile_cnt;
   tc::tc_fence_before();
@@ -1011,8 +1020,8 @@ const void* tensor_core_kernel(bool has_res, bool state_bf16, int dk, int fmt, b
 // Dynamic shared memory of a launch: the bf16 weight ring, the code ring
 // (MXFP4 or MXFP6), the normed-input window (and with MXFP4 weights its
 // quantised copy) with the pad an M = 64 MMA reads past the last slice (also
-// the norm sums' scratch), the window's input-norm weights, and 1 KB of
-// alignment.
+// the norm sums' scratch), the window's input-norm weights, with MXFP6 the
+// code-pair table, and 1 KB of alignment.
 uint32_t tensor_core_xpad(int xslots) {
   const uint32_t sums = (uint32_t)(kMaxRows * xslots * 8 * sizeof(float));
   return sums > kXPadMin ? (sums + 127) / 128 * 128 : kXPadMin;
@@ -1020,7 +1029,7 @@ uint32_t tensor_core_xpad(int xslots) {
 size_t tensor_core_smem_bytes(int stages, int rstages, int xslots, int fmt) {
   const size_t rtile = fmt == kFmtMxfp6 ? code_tile_bytes<kFmtMxfp6>() : code_tile_bytes<kFmtMxfp4>();
   return (size_t)stages * kWBytes + (size_t)rstages * rtile + (size_t)(fmt == kFmtMxfp4 ? 2 : 1) * xslots * kXBytes +
-         tensor_core_xpad(xslots) + (size_t)xslots * kWinBytes + 1024;
+         tensor_core_xpad(xslots) + (size_t)xslots * kWinBytes + (fmt == kFmtMxfp6 ? kE2m3LutEntries * 4 : 0) + 1024;
 }
 size_t tensor_core_static_smem() { return sizeof(SmemPhases) + sizeof(SmemTask) + sizeof(TcShared); }
 int tensor_core_max_stages() { return kMaxStages; }
