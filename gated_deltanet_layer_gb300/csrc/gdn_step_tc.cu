@@ -100,6 +100,8 @@ struct TcShared {
   uint64_t mma_done;        // every MMA issued by the CTA done
   uint64_t obar[kOpMaxStages];  // out_proj: a stage's weight rows landed
   uint64_t sbar[3];             // recurrence: a state tile landed (one per buffer)
+  unsigned char seg_slot[kMaxSegs];  // the CTA's plan entries read late (drain, MMA), copied at kernel start
+  unsigned short ks_first;
   uint32_t tmem_base;
   int abort;
   int dec_issued;  // coded formats: units [0, dec_issued) passed by the decode warps (bf16 tiles issued)
@@ -672,7 +674,7 @@ static __device__ __forceinline__ void mma_loop(const StepParams& p, TcShared& t
                                                 uint8_t* sX, uint8_t* sXq, int ub, int nunits, uint32_t tmem) {
   // Stage and phase advance incrementally: a division per unit by the
   // runtime ring depth costs the loop more than the tensor core's own time.
-  const int ks0 = p.plan->ks_first[blockIdx.x], KS = p.ksteps, S = p.stages;
+  const int ks0 = ts.ks_first, KS = p.ksteps, S = p.stages;
   UnitIter it(p, ub);
   int seg = -1;
   bool seg_open = false;
@@ -767,7 +769,7 @@ static __device__ __forceinline__ void drain_loop(const StepParams& p, TcShared&
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     tc::tc_fence_after();
     unsigned long long* dst = p.proj_part +
-                              ((size_t)t * p.max_contrib + p.plan->seg_slot[blockIdx.x][seg]) * kMaxRows * kTileM +
+                              ((size_t)t * p.max_contrib + ts.seg_slot[seg]) * kMaxRows * kTileM +
                               (size_t)lane * kTileM;
 #pragma unroll 1
     for (int c = dw; c < kTileM / 32; c += kDrainWarps) {
@@ -853,6 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   // the stream is done (the caller's kernel just before may write weights).
   if (!p.early_weights) griddep_wait();
   const int ub = p.plan->unit_begin[cta], nunits = p.plan->unit_begin[cta + 1] - ub;
+  // The plan entries the drain and the MMA issuer read once the weight stream
+  // fills HBM (a cold global load then takes a microsecond): loaded now, with
+  // unit_begin, which the first weight tiles wait for anyway.
+  if (tid >= 64 && tid < 64 + kMaxSegs) ts.seg_slot[tid - 64] = p.plan->seg_slot[cta][tid - 64];
+  if (tid == 64 + kMaxSegs) ts.ks_first = p.plan->ks_first[cta];
 
   if (tid == 0) {
     tc::prefetch_tensormap(&p.tm_qkvz);
