@@ -28,7 +28,7 @@ constexpr int kMaxKHeads = 64;             // key heads of a layer (conv-group c
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
 constexpr uint32_t kStatusDeadline = 4;
 constexpr uint32_t kStatusIndex = 5;
-constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3;
+constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3, kWaitProj = 9;
 
 // in_proj_qkvz weight formats (the values of gdn_weight_format).
 constexpr int kFmtBf16 = 0, kFmtMxfp4 = 1, kFmtMxfp6 = 2;
@@ -47,6 +47,10 @@ struct WsCounters {
   unsigned long long pad0[15];
   unsigned long long xn_arrive;     // +1 per CTA once its normed columns are out (CUDA-core engine)
   unsigned long long pad1[15];
+  // +1 per CTA (tensor-core engine, a release) once every projection partial
+  // it writes is stored: at (L + 1) x grid, launch L's partials are final
+  unsigned long long proj_done;
+  unsigned long long pad3[15];
   unsigned int error;               // sticky error word
   unsigned int pad2[63];
   // +1 per recurrence task of (row, key head) once it has read the old q/k

@@ -6,8 +6,13 @@
 //     task j + 2's tile in while task j runs; the threads update a tile in
 //     place; a bulk copy takes it back out (task 0's tile was prefetched
 //     into L2 under the projection);
-//   * the projection partials of task j + 1 (and its old conv taps) are
-//     loaded while task j updates its state, and polled when j + 1 starts;
+//   * task 0's projection partials are polled as tagged words of the
+//     launch, so it starts as soon as its own tiles are done; task j + 1's
+//     (and its old conv taps) are loaded while task j updates its state,
+//     once every CTA has counted itself on the projection counter (a release
+//     after its last partial): they are then final and are read as plain f32
+//     values (the low halves of the tagged words), with half the registers
+//     and no tags to check;
 //   * the key-head group's counter of task j is read back at task j + 1, and
 //     the new q/k taps of task j (held in the registers of their threads)
 //     are written then if j was the group's last reader.
@@ -17,6 +22,8 @@
 // barriers; a wait that runs out stops the phase at the next barrier (the
 // error is recorded) after the copies in flight have landed.
 #pragma once
+
+#include <type_traits>
 
 #include "gdn_phases.cuh"
 #include "gdn_tc_ptx.cuh"
@@ -39,6 +46,7 @@ struct StagedTask {
 // The state slots of the launch's rows (read once per phase).
 struct StagedSlots {
   int idx[kMaxRows];
+  int go;  // every CTA's projection partials are stored
 };
 
 template <int DK, bool STATE_BF16>
@@ -60,11 +68,9 @@ __host__ __device__ constexpr size_t staged_recurrence_bytes() {
 // the last two warps.
 struct StagedLoads {
   static constexpr int kMaxSlots = 24;  // partials per tile (the plan's bound)
-  unsigned long long pw[kMaxSlots];
-  const unsigned long long* src;
+  uint32_t pv[kMaxSlots];    // the partials' f32 bits
   int nc;
-  unsigned long long baw[1];
-  const unsigned long long* ba_src;
+  uint32_t bav;              // b or a: this lane's slot
   int ba_nc;
   uint2 cwv;                 // conv weights of the channel
   __nv_bfloat16 tap[3];      // its old taps
@@ -152,11 +158,9 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     // task), so nothing of a task's loads stays live past its use
     ld.nc = 0;
     ld.ba_nc = 0;
-    ld.src = nullptr;
-    ld.ba_src = nullptr;
-    ld.baw[0] = 0ull;
+    ld.bav = 0u;
 #pragma unroll
-    for (int jj = 0; jj < kMaxSlots; ++jj) ld.pw[jj] = 0ull;
+    for (int jj = 0; jj < kMaxSlots; ++jj) ld.pv[jj] = 0u;
     ld.cwv = make_uint2(0u, 0u);
     ld.tap[0] = ld.tap[1] = ld.tap[2] = __float2bfloat16_rn(0.f);
     ld.A_log = 0.f;
@@ -164,16 +168,19 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     if (!row_is_live(p, slot)) return;
     ld.A_log = p.A_log[h];
     ld.dt_bias = p.dt_bias[h];
+    // a partial's f32 bits: the low half of its tagged word
+    auto ld_part = [](const unsigned long long* q) { return ld_relaxed_u32(reinterpret_cast<const unsigned*>(q)); };
     if (ba_warp) {  // first: these lanes also have an output of their own
-      ld.ba_src = part_src(proj_row(4 * DK + (warp - (kWarps - 2)), h, kh), w, ld.ba_nc) + (size_t)lane * kSlot;
-      if (lane < ld.ba_nc) ld.baw[0] = ld_tagged(ld.ba_src);
+      const unsigned long long* bsrc =
+          part_src(proj_row(4 * DK + (warp - (kWarps - 2)), h, kh), w, ld.ba_nc) + (size_t)lane * kSlot;
+      if (lane < ld.ba_nc) ld.bav = ld_part(bsrc);
     }
     if (tid < 4 * DK && !(tid < 2 * DK && same_qk(j))) {
       const int nr = proj_row(tid, h, kh);
-      ld.src = part_src(nr, w, ld.nc);
+      const unsigned long long* src = part_src(nr, w, ld.nc);
 #pragma unroll
       for (int jj = 0; jj < kMaxSlots; ++jj)
-        if (jj < ld.nc) ld.pw[jj] = ld_tagged(ld.src + (size_t)jj * kSlot);
+        if (jj < ld.nc) ld.pv[jj] = ld_part(src + (size_t)jj * kSlot);
       if (tid < 3 * DK) {
         const __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + nr) * 3;
         ld.tap[0] = cs[0];
@@ -192,93 +199,153 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     for (int j = 0; j < min(n, SL::kBufs); ++j)
       if (issue_state(j)) pending |= 1u << j;
   }
-  issue_inputs(0, true);
+  StagedSlots* sst = reinterpret_cast<StagedSlots*>(tb + 2);
+  bool ok = true;
   // timeline (test hook): stamps 16 + 4 j + k of the first four tasks
   auto stamp = [&](int j, int k) {
     if ((p.debug_flags & kDebugTimeline) && j < 4 && tid == 0) p.ctr->tl_cta[cta][TL_TASK + 4 * j + k] = globaltimer_ns();
   };
   const float gw = tid < DK ? bf16_to_f(p.gnorm_w[tid]) : 0.f;
-  bool ok = true;
+  // Task j's inputs (its row live): partial sums, conv update + SiLU, per-warp
+  // sums of squares into tb[j & 1], this thread's new q/k taps into c1, c2,
+  // pvq. Task 0 (TAGGED): its partials polled as tagged words of this launch,
+  // so it starts as soon as its own tiles are done; later tasks: loaded once
+  // the projection counter was seen complete, so read as plain f32 values.
+  struct TaggedLoads {
+    unsigned long long pw[kMaxSlots];
+    const unsigned long long* src;
+    unsigned long long baw[1];
+    const unsigned long long* ba_src;
+  } ld0;
+  float c1 = 0.f, c2 = 0.f, pvq = 0.f;    // this task's new q/k taps (threads < 2 dk)
+  float nt0 = 0.f, nt1 = 0.f, nt2 = 0.f;  // the previous task's
+  auto gather = [&](int j, auto tagged) {
+    constexpr bool TAGGED = decltype(tagged)::value;
+    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int slot = sidx[w];
+    StagedTask& T = tb[j & 1];
+    if (tid < 2 * DK && same_qk(j)) {
+      // q/k as the previous task had them (same values, so the same sums)
+      const StagedTask& P = tb[(j - 1) & 1];
+      const float y = tid < DK ? P.q[tid] : P.k[tid - DK];
+      if (tid < DK)
+        T.q[tid] = y;
+      else
+        T.k[tid - DK] = y;
+      c1 = nt0;
+      c2 = nt1;
+      pvq = nt2;
+      const float y2 = warp_sum(y * y);
+      if (lane == 0) T.red[warp] = y2;
+    } else if (tid < 4 * DK) {
+      const int i = tid;
+      float acc = 0.f;
+      if constexpr (TAGGED) {
+        if (!poll_tagged<kMaxSlots>(p, ld0.pw, ld0.src, kSlot, ld.nc, L, kWaitTile)) ok = false;
+        if (i == 0 && (p.debug_flags & kDebugTimeline)) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
+#pragma unroll
+        for (int jj = 0; jj < kMaxSlots; ++jj)
+          if (jj < ld.nc) acc += tagged_value(ld0.pw[jj]);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kMaxSlots; ++jj)
+          if (jj < ld.nc) acc += __uint_as_float(ld.pv[jj]);
+      }
+      const float pv = round_bf16(acc);
+      float y2 = 0.f;
+      if (i < 3 * DK) {
+        const float c0 = bf16_to_f(ld.tap[0]);
+        c1 = bf16_to_f(ld.tap[1]);
+        c2 = bf16_to_f(ld.tap[2]);
+        float y = bf16_lo(ld.cwv.x) * c0;
+        y = fmaf(bf16_hi(ld.cwv.x), c1, y);
+        y = fmaf(bf16_lo(ld.cwv.y), c2, y);
+        y = fmaf(bf16_hi(ld.cwv.y), pv, y);
+        y = silu_f(y);
+        if (i < DK) {
+          T.q[i] = y;
+        } else if (i < 2 * DK) {
+          T.k[i - DK] = y;
+        } else {
+          T.v[i - 2 * DK] = y;
+          __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + proj_row(i, h, kh)) * 3;  // own channel
+          cs[0] = __float2bfloat16_rn(c1);
+          cs[1] = __float2bfloat16_rn(c2);
+          cs[2] = __float2bfloat16_rn(pv);
+        }
+        if (i < 2 * DK) {
+          y2 = y * y;
+          pvq = pv;
+        }
+      } else {
+        T.z[i - 3 * DK] = pv;
+      }
+      if (warp < 2 * DK / 32) {
+        y2 = warp_sum(y2);
+        if (lane == 0) T.red[warp] = y2;
+      }
+    }
+    if (ba_warp) {
+      float v;
+      if constexpr (TAGGED) {
+        if (!poll_tagged<1>(p, ld0.baw, ld0.ba_src, 0, lane < ld.ba_nc ? 1 : 0, L, kWaitTile)) ok = false;
+        v = tagged_value(ld0.baw[0]);
+      } else {
+        v = __uint_as_float(ld.bav);
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kMaxSlots; ++jj) {  // slot order, as for the other outputs
+        const float x = __shfl_sync(0xffffffffu, v, jj);
+        if (jj < ld.ba_nc) acc += x;
+      }
+      if (lane == 0) T.ba[warp - (kWarps - 2)] = round_bf16(acc);
+    }
+  };
+  // task 0: its loads as tagged words (the non-partial ones into `ld`), then
+  // its inputs
+  issue_inputs(0, false);  // clears `ld`
+  {
+    const int w0 = t0 / p.Hv, h0 = t0 - w0 * p.Hv, kh0 = h0 / p.group;
+    const int slot0 = sidx[w0];
+    if (row_is_live(p, slot0)) {
+      ld.A_log = p.A_log[h0];
+      ld.dt_bias = p.dt_bias[h0];
+      if (ba_warp) {
+        ld0.ba_src = part_src(proj_row(4 * DK + (warp - (kWarps - 2)), h0, kh0), w0, ld.ba_nc) + (size_t)lane * kSlot;
+        ld0.baw[0] = lane < ld.ba_nc ? ld_tagged(ld0.ba_src) : 0ull;
+      }
+      if (tid < 4 * DK) {
+        const int nr = proj_row(tid, h0, kh0);
+        ld0.src = part_src(nr, w0, ld.nc);
+#pragma unroll
+        for (int jj = 0; jj < kMaxSlots; ++jj) ld0.pw[jj] = jj < ld.nc ? ld_tagged(ld0.src + (size_t)jj * kSlot) : 0ull;
+        if (tid < 3 * DK) {
+          const __nv_bfloat16* cs = p.conv_state + ((size_t)slot0 * p.C + nr) * 3;
+          ld.tap[0] = cs[0];
+          ld.tap[1] = cs[1];
+          ld.tap[2] = cs[2];
+          ld.cwv = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)nr * 4);
+        }
+      }
+      gather(0, std::true_type());
+    }
+  }
   unsigned int group_old = 0;  // thread 0: the previous task's group counter
   bool prev_live = false;
   int prev_slot = 0, prev_row = 0;
-  float nt0 = 0.f, nt1 = 0.f, nt2 = 0.f;  // the previous task's new q/k taps of this thread's channel
-  for (int j = 0; j < n; ++j) {
+  for (int j = 0; j < n && ok; ++j) {
     const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
     const int slot = sidx[w];
     const bool live = row_is_live(p, slot);
     StagedTask& T = tb[j & 1];
     __nv_bfloat16* core = p.core_out + (size_t)w * p.Hv * DK + (size_t)h * DK;
     const int b = j % SL::kBufs;  // the tile's buffer and its mbarrier
-    float c1 = 0.f, c2 = 0.f, pvq = 0.f;  // this task's new taps (threads < 2 dk)
+    if (j > 0) {  // (task 0's inputs were gathered before the loop)
+      c1 = c2 = pvq = 0.f;
+      if (live) gather(j, std::false_type());
+    }
     if (live) {
-      // ---- inputs: partial sums, conv update + SiLU, per-warp sums of squares
-      if (tid < 2 * DK && same_qk(j)) {
-        // q/k as the previous task had them (same values, so the same sums)
-        const StagedTask& P = tb[(j - 1) & 1];
-        const float y = tid < DK ? P.q[tid] : P.k[tid - DK];
-        if (tid < DK)
-          T.q[tid] = y;
-        else
-          T.k[tid - DK] = y;
-        c1 = nt0;
-        c2 = nt1;
-        pvq = nt2;
-        const float y2 = warp_sum(y * y);
-        if (lane == 0) T.red[warp] = y2;
-      } else if (tid < 4 * DK) {
-        const int i = tid;
-        if (!poll_tagged<kMaxSlots>(p, ld.pw, ld.src, kSlot, ld.nc, L, kWaitTile)) ok = false;
-        if (i == 0 && (p.debug_flags & kDebugTimeline) && j == 0) p.ctr->tl_cta[cta][TL_REC_WAITED] = globaltimer_ns();
-        float acc = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < kMaxSlots; ++jj)
-          if (jj < ld.nc) acc += tagged_value(ld.pw[jj]);
-        const float pv = round_bf16(acc);
-        float y2 = 0.f;
-        if (i < 3 * DK) {
-          const float c0 = bf16_to_f(ld.tap[0]);
-          c1 = bf16_to_f(ld.tap[1]);
-          c2 = bf16_to_f(ld.tap[2]);
-          float y = bf16_lo(ld.cwv.x) * c0;
-          y = fmaf(bf16_hi(ld.cwv.x), c1, y);
-          y = fmaf(bf16_lo(ld.cwv.y), c2, y);
-          y = fmaf(bf16_hi(ld.cwv.y), pv, y);
-          y = silu_f(y);
-          if (i < DK) {
-            T.q[i] = y;
-          } else if (i < 2 * DK) {
-            T.k[i - DK] = y;
-          } else {
-            T.v[i - 2 * DK] = y;
-            __nv_bfloat16* cs = p.conv_state + ((size_t)slot * p.C + proj_row(i, h, kh)) * 3;  // own channel
-            cs[0] = __float2bfloat16_rn(c1);
-            cs[1] = __float2bfloat16_rn(c2);
-            cs[2] = __float2bfloat16_rn(pv);
-          }
-          if (i < 2 * DK) {
-            y2 = y * y;
-            pvq = pv;
-          }
-        } else {
-          T.z[i - 3 * DK] = pv;
-        }
-        if (warp < 2 * DK / 32) {
-          y2 = warp_sum(y2);
-          if (lane == 0) T.red[warp] = y2;
-        }
-      }
-      if (ba_warp) {
-        if (!poll_tagged<1>(p, ld.baw, ld.ba_src, 0, lane < ld.ba_nc ? 1 : 0, L, kWaitTile)) ok = false;
-        const float v = tagged_value(ld.baw[0]);
-        float acc = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < kMaxSlots; ++jj) {  // slot order, as for the other outputs
-          const float x = __shfl_sync(0xffffffffu, v, jj);
-          if (jj < ld.ba_nc) acc += x;
-        }
-        if (lane == 0) T.ba[warp - (kWarps - 2)] = round_bf16(acc);
-      }
       stamp(j, 0);  // inputs in
       // ---- this task's state tile in shared memory (bounded wait)
       if (ok) {
@@ -317,6 +384,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
       if (live) group_old = atom_add_relaxed_u32(&p.ctr->conv_group[w][kh], 1u);
       if ((p.debug_flags & kDebugTimeline) && j == 0) p.ctr->tl_cta[cta][TL_REC_INPUTS] = globaltimer_ns();
     }
+    float inv_q = 0.f, inv_k = 0.f, eg = 0.f, beta = 0.f;
     if (live) {
       // ---- L2 norms of q and k, gates (the single-task phase's arithmetic)
       float sq = 0.f, sk = 0.f;
@@ -325,13 +393,26 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
         sq += T.red[i];
         sk += T.red[DK / 32 + i];
       }
-      const float inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
-      const float inv_k = 1.0f / sqrtf(sk + p.l2_eps);
+      inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
+      inv_k = 1.0f / sqrtf(sk + p.l2_eps);
       const float sp_in = T.ba[1] + bf16_to_f(ld.dt_bias);
       const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
       const float g = -expf(ld.A_log) * sp;
-      const float eg = expf(g);
-      const float beta = 1.0f / (1.0f + expf(-T.ba[0]));
+      eg = expf(g);
+      beta = 1.0f / (1.0f + expf(-T.ba[0]));
+    }
+    // the next task's inputs (this task's head constants are used above),
+    // while this one updates its state. From task 1 on they are read as
+    // plain values: first, every CTA's partials must be stored (the acquire,
+    // and the barrier after it, order the loads after them).
+    if (j == 0 && n > 1) {
+      if (tid == 0)
+        sst->go = wait_counter(p, &p.ctr->proj_done, (unsigned long long)(L + 1) * p.num_ctas, kWaitProj) ? 1 : 0;
+      __syncthreads();
+      if (!sst->go) ok = false;  // (the error is recorded; the loop ends after this task)
+    }
+    issue_inputs(j + 1, j + 1 < n && ok);
+    if (live) {
       uint8_t* sb = sbuf(j);  // each thread reads and writes only its own elements
       float4 k4[CH], q4[CH];  // this lane's chunks of k^ and q^
 #pragma unroll
@@ -391,8 +472,6 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
       }
     }
     stamp(j, 2);
-    // the next task's inputs, while this one finishes
-    issue_inputs(j + 1, j + 1 < n);
     tc::fence_proxy_async_smem();  // this thread's tile writes before the bulk copy out
     __syncthreads();  // S2: o, last and the updated tile complete
     stamp(j, 3);

@@ -970,6 +970,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   tc::tc_fence_before();
   __syncthreads();
   const bool aborted = ts.abort != 0;
+  // every partial of this CTA is stored (the drain's stores are ordered
+  // before this release by the barrier above)
+  if (!aborted && tid == 0) red_add_release_u64(&p.ctr->proj_done, 1ull);
   if (aborted && tid == 0)  // TMA in flight lands before exit
     land_issued<FMT>(p, ts, ub, issued_total, issued, *reinterpret_cast<volatile int*>(&ts.dec_issued));
   if (warp == 1) {
