@@ -40,13 +40,22 @@ struct StagedTask {
   alignas(16) float z[128];  // z (bf16 projection)
   alignas(16) float o[128];  // o = S q^
   float red[kWarps];         // per-warp sums of q^2 (warps 0 .. dk/32-1), then k^2
-  float ba[2];               // b, a (bf16 projections)
+  float eg, beta;            // the head's gates e^g and beta
   int last;                  // the previous task was its key-head group's last reader
 };
-// The state slots of the launch's rows (read once per phase).
+constexpr int kMaxStagedTasks = 64;  // (row, value head) tasks of one CTA the staged phase takes
+constexpr int kBulkTid = 128;        // the thread that issues and waits for the state tiles' bulk copies
+// A task's indices, worked out once per phase (no divisions in the loop).
+struct StagedTaskIdx {
+  short w, h, kh;      // row, value head, key head
+  unsigned char same;  // the same (row, key head) as the task before: same q/k
+  unsigned char pad;
+};
+// The state slots of the launch's rows and the CTA's tasks (once per phase).
 struct StagedSlots {
   int idx[kMaxRows];
   int go;  // every CTA's projection partials are stored
+  StagedTaskIdx task[kMaxStagedTasks];
 };
 
 template <int DK, bool STATE_BF16>
@@ -106,8 +115,14 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   const int n = t1 - t0;
   auto sbuf = [&](int j) { return ring + (size_t)(j % SL::kBufs) * SL::kStateBytes; };  // task j's tile
   StagedTask* tb = reinterpret_cast<StagedTask*>(ring + SL::kBufs * (size_t)SL::kStateBytes);
-  int* sidx = reinterpret_cast<StagedSlots*>(tb + 2)->idx;  // the rows' state slots
+  StagedSlots* sst = reinterpret_cast<StagedSlots*>(tb + 2);
+  int* sidx = sst->idx;  // the rows' state slots
   if (tid < p.rows) sidx[tid] = p.idx[tid];
+  if (tid < n) {  // task tid's indices
+    const int task = t0 + tid, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int pt = task - 1, pw = pt / p.Hv, pkh = (pt - pw * p.Hv) / p.group;
+    sst->task[tid] = StagedTaskIdx{(short)w, (short)h, (short)kh, (unsigned char)(tid > 0 && pw == w && pkh == kh), 0};
+  }
   __syncthreads();
   const bool ba_warp = warp >= kWarps - 2;
 
@@ -128,11 +143,11 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   auto state_src = [&](int slot, int h) {
     return reinterpret_cast<uint8_t*>(p.ssm_state) + ((size_t)slot * p.Hv + h) * SL::kStateBytes;
   };
-  // Thread 0: the bulk copy of task j's state tile into its buffer,
+  // The bulk thread: the bulk copy of task j's state tile into its buffer,
   // completing on that buffer's mbarrier. Returns whether one was issued
   // (not for a pad row).
   auto issue_state = [&](int j) -> bool {
-    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv;
+    const int w = sst->task[j].w, h = sst->task[j].h;
     const int slot = sidx[w];
     if (!row_is_live(p, slot)) return false;
     uint64_t* bar = &sbar[j % SL::kBufs];
@@ -142,17 +157,13 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   };
   // Task j reads the same q/k channels (row and key head) as task j - 1:
   // their conv + SiLU outputs are the previous task's, copied, not reloaded.
-  auto same_qk = [&](int j) {
-    if (j == 0) return false;
-    const int a = t0 + j - 1, b = t0 + j;
-    const int wa = a / p.Hv, wb = b / p.Hv;
-    return wa == wb && (a - wa * p.Hv) / p.group == (b - wb * p.Hv) / p.group;
-  };
+  auto same_qk = [&](int j) { return sst->task[j].same != 0; };
   // Every thread: issue its loads of task j's inputs (nothing for a pad row,
   // or when `real` is false: then the fields are only cleared).
   StagedLoads ld;
   auto issue_inputs = [&](int j, bool real) {
-    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int jj0 = real ? j : 0;
+    const int w = sst->task[jj0].w, h = sst->task[jj0].h, kh = sst->task[jj0].kh;
     const int slot = real ? sidx[w] : 0;
     // every field is assigned on every path (and the call made after every
     // task), so nothing of a task's loads stays live past its use
@@ -191,15 +202,15 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     }
   };
 
-  // bulk copies in flight into each buffer (thread 0) and the buffers'
-  // mbarrier phases (every thread)
+  // bulk copies in flight into each buffer (the bulk thread: its warp has no
+  // core row to write, so the copies stay off the path of the next task) and
+  // the buffers' mbarrier phases (every thread)
   uint32_t pending = 0, ph = 0;
-  if (tid == 0) {
+  if (tid == kBulkTid) {
     tc::fence_proxy_async_smem();  // the ring's earlier generic accesses before the copies
     for (int j = 0; j < min(n, SL::kBufs); ++j)
       if (issue_state(j)) pending |= 1u << j;
   }
-  StagedSlots* sst = reinterpret_cast<StagedSlots*>(tb + 2);
   bool ok = true;
   // timeline (test hook): stamps 16 + 4 j + k of the first four tasks
   auto stamp = [&](int j, int k) {
@@ -221,7 +232,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   float nt0 = 0.f, nt1 = 0.f, nt2 = 0.f;  // the previous task's
   auto gather = [&](int j, auto tagged) {
     constexpr bool TAGGED = decltype(tagged)::value;
-    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int w = sst->task[j].w, h = sst->task[j].h, kh = sst->task[j].kh;
     const int slot = sidx[w];
     StagedTask& T = tb[j & 1];
     if (tid < 2 * DK && same_qk(j)) {
@@ -299,14 +310,24 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
         const float x = __shfl_sync(0xffffffffu, v, jj);
         if (jj < ld.ba_nc) acc += x;
       }
-      if (lane == 0) T.ba[warp - (kWarps - 2)] = round_bf16(acc);
+      if (lane == 0) {  // the head's gates, once (the one-task phase's arithmetic)
+        const float x = round_bf16(acc);
+        if (warp == kWarps - 2) {
+          T.beta = 1.0f / (1.0f + expf(-x));  // b
+        } else {
+          const float sp_in = x + bf16_to_f(ld.dt_bias);  // a
+          const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
+          const float g = -expf(ld.A_log) * sp;
+          T.eg = expf(g);
+        }
+      }
     }
   };
   // task 0: its loads as tagged words (the non-partial ones into `ld`), then
   // its inputs
   issue_inputs(0, false);  // clears `ld`
   {
-    const int w0 = t0 / p.Hv, h0 = t0 - w0 * p.Hv, kh0 = h0 / p.group;
+    const int w0 = sst->task[0].w, h0 = sst->task[0].h, kh0 = sst->task[0].kh;
     const int slot0 = sidx[w0];
     if (row_is_live(p, slot0)) {
       ld.A_log = p.A_log[h0];
@@ -335,7 +356,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
   bool prev_live = false;
   int prev_slot = 0, prev_row = 0;
   for (int j = 0; j < n && ok; ++j) {
-    const int task = t0 + j, w = task / p.Hv, h = task - w * p.Hv, kh = h / p.group;
+    const int w = sst->task[j].w, h = sst->task[j].h, kh = sst->task[j].kh;
     const int slot = sidx[w];
     const bool live = row_is_live(p, slot);
     StagedTask& T = tb[j & 1];
@@ -366,7 +387,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
         }
         if (landed) {
           ph ^= 1u << b;  // this buffer's copy is consumed
-          if (tid == 0) pending &= ~(1u << b);
+          if (tid == kBulkTid) pending &= ~(1u << b);
         } else {
           ok = false;
         }
@@ -395,11 +416,8 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
       }
       inv_q = (1.0f / sqrtf(sq + p.l2_eps)) * p.q_scale;
       inv_k = 1.0f / sqrtf(sk + p.l2_eps);
-      const float sp_in = T.ba[1] + bf16_to_f(ld.dt_bias);
-      const float sp = sp_in > 20.f ? sp_in : log1pf(expf(sp_in));
-      const float g = -expf(ld.A_log) * sp;
-      eg = expf(g);
-      beta = 1.0f / (1.0f + expf(-T.ba[0]));
+      eg = T.eg;
+      beta = T.beta;
     }
     // the next task's inputs (this task's head constants are used above),
     // while this one updates its state. From task 1 on they are read as
@@ -475,7 +493,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     tc::fence_proxy_async_smem();  // this thread's tile writes before the bulk copy out
     __syncthreads();  // S2: o, last and the updated tile complete
     stamp(j, 3);
-    if (tid == 0) {
+    if (tid == kBulkTid) {
       // the tile back to its slot (an empty group for a pad row), then task
       // j + 2's tile into the buffer task j - 1's copy out has finished reading
       if (live) tc::bulk_store(state_src(slot, h), sbuf(j), SL::kStateBytes);
@@ -527,7 +545,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
       cs[1] = __float2bfloat16_rn(nt1);
       cs[2] = __float2bfloat16_rn(nt2);
     }
-  } else if (tid == 0) {
+  } else if (tid == kBulkTid) {
     // let the copies in flight land before the ring is reused or the CTA ends (bounded)
     for (int bb = 0; bb < SL::kBufs; ++bb) {
       if (!((pending >> bb) & 1u)) continue;
@@ -537,7 +555,7 @@ __device__ bool phase_recurrence_staged(const StepParams& p, uint8_t* ring, uint
     }
   }
   // the tiles' copies out complete (written to global memory, the ring free)
-  if (tid == 0) tc::bulk_wait_all();
+  if (tid == kBulkTid) tc::bulk_wait_all();
   // the buffers' generic accesses before any later copy into the ring
   tc::fence_proxy_async_smem();
   __syncthreads();

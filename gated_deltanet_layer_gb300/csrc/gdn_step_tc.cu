@@ -952,7 +952,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_step_tc_kernel(const __grid_c
   task_range(p, rt0, rt1);
   // two or more decode tasks: the staged recurrence, in the shared memory
   // the projection leaves
-  const bool staged = !MULTI && rt1 - rt0 >= 2 && p.dyn_free >= staged_recurrence_bytes<DK, STATE_BF16>();
+  const bool staged = !MULTI && rt1 - rt0 >= 2 && rt1 - rt0 <= kMaxStagedTasks &&
+                      p.dyn_free >= staged_recurrence_bytes<DK, STATE_BF16>();
   if (rt0 < rt1 && !staged) load_state<DK, STATE_BF16>(p, rt0, first_state);
   if (staged && tid == 0) prefetch_state_l2<DK, STATE_BF16>(p, rt0);  // its bulk copy reads L2
   int issued_total = issued;
