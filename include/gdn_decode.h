@@ -252,7 +252,8 @@ gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, cons
  * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
  * 3 projection tile, 4 a tensor-core pipeline stage, 6 the core rows before
  * out_proj, 7 an out_proj weight chunk, 8 a state tile's copy into shared
- * memory), 15..0 the CTA (deadline) or row
+ * memory, 9 every CTA's projection partials stored), 15..0 the CTA
+ * (deadline) or row
  * (index error). This is the host
  * side of the pages' failure design: every wait in the launch is bounded, a
  * CTA that gives up records which wait in a sticky failed word, and the host
