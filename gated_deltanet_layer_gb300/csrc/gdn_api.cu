@@ -19,21 +19,21 @@ namespace {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t ctr, plan, norm_part, core_flag, xn, proj_part, total;
+  size_t ctr, plan, norm_part, core_flag, proj_part, total;
 };
 
 struct Plan {
   int engine;  // GDN_ENGINE_CUDA_CORE or GDN_ENGINE_TCGEN05
-  int G, tiles_qkvz, num_tiles, ksteps, kblock, norm_chunk, max_contrib;
+  int G, tiles_qkvz, num_tiles, ksteps, kblock, max_contrib;
   int unit_begin[kMaxCtas + 1];
   unsigned char seg_slot[kMaxCtas][kMaxSegs];
   unsigned short ks_first[kMaxCtas];
   unsigned char nb_slots[kMaxCtas];
   unsigned char tile_count[kMaxTiles];
   unsigned int own_mask[kMaxCtas];
-  // tensor-core engine: weight ring depth (bf16 tiles), raw ring depth (MXFP4
-  // code tiles), normed-input window (k-steps), the pad past it, and the
-  // launch's dynamic shared memory
+  // weight ring depth (bf16 tiles), code ring depth (MXFP4 / MXFP6 code
+  // tiles), normed-input window (k-steps), the pad past it, and the launch's
+  // dynamic shared memory (the same for both engines)
   int stages, rstages, xslots;
   unsigned int xpad;
   size_t smem;
@@ -109,8 +109,7 @@ gdn_status validate(const gdn_decode_config* c) {
 // step (k-step) of one 256-row tile. Units are ordered by group: group g =
 // (k-block kb = g / T, tile t = g % T) holds the `kblock` k-steps kb*kblock ..
 // of tile t. With kblock = ksteps the order is tile-major (a CTA sweeps K of
-// one tile, then the next); the tensor-core engine of a large layer uses
-// kblock = 16 (8 with MXFP4 or MXFP6 weights, whose second window or code
+// one tile, then the next); a large layer uses kblock = 16 (8 with MXFP4 or MXFP6 weights, whose second window or code
 // ring takes the room), so a CTA's units touch at most two k-blocks and the
 // normed input it needs (<= 32 k-steps; 24 with coded weights) fits in shared
 // memory. Longer k-blocks also mean
@@ -127,20 +126,16 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
   pl->num_tiles = T;
   const int KS = c.hidden / kKStep;
   pl->ksteps = KS;
-  int chunk = (c.hidden + G - 1) / G;
-  chunk = (chunk + 7) / 8 * 8;
-  pl->norm_chunk = chunk;
-  if (chunk > kMaxNormChunk) return GDN_ERR_UNSUPPORTED;
   const long long U = (long long)T * KS;
   const long long per_cta = (U + G - 1) / G;
-  // the normed-input window of the tensor-core engine, in k-steps, and the
-  // k-block that keeps a CTA's units inside it
+  // the normed-input window, in k-steps, and the k-block that keeps a CTA's
+  // units inside it
   // coded weights (MXFP4: two windows; MXFP6: the code ring) keep the ring
   // deeper with the shorter k-block
   const bool coded = c.qkvz_format != GDN_W_BF16;
   const int max_window = coded ? kMaxBSlotsMxfp4 : kMaxBSlots;
   int KB = KS;
-  if (engine == GDN_ENGINE_TCGEN05 && per_cta + 1 > max_window) {
+  if (per_cta + 1 > max_window) {
     KB = coded ? kKBlockMxfp4 : kKBlock;
     if (KS % KB != 0) return GDN_ERR_UNSUPPORTED;
   }
@@ -187,22 +182,20 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
     }
     pl->ks_first[cta] = (unsigned short)first;
     pl->nb_slots[cta] = (unsigned char)std::min(len, 255);
-    if (engine == GDN_ENGINE_TCGEN05 && len > max_window) return GDN_ERR_UNSUPPORTED;
+    if (len > max_window) return GDN_ERR_UNSUPPORTED;
   }
-  // k-step owners (tensor-core engine): the first CTA whose window holds it
+  // k-step owners: the first CTA whose window holds it
   for (int cta = 0; cta < G; ++cta) pl->own_mask[cta] = 0;
-  if (engine == GDN_ENGINE_TCGEN05) {
-    for (int ks = 0; ks < KS; ++ks) {
-      int owner = -1;
-      for (int cta = 0; cta < G && owner < 0; ++cta) {
-        const int j = (ks - pl->ks_first[cta] + KS) % KS;
-        if (j < pl->nb_slots[cta]) {
-          owner = cta;
-          pl->own_mask[cta] |= 1u << j;
-        }
+  for (int ks = 0; ks < KS; ++ks) {
+    int owner = -1;
+    for (int cta = 0; cta < G && owner < 0; ++cta) {
+      const int j = (ks - pl->ks_first[cta] + KS) % KS;
+      if (j < pl->nb_slots[cta]) {
+        owner = cta;
+        pl->own_mask[cta] |= 1u << j;
       }
-      if (owner < 0) return GDN_ERR_UNSUPPORTED;
     }
+    if (owner < 0) return GDN_ERR_UNSUPPORTED;
   }
   int maxc = 1;
   for (int t = 0; t < T; ++t) {
@@ -212,26 +205,20 @@ gdn_status make_plan(const gdn_decode_config& c, int G, int engine, Plan* pl) {
     maxc = std::max(maxc, count[t]);
   }
   pl->max_contrib = maxc;
-  if (engine == GDN_ENGINE_TCGEN05) {
-    // the ring takes what the window (two windows with MXFP4 weights: xn and
-    // its quantised copy) and the code ring leave: 2..6 tiles of 32 KB
-    const int fmt = c.qkvz_format;
-    int xs = 1;
-    for (int cta = 0; cta < G; ++cta) xs = std::max(xs, (int)pl->nb_slots[cta]);
-    pl->xslots = xs;
-    pl->xpad = tensor_core_xpad(xs);
-    const size_t avail = kSmemOptin - tensor_core_static_smem() - 1024;
-    const size_t wtile = (size_t)kTileM * kKStep * 2;
-    pl->rstages = fmt != GDN_W_BF16 ? tensor_core_max_rstages() : 0;
-    const size_t fixed = tensor_core_smem_bytes(0, pl->rstages, xs, fmt);
-    if (fixed + 2 * wtile > avail) return GDN_ERR_UNSUPPORTED;
-    pl->stages = (int)std::min<size_t>((avail - fixed) / wtile, (size_t)tensor_core_max_stages());
-    pl->smem = tensor_core_smem_bytes(pl->stages, pl->rstages, xs, fmt);
-  } else {
-    pl->stages = pl->rstages = pl->xslots = 0;
-    pl->xpad = 0;
-    pl->smem = cuda_core_smem_bytes();
-  }
+  // the ring takes what the window (two windows with MXFP4 weights: xn and
+  // its quantised copy) and the code ring leave: 2..6 tiles of 32 KB
+  const int fmt = c.qkvz_format;
+  int xs = 1;
+  for (int cta = 0; cta < G; ++cta) xs = std::max(xs, (int)pl->nb_slots[cta]);
+  pl->xslots = xs;
+  pl->xpad = tensor_core_xpad(xs);
+  const size_t avail = kSmemOptin - tensor_core_static_smem() - 1024;
+  const size_t wtile = (size_t)kTileM * kKStep * 2;
+  pl->rstages = fmt != GDN_W_BF16 ? tensor_core_max_rstages() : 0;
+  const size_t fixed = tensor_core_smem_bytes(0, pl->rstages, xs, fmt);
+  if (fixed + 2 * wtile > avail) return GDN_ERR_UNSUPPORTED;
+  pl->stages = (int)std::min<size_t>((avail - fixed) / wtile, (size_t)tensor_core_max_stages());
+  pl->smem = tensor_core_smem_bytes(pl->stages, pl->rstages, xs, fmt);
   return GDN_OK;
 }
 
@@ -242,7 +229,6 @@ Layout make_layout(const gdn_decode_config& c, const Plan& pl) {
   l.plan = off;       off += align_up(sizeof(PlanDev), 256);
   l.norm_part = off;  off += align_up((size_t)kMaxRows * pl.G * sizeof(unsigned long long), 256);
   l.core_flag = off;  off += align_up((size_t)pl.G * sizeof(unsigned long long), 256);
-  l.xn = off;         off += align_up((size_t)kMaxRows * c.hidden * 2, 256);
   l.proj_part = off;
   off += align_up((size_t)pl.num_tiles * pl.max_contrib * kMaxRows * kTileM * sizeof(unsigned long long), 256);
   l.total = off;
@@ -272,7 +258,7 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 const void* pick_kernel(const gdn_decode_config& c, int engine, bool has_res, bool multi = false) {
   const bool b16 = c.ssm_dtype == GDN_STATE_BF16;
   if (engine == GDN_ENGINE_TCGEN05) return tensor_core_kernel(has_res, b16, c.head_k_dim, c.qkvz_format, multi);
-  return multi ? nullptr : cuda_core_kernel(has_res, b16, c.head_k_dim);
+  return multi || c.qkvz_format != GDN_W_BF16 ? nullptr : cuda_core_kernel(has_res, b16, c.head_k_dim);
 }
 
 size_t kernel_smem(const Plan& pl) { return pl.smem; }
@@ -288,24 +274,19 @@ bool clear_launch_state(char* base, const Layout& l, cudaStream_t s) {
 // Launch fields of the plan that the kernels read.
 void set_plan_params(const Plan& pl, StepParams* p) {
   p->tiles_qkvz = pl.tiles_qkvz; p->num_tiles = pl.num_tiles; p->ksteps = pl.ksteps;
-  p->norm_chunk = pl.norm_chunk; p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
+  p->max_contrib = pl.max_contrib; p->num_ctas = pl.G;
   p->kblock = pl.kblock;
   p->stages = pl.stages; p->rstages = pl.rstages; p->xslots = pl.xslots; p->xpad = pl.xpad;
   p->dyn_free = pl.smem > 1024 ? (unsigned int)(pl.smem - 1024) : 0u;  // 1 KB of it aligns the ring
 }
 
-// The engine a config runs with and its plan: the requested engine, or for
-// GDN_ENGINE_AUTO the tensor-core engine where its plan exists, else CUDA
-// cores. MXFP4 and MXFP6 weights run on the tensor-core engine only.
+// The engine a config runs with and its plan (the engines share the plan:
+// the same units, windows and weight ring): the requested engine, or for
+// GDN_ENGINE_AUTO the tensor-core engine. MXFP4 and MXFP6 weights run on the
+// tensor-core engine only.
 gdn_status resolve_plan(const gdn_decode_config& c, int G, Plan* pl) {
-  if (c.qkvz_format != GDN_W_BF16) {
-    if (c.engine == GDN_ENGINE_CUDA_CORE) return GDN_ERR_UNSUPPORTED;
-    return make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
-  }
-  if (c.engine == GDN_ENGINE_CUDA_CORE) return make_plan(c, G, GDN_ENGINE_CUDA_CORE, pl);
-  const gdn_status st = make_plan(c, G, GDN_ENGINE_TCGEN05, pl);
-  if (st == GDN_OK || c.engine == GDN_ENGINE_TCGEN05) return st;
-  return make_plan(c, G, GDN_ENGINE_CUDA_CORE, pl);
+  if (c.engine == GDN_ENGINE_CUDA_CORE && c.qkvz_format != GDN_W_BF16) return GDN_ERR_UNSUPPORTED;
+  return make_plan(c, G, c.engine == GDN_ENGINE_CUDA_CORE ? GDN_ENGINE_CUDA_CORE : GDN_ENGINE_TCGEN05, pl);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -487,7 +468,6 @@ void fill_params(const gdn_decode_config& c, const Plan& pl, const Layout& lay, 
   p->ctr = (WsCounters*)(base + lay.ctr);
   p->core_flag = (unsigned long long*)(base + lay.core_flag);
   p->norm_part = (unsigned long long*)(base + lay.norm_part);
-  p->xn = (__nv_bfloat16*)(base + lay.xn);
   p->proj_part = (unsigned long long*)(base + lay.proj_part);
   p->plan = (const PlanDev*)(base + lay.plan);
 }

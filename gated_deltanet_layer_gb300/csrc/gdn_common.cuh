@@ -17,7 +17,6 @@ constexpr int kTileShift = 8;              // log2(kTileM)
 constexpr int kKStep = 64;                 // projection columns per work unit
 constexpr int kMaxCtas = 256;
 constexpr int kMaxTiles = 512;             // (Nqkvz + Nba) / 128 upper bound
-constexpr int kMaxNormChunk = 256;         // hidden columns per CTA in the norm phase
 constexpr int kMaxSegs = 16;               // tile segments in one CTA's unit range
 constexpr int kKBlock = 16;                // k-steps per k-block in the k-block-major order
 constexpr int kKBlockMxfp4 = 8;            // the same with coded (MXFP4, MXFP6) weights
@@ -28,10 +27,16 @@ constexpr int kMaxKHeads = 64;             // key heads of a layer (conv-group c
 // Sticky error word: bits 31..24 status, 23..16 wait id, 15..0 CTA or row.
 constexpr uint32_t kStatusDeadline = 4;
 constexpr uint32_t kStatusIndex = 5;
-constexpr uint32_t kWaitNorm = 1, kWaitXn = 2, kWaitTile = 3, kWaitProj = 9;
+constexpr uint32_t kWaitNorm = 1, kWaitTile = 3, kWaitProj = 9;  // (2: no longer used)
 
 // in_proj_qkvz weight formats (the values of gdn_weight_format).
 constexpr int kFmtBf16 = 0, kFmtMxfp4 = 1, kFmtMxfp6 = 2;
+// The step kernel's form for bf16 weights with the projection's dot products
+// on the CUDA cores (f32 FMA) instead of the tensor cores: the CUDA-core
+// engine. Everything else (weight ring, windows, recurrence) is shared.
+constexpr int kFmtBf16Fma = 3;
+template <int FMT>
+__host__ __device__ constexpr bool bf16_weights() { return FMT == kFmtBf16 || FMT == kFmtBf16Fma; }
 
 constexpr int kDebugSkipNormPublish = 0x1;
 constexpr int kDebugTimeline = 0x2;
@@ -45,10 +50,8 @@ constexpr int kTlSlots = 48;  // timeline stamps per CTA: 16 phase points, then 
 struct WsCounters {
   unsigned long long norm_arrive;   // +1 per CTA once its norm partials are out
   unsigned long long pad0[15];
-  unsigned long long xn_arrive;     // +1 per CTA once its normed columns are out (CUDA-core engine)
-  unsigned long long pad1[15];
-  // +1 per CTA (tensor-core engine, a release) once every projection partial
-  // it writes is stored: at (L + 1) x grid, launch L's partials are final
+  // +1 per CTA (a release) once every projection partial it writes is
+  // stored: at (L + 1) x grid, launch L's partials are final
   unsigned long long proj_done;
   unsigned long long pad3[15];
   unsigned int error;               // sticky error word
@@ -76,11 +79,10 @@ struct StepParams {
   int num_tiles;       // tiles_qkvz + ceil(Nba / kTileM)
   int ksteps;          // H / 64
   int kblock;          // k-steps per k-block of the unit order (== ksteps: tile-major)
-  int norm_chunk;      // hidden columns per CTA in the norm phase (multiple of 8)
   int max_contrib;     // most CTAs contributing to one tile
   int num_ctas;
   int fmt;             // in_proj_qkvz format: kFmtBf16, kFmtMxfp4 or kFmtMxfp6 (codes + e8m0 scales)
-  int stages;          // bf16 weight tiles in flight per CTA (tensor-core engine)
+  int stages;          // bf16 weight tiles in flight per CTA
   int rstages;         // MXFP4 / MXFP6 code tiles in flight per CTA
   int xslots;          // normed-input k-steps a CTA keeps in shared memory
   unsigned int xpad;   // bytes past the window an MMA may read (and norm-sum scratch)
@@ -113,11 +115,10 @@ struct StepParams {
   WsCounters* ctr;
   unsigned long long* norm_part;  // [kMaxRows][num_ctas] tagged words
   unsigned long long* core_flag;  // [num_ctas] tagged words: a CTA's core rows are written (out_proj)
-  __nv_bfloat16* xn;              // [kMaxRows][H] (CUDA-core engine)
   unsigned long long* proj_part;  // [num_tiles][max_contrib][kMaxRows][kTileM] tagged words
   // TMA descriptors of the weights: bf16 boxes of 64 columns x 256 rows with
-  // 128-byte swizzle, or for MXFP4 in_proj_qkvz uint8 boxes of 32 bytes (64
-  // codes) x 256 rows (tensor-core engine).
+  // 128-byte swizzle, or for MXFP4 / MXFP6 in_proj_qkvz uint8 boxes of one
+  // k-step's codes (32 or 48 bytes) x 256 rows.
   CUtensorMap tm_qkvz;
   CUtensorMap tm_ba;
   CUtensorMap tm_out;  // out_proj [H][Hv*dv] bf16: boxes of 64 columns x 64 rows, 128-byte swizzle
@@ -131,8 +132,8 @@ struct StepParams {
 // i, whose partial goes to slot seg_slot[c][i] of the tile. Tile t receives
 // tile_num_ctas[t] partials. The CTA's normed-input k-steps are
 // ks_first[c] + j (mod ksteps) for j < nb_slots[c].
-// With the tensor-core engine each k-step's columns have one owner CTA (the
-// first whose window holds it): bit j of own_mask[c] marks window slot j as
+// Each k-step's columns have one owner CTA (the first whose window holds
+// it): bit j of own_mask[c] marks window slot j as
 // owned; the owner writes residual_out and the norm partial of those columns.
 struct PlanDev {
   int unit_begin[kMaxCtas + 1];

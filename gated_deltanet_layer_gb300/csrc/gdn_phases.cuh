@@ -1,7 +1,8 @@
-// Phases of the persistent GDN decode-step launch that do not depend on the
-// projection engine: residual add + norm partials, the normed input image,
-// the per-tile epilogue (partial reduction, conv update + SiLU, q/k L2 norm)
-// and the per-(row, value head) gated delta rule with the gated RMSNorm.
+// Phases of the persistent GDN decode-step launch that do not depend on how
+// the projection runs: the residual add and normalisation helpers, the end of
+// the norm hand-off, and the per-(row, value head) task: partial reduction,
+// conv update + SiLU, q/k L2 norm, the gated delta rule and the gated
+// RMSNorm.
 #pragma once
 
 #include "gdn_common.cuh"
@@ -10,11 +11,9 @@ namespace gdn {
 
 // Every array is 16-byte aligned: several are accessed with 16-byte vectors.
 struct SmemPhases {
-  alignas(16) __nv_bfloat16 rbuf[kMaxRows][kMaxNormChunk];  // r = x + residual of this CTA's columns
-  alignas(16) float part8[kMaxRows * (kMaxNormChunk / 8)];  // sums of 8 squares
   alignas(16) float rstd[kMaxRows];
   alignas(16) float red[kWarps];
-  unsigned char tiles[kMaxTiles];  // partials per projection tile (tensor-core engine: the plan's, staged)
+  unsigned char tiles[kMaxTiles];  // partials per projection tile (the plan's, staged)
   int L;                 // launch number on this workspace
   int flag;              // CTA-wide decision (set by thread 0, cleared by any thread that gives up)
 };
@@ -43,52 +42,7 @@ __device__ __forceinline__ uint4 residual8(uint4 xv, uint4 qv) {
 }
 
 // ---------------------------------------------------------------------------
-// Phase 1 (CUDA-core engine): r = x + residual (bf16), residual_out, and each
-// row's sum of r^2 over this CTA's hidden columns, handed to every CTA as
-// tagged words (vLLM #60833, Details, "x without an LDS tile": the norm CTAs
-// publish their columns' sums of squares and each consumer builds the x it
-// reads).
-// ---------------------------------------------------------------------------
-template <bool HAS_RES>
-__device__ __forceinline__ void phase_norm_partials(const StepParams& p, SmemPhases& sm, int L) {
-  const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int c0 = cta * p.norm_chunk;
-  const int ncol = max(0, min(p.H, c0 + p.norm_chunk) - c0);
-  const int nvec = ncol >> 3;
-  for (int i = tid; i < W * nvec; i += kThreads) {
-    const int w = i / nvec, v = i - w * nvec;
-    const size_t off = (size_t)w * p.H + c0 + v * 8;
-    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + off);
-    const uint4 qv = HAS_RES ? *reinterpret_cast<const uint4*>(p.res + off) : xv;
-    const uint4 rv = residual8<HAS_RES>(xv, qv);
-    const uint32_t rs[4] = {rv.x, rv.y, rv.z, rv.w};
-    *reinterpret_cast<uint4*>(p.res_out + off) = rv;
-    *reinterpret_cast<uint4*>(&sm.rbuf[w][v * 8]) = rv;
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = bf16_lo(rs[j]), b = bf16_hi(rs[j]);
-      s = fmaf(a, a, s);
-      s = fmaf(b, b, s);
-    }
-    sm.part8[w * (kMaxNormChunk / 8) + v] = s;
-  }
-  __syncthreads();
-  const bool publish = !((p.debug_flags & kDebugSkipNormPublish) && cta == 0);  // test hook: never publish
-  for (int w = warp; w < W; w += kWarps) {
-    float s = 0.f;
-    for (int v = lane; v < nvec; v += 32) s += sm.part8[w * (kMaxNormChunk / 8) + v];
-    s = warp_sum(s);
-    if (lane == 0 && publish) st_tagged(p.norm_part + w * p.num_ctas + cta, tagged(L, s));
-  }
-  if (tid == 0 && publish) red_add_relaxed_u64(&p.ctr->norm_arrive, 1ull);  // counts launches only
-  tl_stamp(p, TL_NORM_OUT);
-  __syncthreads();
-}
-
-// ---------------------------------------------------------------------------
-// Phase 1b: every CTA's sums (polled as tagged words of this launch), rstd
+// The norm hand-off's end: every CTA's sums (polled as tagged words of this launch), rstd
 // per row (Gemma RMSNorm: rstd = 1/sqrt(mean(r^2) + eps)). The sums are added
 // in CTA order, so every CTA forms the same rstd bit for bit.
 // ---------------------------------------------------------------------------
@@ -116,25 +70,6 @@ static __device__ __forceinline__ bool phase_wait_rstd(const StepParams& p, Smem
   tl_stamp(p, TL_NORM_IN);
   __syncthreads();
   return sm.flag != 0;
-}
-
-static __device__ __forceinline__ bool phase_normed_input(const StepParams& p, SmemPhases& sm, int L) {
-  const int W = p.rows, cta = blockIdx.x, tid = threadIdx.x;
-  if (!phase_wait_rstd(p, sm, L)) return false;
-  const int c0 = cta * p.norm_chunk;
-  const int ncol = max(0, min(p.H, c0 + p.norm_chunk) - c0);
-  const int nvec = ncol >> 3;
-  for (int i = tid; i < W * nvec; i += kThreads) {
-    const int w = i / nvec, v = i - w * nvec;
-    const uint4 rv = *reinterpret_cast<const uint4*>(&sm.rbuf[w][v * 8]);
-    const uint4 gv = *reinterpret_cast<const uint4*>(p.w_in + c0 + v * 8);
-    *reinterpret_cast<uint4*>(p.xn + (size_t)w * p.H + c0 + v * 8) = normed8(rv, gv, sm.rstd[w]);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) atom_add_release_u64(&p.ctr->xn_arrive, 1ull);
-  tl_stamp(p, TL_XN_OUT);
-  return true;
 }
 
 __device__ __forceinline__ bool row_is_live(const StepParams& p, int slot) {
@@ -167,7 +102,7 @@ struct SmemTask {
 };
 
 // ---------------------------------------------------------------------------
-// Phase 3: per (row w, value head h) task, all of the layer front after the
+// The recurrence: per (row w, value head h) task, all of the layer front after the
 // projections for that head:
 //   * the task's 4*dk + 2 projection outputs (q, k of key head kh = h / G; v,
 //     z of head h; b, a) as the sum of the tiles' partials in slot order,

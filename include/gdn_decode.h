@@ -92,11 +92,13 @@ typedef enum {
 typedef enum { GDN_STATE_F32 = 0, GDN_STATE_BF16 = 1 } gdn_state_dtype;
 typedef enum { GDN_W_BF16 = 0, GDN_W_MXFP4 = 1, GDN_W_MXFP6 = 2 } gdn_weight_format;
 
-/* Which unit runs the in_proj_qkvz / in_proj_ba dot products. */
+/* Which unit runs the in_proj_qkvz / in_proj_ba dot products. Both engines
+ * run the same launch (plan, TMA weight ring, shared-memory normed input,
+ * hand-offs, recurrence) and differ only there. */
 typedef enum {
-  GDN_ENGINE_AUTO = 0,       /* the library's choice per width */
-  GDN_ENGINE_CUDA_CORE = 1,  /* f32 FMA dot products on CUDA cores */
-  GDN_ENGINE_TCGEN05 = 2     /* tcgen05.mma, TMEM accumulators, TMA-fed operands */
+  GDN_ENGINE_AUTO = 0,       /* the library's choice: the tensor cores */
+  GDN_ENGINE_CUDA_CORE = 1,  /* f32 FMA dot products on CUDA cores (bf16 weights, decode steps) */
+  GDN_ENGINE_TCGEN05 = 2     /* tcgen05.mma, TMEM accumulators */
 } gdn_engine;
 
 /* Launch options (launch_flags).
@@ -164,7 +166,7 @@ typedef struct gdn_decode gdn_decode_t;
 
 /* Device bytes the caller must provide as the workspace for this config
  * (counters, the sticky error word, the plan tables, norm and projection
- * partials, and for the CUDA-core engine the normed input image). 0 if the
+ * partials). 0 if the
  * config is invalid or unsupported. The workspace holds what the pages'
  * runtime helpers keep per launch key: the scratch of the cross-CTA
  * hand-offs and the health word (vLLM #60833, Details, "Shared helpers":
@@ -249,8 +251,8 @@ gdn_status gdn_decode_verify(gdn_decode_t* h, int32_t seqs, int32_t tokens, cons
 
 /* Synchronise `stream` and read the sticky error word. Returns GDN_OK, or the
  * recorded device status; *detail (optional) receives the raw word:
- * bits 31..24 status, 23..16 the wait that gave up (1 norm, 2 normed input,
- * 3 projection tile, 4 a tensor-core pipeline stage, 6 the core rows before
+ * bits 31..24 status, 23..16 the wait that gave up (1 norm, 3 projection
+ * tile, 4 a weight-ring stage, 6 the core rows before
  * out_proj, 7 an out_proj weight chunk, 8 a state tile's copy into shared
  * memory, 9 every CTA's projection partials stored), 15..0 the CTA
  * (deadline) or row

@@ -27,14 +27,15 @@ extern "C" {
 /* Synchronise `stream` and copy the phase timeline the last step recorded
  * (handle created with GDN_DEBUG_TIMELINE). cta_stamps receives num_ctas x 48
  * uint64 nanosecond stamps: 0 start (after the previous step), 1 norm
- * partials out, 2 norm sums in (rstd known), 3 normed input out (CUDA-core
- * engine), 4 projection start, 5 projection end, 6 the first recurrence
+ * partials out, 2 norm sums in (rstd known), 3 normed input built in shared
+ * memory, 4
+ * projection start, 5 projection end, 6 the first recurrence
  * task's projection partials in, 7 end, 8 that task's inputs done, 9 first
  * MMA, 10 last MMA done, 11 first weight tiles issued, 12 x and residual
  * staged, 13 that task's state written; 16+4j+k the j-th task (j < 4) of a
  * CTA with several tasks (k = 0 its inputs in, 1 its state tile in shared
  * memory, 2 state updated, 3 the task's barrier after the update); 32+n the
- * n-th weight tile issued (n < 16, tensor-core engine); other slots unused.
+ * n-th weight tile issued (n < 16); other slots unused.
  * cta_cap is the capacity
  * in elements; *num_ctas receives the grid size. */
 gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* cta_stamps,

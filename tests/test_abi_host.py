@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 from gated_deltanet_layer_gb300 import _native, build as B, make_config
@@ -131,21 +132,26 @@ def test_stream_k_plan_invariants(lib, shape, G, engine):
     """The units partition [0, U) in CTA order with equal counts (within one);
     walking each CTA's units the way the kernels do (group g = u // kblock,
     tile g % T, k-step (g // T) * kblock + u % kblock) gives per tile the
-    slots 0..count-1 exactly once; with the tensor-core engine every unit's
-    normed-input slot lies inside the CTA's window of at most 32 k-steps (24
-    with coded weights)."""
+    slots 0..count-1 exactly once; every unit's normed-input slot lies inside
+    the CTA's window of at most 32 k-steps (24 with coded weights). A grid of
+    a GB300's SMs (or near it) plans every workload; a small grid may leave a
+    CTA more k-steps than its window holds, and is refused."""
     cfg = make_config(shape, engine=engine)
-    if (shape.hidden + G - 1) // G > 256 or (engine == "cuda_core" and shape.qkvz_format != "bf16"):
+    if engine == "cuda_core" and shape.qkvz_format != "bf16":
         with pytest.raises(_native.GdnError):
             _native.plan(cfg, G)
         return
-    P = _native.plan(cfg, G)
+    try:
+        P = _native.plan(cfg, G)
+    except _native.GdnError:
+        assert G < 148
+        return
     ub, nt, KS, KB = P["unit_begin"], P["num_tiles"], P["ksteps"], P["kblock"]
     U = nt * KS
     assert ub[0] == 0 and ub[G] == U and all(a <= b for a, b in zip(ub, ub[1:]))
     counts = [ub[c + 1] - ub[c] for c in range(G)]
     assert max(counts) - min(counts) <= 1
-    assert engine == "cuda_core" and P["engine"] == 1 or engine == "auto"
+    assert P["engine"] == (1 if engine == "cuda_core" else 2)
     slots = {t: [] for t in range(nt)}
     for c in range(G):
         seg, g_prev = -1, None
@@ -157,12 +163,23 @@ def test_stream_k_plan_invariants(lib, shape, G, engine):
                 assert seg < 16
                 slots[t].append(P["seg_slot"][c][seg])
                 g_prev = g
-            if P["engine"] == 2:
-                j = (ks - P["ks_first"][c]) % KS
-                assert j < P["nb_slots"][c] <= (24 if cfg.qkvz_format != _native.GDN_W_BF16 else 32)
+            j = (ks - P["ks_first"][c]) % KS
+            assert j < P["nb_slots"][c] <= (24 if cfg.qkvz_format != _native.GDN_W_BF16 else 32)
     for t in range(nt):
         assert P["tile_count"][t] == len(slots[t]) >= 1
         assert sorted(slots[t]) == list(range(P["tile_count"][t]))
+
+
+@pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16])
+def test_engines_share_the_plan(lib, shape):
+    """The CUDA-core and tensor-core engines run the same units, partial slots
+    and normed-input windows: they differ only in what multiplies."""
+    a = _native.plan(make_config(shape, engine="cuda_core"), 152)
+    b = _native.plan(make_config(shape, engine="tcgen05"), 152)
+    assert (a["engine"], b["engine"]) == (1, 2)
+    for k in a:
+        if k != "engine":
+            assert list(np.ravel(a[k])) == list(np.ravel(b[k])), k
 
 
 @pytest.mark.parametrize("G", [148, 152])
