@@ -90,7 +90,7 @@ def lib() -> ctypes.CDLL:
     u8p = ctypes.POINTER(ctypes.c_uint8)
     i32p = ctypes.POINTER(ctypes.c_int32)
     u16p = ctypes.POINTER(ctypes.c_uint16)
-    L.gdn_decode_plan.argtypes = [cfgp, i32, i32p, i32p, u8p, u16p, u8p, u8p, i32, i32p, i32p, i32p]
+    L.gdn_decode_plan.argtypes = [cfgp, i32, i32p, i32p, u8p, u16p, u8p, u32p, u8p, i32, i32p, i32p, i32p]
     L.gdn_decode_plan.restype = ctypes.c_int
     u64p = ctypes.POINTER(ctypes.c_uint64)
     L.gdn_decode_debug_timeline.argtypes = [vp, vp, u64p, i32, i32p]
@@ -110,16 +110,17 @@ def plan(cfg: Config, num_ctas: int) -> dict:
     seg = (ctypes.c_uint8 * (num_ctas * 16))()
     ksf = (ctypes.c_uint16 * num_ctas)()
     nbs = (ctypes.c_uint8 * num_ctas)()
+    own = (ctypes.c_uint32 * num_ctas)()
     cap = 4096
     tc = (ctypes.c_uint8 * cap)()
     nt, ks, kb = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-    st = L.gdn_decode_plan(ctypes.byref(cfg), num_ctas, ctypes.byref(eng), ub, seg, ksf, nbs, tc, cap,
+    st = L.gdn_decode_plan(ctypes.byref(cfg), num_ctas, ctypes.byref(eng), ub, seg, ksf, nbs, own, tc, cap,
                            ctypes.byref(nt), ctypes.byref(ks), ctypes.byref(kb))
     if st != GDN_OK:
         raise GdnError("gdn_decode_plan", st)
     return {"engine": eng.value, "unit_begin": list(ub),
             "seg_slot": [list(seg[c * 16:(c + 1) * 16]) for c in range(num_ctas)],
-            "ks_first": list(ksf), "nb_slots": list(nbs), "tile_count": list(tc[:nt.value]),
+            "ks_first": list(ksf), "nb_slots": list(nbs), "own_mask": list(own), "tile_count": list(tc[:nt.value]),
             "num_tiles": nt.value, "ksteps": ks.value, "kblock": kb.value}
 
 

@@ -756,12 +756,12 @@ gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* ct
 
 gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* engine,
                            int32_t* unit_begin, uint8_t* seg_slot, uint16_t* ks_first, uint8_t* nb_slots,
-                           uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
-                           int32_t* kblock) {
+                           uint32_t* own_mask, uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles,
+                           int32_t* ksteps, int32_t* kblock) {
   gdn_status st = validate(cfg);
   if (st != GDN_OK) return st;
   if (num_ctas < 1 || num_ctas > kMaxCtas || !engine || !unit_begin || !seg_slot || !ks_first ||
-      !nb_slots || !tile_count || !num_tiles || !ksteps || !kblock)
+      !nb_slots || !own_mask || !tile_count || !num_tiles || !ksteps || !kblock)
     return GDN_ERR_ARG;
   Plan* pl = new (std::nothrow) Plan;
   if (!pl) return GDN_ERR_ARG;
@@ -773,6 +773,7 @@ gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32
     memcpy(seg_slot, pl->seg_slot, (size_t)kMaxSegs * num_ctas);
     memcpy(ks_first, pl->ks_first, sizeof(uint16_t) * num_ctas);
     memcpy(nb_slots, pl->nb_slots, num_ctas);
+    memcpy(own_mask, pl->own_mask, sizeof(uint32_t) * num_ctas);
     memcpy(tile_count, pl->tile_count, pl->num_tiles);
     *num_tiles = pl->num_tiles;
     *ksteps = pl->ksteps;

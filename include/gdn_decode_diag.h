@@ -50,12 +50,14 @@ gdn_status gdn_decode_debug_timeline(gdn_decode_t* h, void* stream, uint64_t* ct
  * unit_begin[c+1])), seg_slot[num_ctas][16] (partial slot of the i-th group
  * CTA c touches), ks_first[num_ctas] and nb_slots[num_ctas] (CTA c keeps the
  * normed input of k-steps ks_first[c] + j mod ksteps, j < nb_slots[c]),
- * tile_count[*num_tiles] (partials per tile; capacity tile_cap), *ksteps and
- * *kblock. Errors as for gdn_decode_create. */
+ * own_mask[num_ctas] (bit j: CTA c owns window slot j, i.e. publishes its
+ * norm partial and writes residual_out of that k-step; each k-step has one
+ * owner), tile_count[*num_tiles] (partials per tile; capacity tile_cap),
+ * *ksteps and *kblock. Errors as for gdn_decode_create. */
 gdn_status gdn_decode_plan(const gdn_decode_config* cfg, int32_t num_ctas, int32_t* engine,
                            int32_t* unit_begin, uint8_t* seg_slot, uint16_t* ks_first, uint8_t* nb_slots,
-                           uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles, int32_t* ksteps,
-                           int32_t* kblock);
+                           uint32_t* own_mask, uint8_t* tile_count, int32_t tile_cap, int32_t* num_tiles,
+                           int32_t* ksteps, int32_t* kblock);
 
 #ifdef __cplusplus
 }

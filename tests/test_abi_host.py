@@ -170,6 +170,25 @@ def test_stream_k_plan_invariants(lib, shape, G, engine):
         assert sorted(slots[t]) == list(range(P["tile_count"][t]))
 
 
+@pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16, WL.DENSE_MXFP4, WL.DENSE_MXFP6])
+@pytest.mark.parametrize("G", [148, 152, 160])
+def test_every_k_step_has_one_owner(lib, shape, G):
+    """Each k-step is owned (its norm partial published, its residual_out
+    written) by exactly one CTA, the first whose window holds it."""
+    P = _native.plan(make_config(shape), G)
+    KS, own = P["ksteps"], P["own_mask"]
+    owners = [0] * KS
+    for c in range(G):
+        for j in range(32):
+            if (own[c] >> j) & 1:
+                assert j < P["nb_slots"][c]
+                owners[(P["ks_first"][c] + j) % KS] += 1
+    assert owners == [1] * KS
+    for ks in range(KS):
+        first = next(c for c in range(G) if (ks - P["ks_first"][c]) % KS < P["nb_slots"][c])
+        assert (own[first] >> ((ks - P["ks_first"][first]) % KS)) & 1
+
+
 @pytest.mark.parametrize("shape", [WL.TINY, WL.SHARD, WL.FULL, WL.SHARD_BF16])
 def test_engines_share_the_plan(lib, shape):
     """The CUDA-core and tensor-core engines run the same units, partial slots
